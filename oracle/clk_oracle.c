@@ -1,0 +1,396 @@
+/*
+ * CPU oracle of the context-lookup speculative decoding step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference that the
+ * CUDA path is compared against.  Only the test suite, the smoke entry point
+ * and the benchmark's CPU-baseline / reference leg may load or run it; the
+ * product library never links, loads or calls it, and it shares no code,
+ * header, table or constant with that library.
+ *
+ * It computes every step from the plain definitions in the pages
+ * (HyperQwen context-lookup article, section "lookup 草稿的原理：三步走"),
+ * slowly and without any index:
+ *
+ *   Step 1 (lookup): the most recent earlier occurrence of the longest
+ *     4..12-token suffix of the request's own history, overlap allowed, by a
+ *     full scan of the history; the tokens that follow it are the draft
+ *     (continued cyclically with period n - j past the end of history).
+ *   Step 2 (fusion): head slots 1..7 take the lookup draft if the match is at
+ *     least 8, or at least 6 with the draft model's first 2 proposals
+ *     agreeing; otherwise they keep the draft model's proposals.  Tail slots
+ *     8..15 take the lookup draft if the block is long and the match is at
+ *     least 4.
+ *   Step 3 (scheduler): the 16-token block is entered after 2 consecutive
+ *     steps that have a match able to fill the tail and follow a nearly full
+ *     step, and is left only after the match flag has stayed down for more
+ *     than 3 steps (sticky 3).
+ *   Greedy verification: row-wise argmax over the target logits (lowest
+ *     index on ties), the accepted prefix up to the first mismatch, plus the
+ *     target's own token at the first mismatch (the bonus token).
+ *
+ * Readings adopted where the pages are silent (each one a parameter):
+ *   - ties on length go to the most recent occurrence; length first;
+ *   - "nearly full" = accepted >= block - 1 - slack with slack 1;
+ *   - the scheduler flag is "k >= tail threshold" on this step's lookup, and
+ *     the near-full signal is the previous step's; at the first step there
+ *     is no previous step;
+ *   - unfilled slots hold the sentinel -1, which no argmax can equal.
+ *
+ * Argmax compares values as float32 (bf16 widens exactly): the first index
+ * of the maximum wins, +0 equals -0, and if a row holds a NaN the first NaN
+ * wins (torch.argmax convention).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <time.h>
+
+#define OR_SENT (-1)
+#define OR_BLOCK 16
+#define OR_SHORT 0
+#define OR_LONG 1
+
+typedef struct or_params {
+    int32_t min_k;           /* shortest suffix match that counts: 4 */
+    int32_t max_k;           /* longest suffix length searched: 12 */
+    int32_t head;            /* draft-model head slots: 7 */
+    int32_t tail;            /* lookup-only tail slots: 8 */
+    int32_t head_replace_k;  /* match that replaces the head outright: 8 */
+    int32_t head_agree_k;    /* match that replaces it if the drafter agrees: 6 */
+    int32_t head_agree_n;    /* leading proposals that must agree: 2 */
+    int32_t tail_k;          /* match that fills the tail: 4 */
+    int32_t enter_streak;    /* consecutive qualifying steps to enter: 2 */
+    int32_t sticky;          /* flag-down steps tolerated in the long block: 3 */
+    int32_t near_full_slack; /* rejected drafts still "nearly full": 1 */
+} or_params;
+
+typedef struct or_sched_state {
+    int32_t mode;
+    int32_t streak;
+    int32_t miss;
+    int32_t has_prev;
+} or_sched_state;
+
+/* Per-request counters, same order as the product's report. */
+typedef struct or_counters {
+    int64_t steps, hits, long_steps, drafted, accepted, emitted;
+    int64_t accept_hist[2][16];
+} or_counters;
+
+void or_params_default(or_params* p)
+{
+    p->min_k = 4;
+    p->max_k = 12;
+    p->head = 7;
+    p->tail = 8;
+    p->head_replace_k = 8;
+    p->head_agree_k = 6;
+    p->head_agree_n = 2;
+    p->tail_k = 4;
+    p->enter_streak = 2;
+    p->sticky = 3;
+    p->near_full_slack = 1;
+}
+
+/* Step 1: longest k in [min_k, max_k] and then largest j with
+ * h[j-k .. j-1] == h[n-k .. n-1] and k <= j <= n-1.  Full scan.
+ * Returns k (0 when nothing matches) and writes j (-1 when nothing matches). */
+int32_t or_lookup(const int32_t* h, int64_t n, int32_t min_k, int32_t max_k, int64_t* j_out)
+{
+    for (int32_t k = max_k; k >= min_k; --k) {
+        for (int64_t j = n - 1; j >= k; --j) {
+            int same = 1;
+            for (int32_t i = 0; i < k; ++i) {
+                if (h[j - k + i] != h[n - k + i]) {
+                    same = 0;
+                    break;
+                }
+            }
+            if (same) {
+                *j_out = j;
+                return k;
+            }
+        }
+    }
+    *j_out = -1;
+    return 0;
+}
+
+/* Step 1, copy: the 16 tokens that follow the match; past the end of the
+ * history the copy continues from its own start (period n - j). */
+void or_copy(const int32_t* h, int64_t n, int32_t k, int64_t j, int32_t* c)
+{
+    for (int64_t i = 0; i < OR_BLOCK; ++i) {
+        if (k == 0)
+            c[i] = OR_SENT;
+        else if (j + i < n)
+            c[i] = h[j + i];
+        else
+            c[i] = c[i - (n - j)];
+    }
+}
+
+/* Step 3: one scheduler step.  Returns the block length for this step. */
+int32_t or_sched(or_sched_state* s, int32_t k, int32_t prev_a, int32_t prev_L, const or_params* p)
+{
+    const int flag = k >= p->tail_k;
+    const int near_full = s->has_prev && prev_a >= prev_L - 1 - p->near_full_slack;
+    if (s->mode == OR_SHORT) {
+        if (flag && near_full)
+            s->streak += 1;
+        else
+            s->streak = 0;
+        if (s->streak >= p->enter_streak) {
+            s->mode = OR_LONG;
+            s->miss = 0;
+        }
+    } else {
+        if (flag)
+            s->miss = 0;
+        else
+            s->miss += 1;
+        if (s->miss > p->sticky) {
+            s->mode = OR_SHORT;
+            s->streak = 0;
+        }
+    }
+    s->has_prev = 1;
+    return s->mode == OR_LONG ? 1 + p->head + p->tail : 1 + p->head;
+}
+
+/* Step 2: the verify block.  blk[0] is the last committed token. */
+void or_fuse(int32_t last, const int32_t* c, int32_t k, const int32_t* m, int32_t L, const or_params* p,
+             int32_t* blk)
+{
+    int take_head = k >= p->head_replace_k;
+    if (!take_head && k >= p->head_agree_k) {
+        take_head = 1;
+        for (int32_t i = 0; i < p->head_agree_n; ++i)
+            if (c[i] != m[i]) take_head = 0;
+    }
+    const int fill_tail = (L == 1 + p->head + p->tail) && k >= p->tail_k;
+    for (int32_t i = 0; i < OR_BLOCK; ++i) blk[i] = OR_SENT;
+    blk[0] = last;
+    for (int32_t i = 0; i < p->head; ++i) blk[1 + i] = take_head ? c[i] : m[i];
+    for (int32_t i = 0; i < p->tail; ++i) blk[1 + p->head + i] = fill_tail ? c[p->head + i] : OR_SENT;
+}
+
+static float or_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Greedy verification, one row: first index of the maximum. */
+int32_t or_argmax_f32(const float* x, int64_t V)
+{
+    for (int64_t v = 0; v < V; ++v)
+        if (isnan(x[v])) return (int32_t)v;
+    int64_t best = 0;
+    for (int64_t v = 1; v < V; ++v)
+        if (x[v] > x[best]) best = v;
+    return (int32_t)best;
+}
+
+int32_t or_argmax_bf16(const uint16_t* x, int64_t V)
+{
+    for (int64_t v = 0; v < V; ++v)
+        if (isnan(or_bf16_value(x[v]))) return (int32_t)v;
+    int64_t best = 0;
+    float bv = or_bf16_value(x[0]);
+    for (int64_t v = 1; v < V; ++v) {
+        float f = or_bf16_value(x[v]);
+        if (f > bv) {
+            bv = f;
+            best = v;
+        }
+    }
+    return (int32_t)best;
+}
+
+/* Greedy verification: number of drafts accepted before the first mismatch. */
+int32_t or_accept(const int32_t* blk, const int32_t* g, int32_t L)
+{
+    int32_t a = 0;
+    while (a < L - 1 && blk[a + 1] == g[a]) a += 1;
+    return a;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Whole decode loop over a set of requests.                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Input providers (the synthetic target and draft model). */
+typedef void (*or_logits_fn)(const void* ctx, int32_t b, int64_t P, void* out_row);
+typedef void (*or_head_fn)(const void* ctx, int32_t b, int32_t t, int64_t n, int32_t* out);
+
+typedef struct or_run_args {
+    const or_params* params;
+    int32_t n_req;          /* requests simulated */
+    const int32_t* req_ids; /* their ids, passed to the providers */
+    const int32_t* prompt;  /* CSR over the n_req requests */
+    const int64_t* prompt_off;
+    int32_t steps;
+    int32_t V;
+    int32_t dtype; /* 0 = bf16, 1 = fp32 */
+    int32_t threads;
+    const void* gen_ctx;
+    or_logits_fn logits_fn;
+    or_head_fn head_fn;
+    /* outputs, indexed [t][i] or [t][i][16] with i the request's position */
+    int32_t* rec_k;
+    int32_t* rec_j;
+    int32_t* rec_L;
+    int32_t* rec_a;
+    int32_t* rec_c;
+    int32_t* rec_blk;
+    int32_t* rec_g;
+    int32_t* hist_out;          /* CSR by hist_off: capacity per request */
+    const int64_t* hist_off;    /* n_req + 1 */
+    int64_t* hist_len;          /* n_req */
+    or_counters* counters;      /* n_req */
+    /* timing (filled): nanoseconds in the method's own work and in the providers */
+    int64_t method_ns;
+    int64_t provider_ns;
+} or_run_args;
+
+typedef struct or_shared {
+    or_run_args* a;
+    int32_t next;
+    pthread_mutex_t mu;
+    int32_t error;
+} or_shared;
+
+static int64_t or_now_ns(void)
+{
+    struct timespec ts;
+    clock_gettime(CLOCK_MONOTONIC, &ts);
+    return (int64_t)ts.tv_sec * 1000000000LL + ts.tv_nsec;
+}
+
+static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t* provider_ns)
+{
+    const or_params* p = a->params;
+    const int32_t b = a->req_ids[i];
+    const int64_t n0 = a->prompt_off[i + 1] - a->prompt_off[i];
+    const int64_t cap = a->hist_off[i + 1] - a->hist_off[i];
+    const size_t esz = a->dtype == 0 ? 2 : 4;
+    int32_t* h = a->hist_out + a->hist_off[i];
+    void* row = malloc((size_t)a->V * esz);
+    if (!row) return -1;
+    if (n0 > cap || n0 < 1) {
+        free(row);
+        return -2;
+    }
+    memcpy(h, a->prompt + a->prompt_off[i], (size_t)n0 * sizeof(int32_t));
+    int64_t n = n0;
+    or_sched_state st = {OR_SHORT, 0, 0, 0};
+    or_counters* cnt = &a->counters[i];
+    memset(cnt, 0, sizeof *cnt);
+    int32_t prev_a = 0, prev_L = 0;
+    const int32_t long_L = 1 + p->head + p->tail;
+    int rc = 0;
+
+    const int64_t start_ns = or_now_ns();
+    int64_t prov = 0;
+    for (int32_t t = 0; t < a->steps; ++t) {
+        int32_t c[OR_BLOCK], m[OR_BLOCK], blk[OR_BLOCK], g[OR_BLOCK];
+        int64_t j;
+        int32_t k = or_lookup(h, n, p->min_k, p->max_k, &j);
+        or_copy(h, n, k, j, c);
+        int32_t L = or_sched(&st, k, prev_a, prev_L, p);
+        int64_t u0 = or_now_ns();
+        a->head_fn(a->gen_ctx, b, t, n, m);
+        prov += or_now_ns() - u0;
+        or_fuse(h[n - 1], c, k, m, L, p, blk);
+        for (int32_t r = 0; r < OR_BLOCK; ++r) g[r] = OR_SENT;
+        for (int32_t r = 0; r < L; ++r) {
+            u0 = or_now_ns();
+            a->logits_fn(a->gen_ctx, b, n + r, row);
+            prov += or_now_ns() - u0;
+            g[r] = a->dtype == 0 ? or_argmax_bf16((const uint16_t*)row, a->V) : or_argmax_f32((const float*)row, a->V);
+        }
+        int32_t acc = or_accept(blk, g, L);
+        if (n + acc + 1 > cap) {
+            rc = -2;
+            break;
+        }
+        for (int32_t r = 0; r <= acc; ++r) h[n + r] = g[r];
+        n += acc + 1;
+        cnt->steps += 1;
+        cnt->hits += (k >= p->min_k);
+        cnt->long_steps += (L == long_L);
+        cnt->drafted += p->head + ((L == long_L && k >= p->tail_k) ? p->tail : 0);
+        cnt->accepted += acc;
+        cnt->emitted += acc + 1;
+        cnt->accept_hist[L == long_L][acc] += 1;
+        prev_a = acc;
+        prev_L = L;
+
+        const int64_t o = (int64_t)t * a->n_req + i;
+        a->rec_k[o] = k;
+        a->rec_j[o] = (int32_t)j;
+        a->rec_L[o] = L;
+        a->rec_a[o] = acc;
+        memcpy(a->rec_c + o * OR_BLOCK, c, sizeof c);
+        memcpy(a->rec_blk + o * OR_BLOCK, blk, sizeof blk);
+        memcpy(a->rec_g + o * OR_BLOCK, g, sizeof g);
+    }
+    *provider_ns += prov;
+    *method_ns += (or_now_ns() - start_ns) - prov;
+    a->hist_len[i] = n;
+    free(row);
+    return rc;
+}
+
+static void* or_worker(void* arg)
+{
+    or_shared* sh = (or_shared*)arg;
+    int64_t meth = 0, prov = 0;
+    for (;;) {
+        pthread_mutex_lock(&sh->mu);
+        int32_t i = sh->next++;
+        pthread_mutex_unlock(&sh->mu);
+        if (i >= sh->a->n_req) break;
+        int rc = or_run_request(sh->a, i, &meth, &prov);
+        if (rc != 0) {
+            pthread_mutex_lock(&sh->mu);
+            if (sh->error == 0) sh->error = rc;
+            pthread_mutex_unlock(&sh->mu);
+        }
+    }
+    pthread_mutex_lock(&sh->mu);
+    sh->a->method_ns += meth;
+    sh->a->provider_ns += prov;
+    pthread_mutex_unlock(&sh->mu);
+    return NULL;
+}
+
+/* Runs the decode loop for every request, `threads` requests at a time.
+ * Returns 0, -1 (out of memory) or -2 (history capacity). */
+int or_run(or_run_args* a)
+{
+    or_shared sh;
+    sh.a = a;
+    sh.next = 0;
+    sh.error = 0;
+    a->method_ns = 0;
+    a->provider_ns = 0;
+    pthread_mutex_init(&sh.mu, NULL);
+    int nt = a->threads < 1 ? 1 : a->threads;
+    if (nt > a->n_req) nt = a->n_req < 1 ? 1 : a->n_req;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!th) return -1;
+    for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, or_worker, &sh);
+    for (int i = 0; i < nt; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&sh.mu);
+    return sh.error;
+}
+
+size_t or_counters_size(void) { return sizeof(or_counters); }
+size_t or_run_args_size(void) { return sizeof(or_run_args); }
