@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of the context-lookup speculative decoding hot path on GB300.
+
+One step = one pass of the whole hot path over the batch: proposal (suffix
+match + LZ77 copy), scheduler, fusion, greedy verification over the target
+logits, and the commit of the emitted tokens into histories and index.  It
+runs as the two fused launches of ``Step`` (propose_fuse_sched, then
+verify_append).
+
+Workload (default): the mixed serving batch, B=64, prompts U{2,000..32,000}
+Zipf(1.1) tokens over V=248,320, half copy-heavy and half chat-like, bf16
+logits [64, 16, 248320] with the +8 ground-truth boost; 8 warm-up steps and
+504 timed steps = the workload's 512 steps.  Every timed step reads logits
+generated beforehand into their own HBM buffers (inputs resident, larger
+than L2, so nothing is served from a previous step's L2 lines).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "spec steps/s and accepted tok/s (1 GB300), % of HBM roofline, vs CPU oracle"
+UNIT = "spec steps/s"
+CONFIG_NAMES = {"0": "tiny B=1 V=1024 fp32", "1": "restatement B=1 L=25000 V=248320 bf16",
+                "2": "mixed serving batch B=64 L=2k-32k V=248320 bf16",
+                "3": "periodic B=16 L=8192 V=32000 bf16", "4a": "long context B=8 L=262144 V=248320 bf16",
+                "4b": "index stress B=256 L=4096 V=248320 bf16"}
+# Lookup-side bytes per request per step that the method must move (besides
+# the logits): suffix 48, index probes 9x8, one match check 48, copy 64,
+# head 28, previous a/L 8, block+draft writes 128, k/j/L 12 (proposal
+# launch); block read 64, argmax/out_tok writes 128, a/emitted 8, history
+# append 64, index inserts 16 x 9 x 16 (verify launch).
+LOOKUP_BYTES_PER_REQ = 48 + 72 + 48 + 64 + 28 + 8 + 128 + 12 + 64 + 128 + 8 + 64 + 16 * 9 * 16
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _verify_sources_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("clk_verify.cu", "clk_device.cuh"):
+        with open(os.path.join(ROOT, "context_lookup_speculative_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """dram read+write bytes per verify launch from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "verify_greedy_cfg2_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") != _verify_sources_hash():
+            return None
+        return float(d["dram_bytes_per_launch_full_size"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), util=float(f[4]),
+                                 hw=f[6], hwt=f[7], swt=f[8], pcap=f[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["util"] > 0] or rows
+        sm = sorted(r["sm"] for r in busy)
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                          ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in busy):
+                reasons.append(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r["smax"] for r in rows), "reasons": reasons,
+                "samples": len(busy)}
+
+
+def _dist():
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local, dist
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank serves its own batch of the same recipe (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value: float, dist, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, world, rank, local, dist):
+    import numpy as np
+    import torch
+
+    import context_lookup_speculative_gb300 as clk
+    import workload as wl
+    from workload import drive
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    clk.lib()
+    w = wl.make(args.config, seed=shard_seed(int(wl.DEFAULT_SEED[args.config]), rank))
+    W, K = args.warmup, args.steps
+    assert W + K <= w.steps, f"warmup + steps must be <= {w.steps} for this workload"
+    B, V = w.B, w.V
+    params = clk.Params.default()
+    stream = torch.cuda.current_stream(device)
+
+    # Lookup state; the prompt ingestion (index build) is timed on its own.
+    lk, slots = drive.make_lookup(w, params, device=device)
+    ptok, poff = w.prompt_csr()
+    d_ptok, d_poff = torch.from_numpy(ptok).to(device), torch.from_numpy(poff).to(device)
+    gen = wl.DevGen(w, device=device)
+    st = clk.Step(lk, slots)
+    head = torch.zeros((B, wl.HEAD), dtype=torch.int32, device=device)
+    assert params.head == wl.HEAD
+    logits = gen.alloc_logits()
+
+    def reinit():
+        clk.lookup_init(lk, slots, d_ptok, d_poff)
+        gen.reset()
+        for t_ in (st.accept, st.length):
+            t_.zero_()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    clk.lookup_init(lk, slots, d_ptok, d_poff)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    index_build_ms = e0.elapsed_time(e1)
+
+    # Dry run: the positions every step starts from (the path is deterministic).
+    reinit()
+    pos_hist = torch.zeros((W + K + 1, B), dtype=torch.int64, device=device)
+    for t in range(W + K):
+        pos_hist[t].copy_(gen.pos)
+        gen.head(t, head)
+        st.pre(head)
+        gen.logits(logits)
+        st.post(logits)
+        gen.advance(st.emitted)
+    pos_hist[W + K].copy_(gen.pos)
+    torch.cuda.synchronize()
+
+    # Warm-up steps (untimed), from the reset state.
+    reinit()
+    for t in range(W):
+        gen.head(t, head)
+        st.pre(head)
+        gen.logits(logits)
+        st.post(logits)
+        gen.advance(st.emitted)
+    torch.cuda.synchronize()
+    c_before = lk.counters(-1)
+    del logits
+
+    # Timed steps in chunks whose inputs are generated beforehand into HBM.
+    per_step = B * 16 * V * (2 if w.dtype == wl.BF16 else 4)
+    chunk = max(1, min(K, int(args.input_gb * 2 ** 30 // per_step)))
+    heads = torch.zeros((chunk, B, wl.HEAD), dtype=torch.int32, device=device)
+    bufs = torch.empty((chunk, B, 16, V), dtype=gen.torch_dtype(), device=device)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    total_ms, verify_ms, pre_ms = 0.0, 0.0, 0.0
+    launches = 0
+    t = W
+    while t < W + K:
+        n = min(chunk, W + K - t)
+        for i in range(n):
+            gen.head(t + i, heads[i], pos=pos_hist[t + i])
+            gen.logits(bufs[i], pos=pos_hist[t + i])
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n + 1)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(n):
+            ev[2 * i].record(stream)
+            st.pre(heads[i])
+            ev[2 * i + 1].record(stream)
+            st.post(bufs[i])
+            launches += 2
+        ev[2 * n].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        total_ms += start.elapsed_time(end)
+        for i in range(n):
+            pre_ms += ev[2 * i].elapsed_time(ev[2 * i + 1])
+            verify_ms += ev[2 * i + 1].elapsed_time(ev[2 * i + 2])
+        t += n
+    clocks.stop()
+    c_after = lk.counters(-1)
+    status = lk.status()
+    gen.pos.copy_(pos_hist[W + K])  # the generator did not advance in the timed loop
+    # Determinism check: the timed steps ended where the dry run did.
+    if status[0] != 0:
+        raise RuntimeError(f"device status after the timed steps: {status}")
+    hist_lens = torch.tensor([lk.slot_info(int(s))["n"] for s in slots.tolist()], dtype=torch.int64, device=device)
+    if not torch.equal(hist_lens, pos_hist[W + K]):
+        raise RuntimeError("timed steps diverged from the dry run")
+    del bufs
+
+    total_s = max_over_ranks(total_ms * 1e-3, dist, world, device)
+    dc = {k: c_after[k] - c_before[k] for k in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")}
+    rows = 8 * dc["steps"] + (params.long_len - params.short_len) * dc["long_steps"]
+    esz = 2 if w.dtype == wl.BF16 else 4
+    verify_bytes = rows * V * esz                       # logits rows read, all timed steps
+    path_bytes = verify_bytes + LOOKUP_BYTES_PER_REQ * B * K
+    peak, peak_kind = _peaks()
+    verify_gbs = verify_bytes / (verify_ms * 1e-3) / 1e9
+    path_gbs = path_bytes / (total_ms * 1e-3) / 1e9
+    traffic = _traffic_per_launch()
+
+    e2e = run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device) if (rank == 0 and not args.no_e2e) else None
+    cpu = run_cpu_baseline(args, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    steps_s = world * K / total_s
+    out = {
+        "metric": METRIC, "value": round(steps_s, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(total_s * 1e3 / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}, {W} warm-up + {K} timed of "
+                               f"{w.steps} steps", "batch": B, "vocab": V, "block": "8 or 16",
+                   "l2": "inputs larger than L2: every step reads its own pre-generated logits",
+                   "parallelism": f"replicas x{world} (independent request batches)"},
+        "tokens": {"accepted_tok_s": round(world * dc["accepted"] / total_s, 1),
+                   "drafted_tok_s": round(world * dc["drafted"] / total_s, 1),
+                   "emitted_tok_s": round(world * dc["emitted"] / total_s, 1),
+                   "emitted_per_request_step": round(dc["emitted"] / max(1, dc["steps"]), 4),
+                   "accepted_per_request_step": round(dc["accepted"] / max(1, dc["steps"]), 4),
+                   "long_block_share": round(dc["long_steps"] / max(1, dc["steps"]), 4)},
+        "path": {"bytes_per_step": int(path_bytes // K), "verify_bytes_per_step": int(verify_bytes // K),
+                 "achieved_gbs": round(path_gbs, 1), "frac": round(path_gbs / peak, 4),
+                 "propose_fuse_sched_us_per_step": round(pre_ms * 1e3 / K, 3),
+                 "verify_append_us_per_step": round(verify_ms * 1e3 / K, 3),
+                 "index_build_ms": round(index_build_ms, 3)},
+        "roofline": {"bound": "hbm", "kernel": "verify_append (k_verify)", "achieved": round(verify_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(verify_gbs / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(verify_bytes // K)},
+        "clocks": clocks.summary(),
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return out
+
+
+def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
+    """Same metric through the public API with host buffers: each step copies
+    its head proposals and logits from pinned host memory to the device, runs
+    the two launches and reads back the emitted tokens and counts."""
+    import torch
+
+    import context_lookup_speculative_gb300 as clk
+    import workload as wl
+    from workload import drive
+
+    W = args.warmup
+    n = min(args.steps, args.e2e_steps)
+    B, V = w.B, w.V
+    lk, slots = drive.make_lookup(w, params, device=device)
+    gen = wl.DevGen(w, device=device)
+    st = clk.Step(lk, slots)
+    head = torch.zeros((B, wl.HEAD), dtype=torch.int32, device=device)
+    dl = gen.alloc_logits()
+    for t in range(W):
+        gen.head(t, head)
+        st.pre(head)
+        gen.logits(dl)
+        st.post(dl)
+        gen.advance(st.emitted)
+    # host copies of the next n steps' inputs (pinned)
+    h_heads = torch.empty((n, B, wl.HEAD), dtype=torch.int32, pin_memory=True)
+    h_logits = torch.empty((n, B, 16, V), dtype=gen.torch_dtype(), pin_memory=True)
+    for i in range(n):
+        gen.head(W + i, head, pos=pos_hist[W + i])
+        gen.logits(dl, pos=pos_hist[W + i])
+        h_heads[i].copy_(head)
+        h_logits[i].copy_(dl)
+    h_out = torch.empty((n, B, 16), dtype=torch.int32, pin_memory=True)
+    h_em = torch.empty((n, B), dtype=torch.int32, pin_memory=True)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record(stream)
+    for i in range(n):
+        head.copy_(h_heads[i], non_blocking=True)
+        dl.copy_(h_logits[i], non_blocking=True)
+        st.pre(head)
+        st.post(dl)
+        h_out[i].copy_(st.out_tok, non_blocking=True)
+        h_em[i].copy_(st.emitted, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = start.elapsed_time(end)
+    bi = B * wl.HEAD * 4 + B * 16 * V * dl.element_size()
+    bo = B * 16 * 4 + B * 4
+    return {"value": round(n / (ms * 1e-3), 2), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": n, "wall_s": round(wall, 4),
+            "note": "pinned host logits [B,16,V] copied in every step; the copy dominates"}
+
+
+def run_cpu_baseline(args, w):
+    """The oracle as it stands, on this host's cores, over a bounded sample:
+    all requests of the workload for the first `cpu_steps` steps."""
+    import oracle
+
+    steps = min(args.cpu_steps, w.steps)
+    threads = os.cpu_count() or 1
+    res = oracle.run(w, steps=steps, threads=threads)
+    used = min(threads, w.B)
+    per_thread = res.method_s / used
+    return {"value": round(steps / per_thread, 3), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{w.B} requests x first {steps} steps of the same workload; full-scan lookup, copy, "
+                      f"scheduler, fusion, argmax over every verified row, accept, append; host generation of "
+                      f"the logit rows excluded ({res.provider_s / used:.2f} s/thread), wall incl. generation "
+                      f"{res.wall_s:.2f} s", "cpu": _cpu_model()}
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores as the reference arm."""
+    import oracle
+    import workload as wl
+
+    if rank != 0:
+        return None
+    w = wl.make(args.config)
+    W, K = args.warmup, args.steps
+    K = min(K, w.steps - W)
+    threads = os.cpu_count() or 1
+    res = oracle.run(w, steps=W + K, threads=threads, timed_from=W)
+    used = min(threads, w.B)
+    per_thread = res.method_s / used
+    v = round(K / per_thread, 3)
+    return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(per_thread * 1e3 / K, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}", "batch": w.B, "vocab": w.V},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"{w.B} requests x {W} warm-up + {K} timed steps, host generation of the "
+                                       f"logit rows excluded", "cpu": _cpu_model()},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=504)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="2", choices=sorted(CONFIG_NAMES))
+    ap.add_argument("--input-gb", type=float, default=40.0, help="HBM for pre-generated timed inputs")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--cpu-steps", type=int, default=128)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local, dist = _dist()
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    if world > 1:
+        dist.init_process_group(backend="nccl")
+    try:
+        out = run_ours(args, world, rank, local, dist)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

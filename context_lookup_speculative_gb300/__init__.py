@@ -1,0 +1,352 @@
+"""GB300 (sm_103a) hot path of context-lookup speculative decoding.
+
+A thin ctypes binding over ``libclk.so`` (C ABI in ``include/clk.h``).  Every
+step of the path runs in the library's CUDA kernels; this module only checks
+tensors and passes their device pointers and the current CUDA stream.  There
+is no fallback: if the library is missing, importing the binding's functions
+raises.
+
+Per decode step (HyperQwen context-lookup article, "lookup 草稿的原理：三步走"):
+
+    lookup_propose    Step 1: longest 4..12 suffix match, most recent, LZ77 copy
+    sched_step        Step 3: long-block scheduler (enter after 2, sticky 3)
+    fuse              Step 2: head / tail fusion rule
+    verify_greedy     greedy verification: argmax rows + accepted prefix
+    lookup_append     commit the emitted tokens (incremental index update)
+
+plus the fused launches ``propose_fuse_sched`` and ``verify_append`` that the
+``Step`` driver uses (two kernels per step).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from functools import lru_cache
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libclk.so")
+
+OK, EINVAL, ECAPACITY, ECUDA, ENOTIMPL, ESTATE = 0, -1, -2, -3, -4, -5
+BF16, F32 = 0, 1
+SENT = -1
+BLOCK = 16
+MAX_BATCH = 8192
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+
+class ClkError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        self.code = code
+
+
+class Params(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "min_k", "max_k", "head", "tail", "head_replace_k", "head_agree_k", "head_agree_n", "tail_k",
+        "enter_streak", "sticky", "near_full_slack")]
+
+    @classmethod
+    def default(cls, **kw) -> "Params":
+        p = cls()
+        lib().clk_params_default(ctypes.byref(p))
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return p
+
+    @property
+    def long_len(self) -> int:
+        return 1 + self.head + self.tail
+
+    @property
+    def short_len(self) -> int:
+        return 1 + self.head
+
+
+class Counters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")] + \
+               [("accept_hist", (ctypes.c_int64 * 16) * 2)]
+
+    def as_dict(self):
+        d = {n: getattr(self, n) for n in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")}
+        d["accept_hist"] = [[self.accept_hist[i][j] for j in range(16)] for i in range(2)]
+        return d
+
+
+class SlotInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n", "mode", "streak", "miss", "has_prev", "cur_len")]
+
+
+# (name, restype, argtypes) of every exported entry point
+_SIGS = [
+    ("clk_params_default", None, [_P]),
+    ("clk_params_check", ctypes.c_int, [_P]),
+    ("clk_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("clk_lookup_workspace_bytes", ctypes.c_int, [_P, _I32, _I64, ctypes.POINTER(ctypes.c_size_t)]),
+    ("clk_lookup_create", ctypes.c_int, [ctypes.POINTER(_P), _P, _I32, _I64, _I32, _P, ctypes.c_size_t]),
+    ("clk_lookup_reset", ctypes.c_int, [_P, _P]),
+    ("clk_lookup_init", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
+    ("clk_lookup_append", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
+    ("clk_lookup_propose", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
+    ("clk_sched_step", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P]),
+    ("clk_fuse", ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    ("clk_fuse_sched", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    ("clk_propose_fuse_sched", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    ("clk_verify_scratch_bytes", ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
+    ("clk_verify_scratch_init", ctypes.c_int, [_P, ctypes.c_size_t, _P]),
+    ("clk_verify_greedy", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                         ctypes.c_size_t, _P]),
+    ("clk_verify_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
+    ("clk_status_clear", ctypes.c_int, [_P, _P]),
+    ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
+    ("clk_read_slot_info", ctypes.c_int, [_P, _I32, _P, _P]),
+    ("clk_lookup_read_history", ctypes.c_int, [_P, _I32, _P, _I64, ctypes.POINTER(_I64), _P]),
+    ("clk_lookup_destroy", None, [_P]),
+]
+
+
+@lru_cache(maxsize=None)
+def lib() -> ctypes.CDLL:
+    """The loaded libclk.so; raises if it has not been built."""
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    for name, res, args in _SIGS:
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().clk_status_string(code).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        raise ClkError(fn, rc)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=torch.int32, shape=None, name="tensor") -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _logits_args(logits: torch.Tensor):
+    if not logits.is_cuda or logits.dim() != 3:
+        raise ValueError("logits must be a CUDA tensor [B, rows, V]")
+    if logits.dtype == torch.bfloat16:
+        dt = BF16
+    elif logits.dtype == torch.float32:
+        dt = F32
+    else:
+        raise ValueError("logits must be bfloat16 or float32")
+    if logits.stride(2) != 1:
+        raise ValueError("logits rows must be contiguous")
+    return dt, logits.stride(1), logits.stride(0), logits.shape[2]
+
+
+class Lookup:
+    """Histories, k-gram index and scheduler state of up to `max_slots` requests.
+
+    Owns its device workspace (a torch uint8 tensor) and the C handle."""
+
+    def __init__(self, max_slots: int, max_hist: int, vocab: int = 0, params: Optional[Params] = None,
+                 device="cuda", stream=None):
+        self.params = params or Params.default()
+        L = lib()
+        nbytes = ctypes.c_size_t()
+        _check("clk_lookup_workspace_bytes",
+               L.clk_lookup_workspace_bytes(ctypes.byref(self.params), max_slots, max_hist, ctypes.byref(nbytes)))
+        self.workspace_bytes = nbytes.value
+        # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks.
+        self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+        h = _P()
+        _check("clk_lookup_create", L.clk_lookup_create(ctypes.byref(h), ctypes.byref(self.params), max_slots,
+                                                        max_hist, vocab, self.workspace.data_ptr(),
+                                                        self.workspace_bytes))
+        self.handle = h
+        self.max_slots, self.max_hist, self.vocab = max_slots, max_hist, vocab
+        _check("clk_lookup_reset", L.clk_lookup_reset(self.handle, _stream(stream)))
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            try:
+                lib().clk_lookup_destroy(h)
+            except Exception:
+                pass
+            self.handle = None
+
+    # -- inspection (synchronising) -------------------------------------
+    def status(self, stream=None):
+        st, det = _I32(), _I32()
+        _check("clk_status", lib().clk_status(self.handle, ctypes.byref(st), ctypes.byref(det), _stream(stream)))
+        return st.value, det.value
+
+    def status_clear(self, stream=None):
+        _check("clk_status_clear", lib().clk_status_clear(self.handle, _stream(stream)))
+
+    def counters(self, slot: int = -1, stream=None) -> dict:
+        c = Counters()
+        _check("clk_read_counters", lib().clk_read_counters(self.handle, slot, ctypes.byref(c), _stream(stream)))
+        return c.as_dict()
+
+    def slot_info(self, slot: int, stream=None) -> dict:
+        s = SlotInfo()
+        _check("clk_read_slot_info", lib().clk_read_slot_info(self.handle, slot, ctypes.byref(s), _stream(stream)))
+        return {n: getattr(s, n) for n, _ in SlotInfo._fields_}
+
+    def history(self, slot: int, stream=None):
+        import numpy as np
+        n = _I64()
+        _check("clk_lookup_read_history",
+               lib().clk_lookup_read_history(self.handle, slot, None, 0, ctypes.byref(n), _stream(stream)))
+        out = np.empty(n.value, dtype=np.int32)
+        _check("clk_lookup_read_history",
+               lib().clk_lookup_read_history(self.handle, slot, out.ctypes.data, n.value, ctypes.byref(n),
+                                             _stream(stream)))
+        return out
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI without the clk_ prefix)
+# ---------------------------------------------------------------------------
+def lookup_init(h: Lookup, slots, prompt, prompt_off, stream=None):
+    B = slots.numel()
+    _check("clk_lookup_init", lib().clk_lookup_init(h.handle, _ptr(slots, name="slots"), B,
+                                                    _ptr(prompt, name="prompt"),
+                                                    _ptr(prompt_off, torch.int64, (B + 1,), "prompt_off"),
+                                                    _stream(stream)))
+
+
+def lookup_append(h: Lookup, slots, tok, count, stream=None):
+    B = slots.numel()
+    _check("clk_lookup_append", lib().clk_lookup_append(h.handle, _ptr(slots, name="slots"), B,
+                                                        _ptr(tok, shape=(B, BLOCK), name="tok"),
+                                                        _ptr(count, shape=(B,), name="count"), _stream(stream)))
+
+
+def lookup_propose(h: Lookup, slots, draft, k, j, stream=None):
+    B = slots.numel()
+    _check("clk_lookup_propose", lib().clk_lookup_propose(h.handle, _ptr(slots, name="slots"), B,
+                                                          _ptr(draft, shape=(B, BLOCK), name="draft"),
+                                                          _ptr(k, shape=(B,), name="k"), _ptr(j, shape=(B,), name="j"),
+                                                          _stream(stream)))
+
+
+def sched_step(h: Lookup, slots, k, prev_accept, prev_len, length, stream=None):
+    B = slots.numel()
+    _check("clk_sched_step", lib().clk_sched_step(h.handle, _ptr(slots, name="slots"), B, _ptr(k, shape=(B,)),
+                                                  _ptr(prev_accept, shape=(B,)), _ptr(prev_len, shape=(B,)),
+                                                  _ptr(length, shape=(B,)), _stream(stream)))
+
+
+def fuse(params: Params, last_tok, draft, k, head, length, block, stream=None):
+    B = last_tok.numel()
+    _check("clk_fuse", lib().clk_fuse(ctypes.byref(params), B, _ptr(last_tok, shape=(B,)),
+                                      _ptr(draft, shape=(B, BLOCK)), _ptr(k, shape=(B,)),
+                                      _ptr(head, shape=(B, params.head)), _ptr(length, shape=(B,)),
+                                      _ptr(block, shape=(B, BLOCK)), _stream(stream)))
+
+
+def fuse_sched(h: Lookup, slots, draft, k, head, prev_accept, prev_len, length, block, stream=None):
+    B = slots.numel()
+    _check("clk_fuse_sched", lib().clk_fuse_sched(h.handle, _ptr(slots), B, _ptr(draft, shape=(B, BLOCK)),
+                                                  _ptr(k, shape=(B,)), _ptr(head, shape=(B, h.params.head)),
+                                                  _ptr(prev_accept, shape=(B,)), _ptr(prev_len, shape=(B,)),
+                                                  _ptr(length, shape=(B,)), _ptr(block, shape=(B, BLOCK)),
+                                                  _stream(stream)))
+
+
+def propose_fuse_sched(h: Lookup, slots, head, prev_accept, prev_len, draft, k, j, length, block, stream=None):
+    B = slots.numel()
+    _check("clk_propose_fuse_sched",
+           lib().clk_propose_fuse_sched(h.handle, _ptr(slots), B, _ptr(head, shape=(B, h.params.head)),
+                                        _ptr(prev_accept, shape=(B,)), _ptr(prev_len, shape=(B,)),
+                                        _ptr(draft, shape=(B, BLOCK)), _ptr(k, shape=(B,)), _ptr(j, shape=(B,)),
+                                        _ptr(length, shape=(B,)), _ptr(block, shape=(B, BLOCK)), _stream(stream)))
+
+
+def verify_scratch_bytes(B: int) -> int:
+    n = ctypes.c_size_t()
+    _check("clk_verify_scratch_bytes", lib().clk_verify_scratch_bytes(B, ctypes.byref(n)))
+    return n.value
+
+
+def verify_scratch(B: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zeroed scratch buffer for verify_greedy with up to B requests."""
+    t = torch.empty(verify_scratch_bytes(B), dtype=torch.uint8, device=device)
+    _check("clk_verify_scratch_init", lib().clk_verify_scratch_init(t.data_ptr(), t.numel(), _stream(stream)))
+    return t
+
+
+def verify_greedy(logits, block, length, argmax, accept, emitted, out_tok, scratch, stream=None):
+    dt, rs, qs, V = _logits_args(logits)
+    B = block.shape[0]
+    _check("clk_verify_greedy",
+           lib().clk_verify_greedy(logits.data_ptr(), dt, rs, qs, V, B, _ptr(block, shape=(B, BLOCK)),
+                                   _ptr(length, shape=(B,)), _ptr(argmax, shape=(B, BLOCK)),
+                                   _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
+                                   _ptr(out_tok, shape=(B, BLOCK)), _ptr(scratch, torch.uint8, name="scratch"),
+                                   scratch.numel(), _stream(stream)))
+
+
+def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None):
+    dt, rs, qs, V = _logits_args(logits)
+    B = slots.numel()
+    _check("clk_verify_append",
+           lib().clk_verify_append(h.handle, _ptr(slots), logits.data_ptr(), dt, rs, qs, V, B,
+                                   _ptr(block, shape=(B, BLOCK)), _ptr(length, shape=(B,)),
+                                   _ptr(argmax, shape=(B, BLOCK)), _ptr(accept, shape=(B,)),
+                                   _ptr(emitted, shape=(B,)), _ptr(out_tok, shape=(B, BLOCK)), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Step driver: two launches per decode step
+# ---------------------------------------------------------------------------
+class Step:
+    """Per-step buffers of one batch and the two fused launches of a step.
+
+    ``pre(head)``   -> propose + scheduler + fusion: draft, k, j, length, block
+    ``post(logits)``-> verify + commit: argmax, accept, emitted, out_tok
+    The previous step's accept/length feed the scheduler (in place)."""
+
+    def __init__(self, lookup: Lookup, slots: torch.Tensor):
+        self.h = lookup
+        self.slots = slots
+        B = slots.numel()
+        dev = slots.device
+        z = lambda *s: torch.zeros(s, dtype=torch.int32, device=dev)  # noqa: E731
+        self.B = B
+        self.draft, self.k, self.j = z(B, BLOCK), z(B), z(B)
+        self.length, self.block = z(B), z(B, BLOCK)
+        self.argmax, self.accept, self.emitted, self.out_tok = z(B, BLOCK), z(B), z(B), z(B, BLOCK)
+
+    def pre(self, head, stream=None):
+        propose_fuse_sched(self.h, self.slots, head, self.accept, self.length, self.draft, self.k, self.j,
+                           self.length, self.block, stream)
+
+    def post(self, logits, stream=None):
+        verify_append(self.h, self.slots, logits, self.block, self.length, self.argmax, self.accept,
+                      self.emitted, self.out_tok, stream)

@@ -1,0 +1,354 @@
+// Device-side building blocks of the context-lookup hot path (sm_103a).
+//
+// Workspace layout (one caller-owned device buffer, see clk_lookup_workspace_bytes):
+//   status  int32[64]                   latched device error (word 0) and its slot (word 1)
+//   state   SlotState[max_slots]        scheduler state, history length, counters
+//   vkeys   u64[max_slots * 16]         fused verify: per-row packed (value, index) maxima
+//   vdone   u64[max_slots]              fused verify: vectors verified per request
+//   hist    int32[max_slots][hstride]   token histories
+//   tab     u64[max_slots][nlev][tsize] k-gram index, one table per match length
+//
+// The k-gram index.  For every match length k in [min_k, max_k] a slot owns an
+// open-addressing table (linear probing, load <= 1/2) that maps a k-gram to
+// the END position q of its most recent occurrence.  An entry is
+// (fingerprint << 32) | (q + 1); 0 is empty.  A k-gram ending at q is
+// inserted once position q + 1 exists, so a table never returns the current
+// suffix itself and every hit q gives a candidate j = q + 1 <= n - 1 with
+// j >= k.  The longest suffix match of the pages' Step 1 is then the largest
+// k whose table holds the suffix's k-gram, and its most recent occurrence is
+// that table's entry: no chain walk and no history rescan, whatever the
+// history length or its periodicity.  Entries are only ever inserted (the
+// history only grows), so concurrent inserts use a CAS to claim an empty
+// slot and an atomicMax on the same key to keep the largest q.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "clk.h"
+
+namespace clk {
+
+constexpr int kBlock = CLK_BLOCK;
+constexpr int kMaxK = CLK_MAX_K;
+constexpr int kShort = 0;
+constexpr int kLong = 1;
+
+struct __align__(16) SlotState {
+    int32_t n;
+    int32_t mode;
+    int32_t streak;
+    int32_t miss;
+    int32_t has_prev;
+    int32_t cur_len;
+    int32_t pad0, pad1;
+    long long steps, hits, long_steps, drafted, accepted, emitted;
+    long long accept_hist[2][16];
+};
+
+struct LookupDev {
+    int32_t* status;
+    SlotState* state;
+    unsigned long long* vkeys;
+    unsigned long long* vdone;
+    int32_t* hist;
+    unsigned long long* tab;
+    int64_t hstride;  // int32 elements per history
+    int64_t cap;      // max_hist
+    uint64_t tsize;   // entries per table (power of two)
+    int32_t nlev;     // max_k - min_k + 1
+    int32_t max_slots;
+    int32_t vocab;
+    int32_t pad;
+    clk_params p;
+};
+
+__device__ __forceinline__ void latch(int32_t* status, int32_t code, int32_t detail)
+{
+    if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
+}
+
+__device__ __forceinline__ int32_t* hist_of(const LookupDev& L, int32_t slot)
+{
+    return L.hist + (int64_t)slot * L.hstride;
+}
+
+__device__ __forceinline__ unsigned long long* table_of(const LookupDev& L, int32_t slot, int32_t level)
+{
+    return L.tab + ((uint64_t)slot * (uint64_t)L.nlev + (uint64_t)level) * L.tsize;
+}
+
+__device__ __forceinline__ bool token_ok(const LookupDev& L, int32_t t)
+{
+    return t >= 0 && (L.vocab <= 0 || t < L.vocab);
+}
+
+__device__ __forceinline__ int32_t long_len(const clk_params& p) { return 1 + p.head + p.tail; }
+__device__ __forceinline__ int32_t short_len(const clk_params& p) { return 1 + p.head; }
+
+// ---------------------------------------------------------------------------
+// k-gram hashing: tokens taken backwards from the end position, w[l] = h[q-l].
+// Each step xors a token in, multiplies by an odd 64-bit constant and folds
+// the high half down; the final step mixes in k.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t kg_step(uint64_t acc, int32_t tok)
+{
+    acc ^= (uint32_t)tok;
+    acc *= 0xFF51AFD7ED558CCDull;
+    acc ^= acc >> 32;
+    return acc;
+}
+
+__device__ __forceinline__ uint64_t kg_final(uint64_t acc, int32_t k)
+{
+    acc ^= (uint64_t)(uint32_t)k << 56;
+    acc *= 0xC4CEB9FE1A85EC53ull;
+    acc ^= acc >> 29;
+    return acc;
+}
+
+constexpr uint64_t kHashSeed = 0x243F6A8885A308D3ull;
+
+// True if h[p - l] == w[l] for l < k (the stored occurrence is the k-gram w).
+// Loads go through L2 (ld.cg): the fused append compares against tokens that
+// the same kernel has just written.
+__device__ __forceinline__ bool kgram_at(const int32_t* h, int32_t p, const int32_t* w, int32_t k)
+{
+    if (p - (k - 1) < 0) return false;
+    bool same = true;
+#pragma unroll
+    for (int l = 0; l < kMaxK; ++l)
+        if (l < k) same &= (__ldcg(h + p - l) == w[l]);
+    return same;
+}
+
+// Insert k-gram w (ending at q, hash H) into one table; keeps the largest q.
+// Returns false only if the table is full (cannot happen at load <= 1/2).
+__device__ __forceinline__ bool index_insert(unsigned long long* tab, uint64_t mask, uint64_t H,
+                                             const int32_t* h, int32_t q, const int32_t* w,
+                                             int32_t k)
+{
+    const uint32_t fp = (uint32_t)(H >> 32);
+    const unsigned long long entry = ((unsigned long long)fp << 32) | (uint32_t)(q + 1);
+    uint64_t s = H & mask;
+    for (uint64_t probe = 0; probe <= mask; ++probe, s = (s + 1) & mask) {
+        unsigned long long cur = __ldcg(tab + s);
+        if (cur == 0ull) {
+            unsigned long long old = atomicCAS(tab + s, 0ull, entry);
+            if (old == 0ull) return true;
+            cur = old;
+        }
+        if ((uint32_t)(cur >> 32) == fp && kgram_at(h, (int32_t)(uint32_t)cur - 1, w, k)) {
+            atomicMax(tab + s, entry);
+            return true;
+        }
+    }
+    return false;
+}
+
+// Most recent end position of k-gram w (hash H) in one table, or -1.
+__device__ __forceinline__ int32_t index_find(const unsigned long long* tab, uint64_t mask, uint64_t H,
+                                              const int32_t* h, const int32_t* w, int32_t k)
+{
+    const uint32_t fp = (uint32_t)(H >> 32);
+    uint64_t s = H & mask;
+    for (uint64_t probe = 0; probe <= mask; ++probe, s = (s + 1) & mask) {
+        unsigned long long cur = tab[s];
+        if (cur == 0ull) return -1;
+        if ((uint32_t)(cur >> 32) == fp) {
+            int32_t p = (int32_t)(uint32_t)cur - 1;
+            if (kgram_at(h, p, w, k)) return p;
+        }
+    }
+    return -1;
+}
+
+// ---------------------------------------------------------------------------
+// Step 3 (long-block scheduler) on one slot's state; returns the block length.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t sched_update(const clk_params& p, SlotState* st, int32_t k, int32_t prev_a,
+                                                int32_t prev_len)
+{
+    const bool flag = k >= p.tail_k;
+    const bool near_full = st->has_prev && prev_a >= prev_len - 1 - p.near_full_slack;
+    int32_t mode = st->mode, streak = st->streak, miss = st->miss;
+    if (mode == kShort) {
+        streak = (flag && near_full) ? streak + 1 : 0;
+        if (streak >= p.enter_streak) {
+            mode = kLong;
+            miss = 0;
+        }
+    } else {
+        miss = flag ? 0 : miss + 1;
+        if (miss > p.sticky) {
+            mode = kShort;
+            streak = 0;
+        }
+    }
+    const int32_t len = mode == kLong ? long_len(p) : short_len(p);
+    st->mode = mode;
+    st->streak = streak;
+    st->miss = miss;
+    st->has_prev = 1;
+    st->cur_len = len;
+    st->steps += 1;
+    st->hits += (k >= p.min_k) ? 1 : 0;
+    st->long_steps += (len == long_len(p)) ? 1 : 0;
+    st->drafted += p.head + ((len == long_len(p) && k >= p.tail_k) ? p.tail : 0);
+    return len;
+}
+
+// ---------------------------------------------------------------------------
+// Step 2 (fusion): decisions and the value of one block slot.
+// ---------------------------------------------------------------------------
+// agree_mask: bit i set when lookup draft token i equals draft-model proposal i.
+__device__ __forceinline__ bool fuse_take_head(const clk_params& p, int32_t k, uint32_t agree_mask)
+{
+    if (k >= p.head_replace_k) return true;
+    if (k < p.head_agree_k) return false;
+    const uint32_t need = p.head_agree_n >= 32 ? 0xFFFFFFFFu : ((1u << p.head_agree_n) - 1u);
+    return (agree_mask & need) == need;
+}
+
+__device__ __forceinline__ bool fuse_fill_tail(const clk_params& p, int32_t k, int32_t len)
+{
+    return len == long_len(p) && k >= p.tail_k;
+}
+
+// Slot i of the block given the decisions; c_prev = draft[i-1], m_prev = head[i-1].
+__device__ __forceinline__ int32_t fuse_slot(const clk_params& p, int32_t i, int32_t last, bool take_head,
+                                             bool fill_tail, int32_t c_prev, int32_t m_prev)
+{
+    if (i == 0) return last;
+    if (i <= p.head) return take_head ? c_prev : m_prev;
+    if (i <= p.head + p.tail) return fill_tail ? c_prev : CLK_SENT;
+    return CLK_SENT;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide append of `count` tokens (in shared memory) to one slot, with the
+// index inserts of every k-gram the new tokens complete.  All threads of the
+// block call it with the same arguments.  sm_win needs kBlock + kMaxK ints.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void block_append(const LookupDev& L, int32_t slot, const int32_t* sm_tok, int32_t count,
+                                             int32_t* sm_flag, int32_t* sm_win)
+{
+    const int tid = threadIdx.x;
+    SlotState* st = L.state + slot;
+    if (tid == 0) {
+        int ok = 1;
+        const int32_t n = st->n;
+        if (count < 0 || count > kBlock) {
+            latch(L.status, CLK_EINVAL, slot);
+            ok = 0;
+        } else if ((int64_t)n + count > L.cap) {
+            latch(L.status, CLK_ECAPACITY, slot);
+            ok = 0;
+        } else {
+            for (int i = 0; i < count; ++i)
+                if (!token_ok(L, sm_tok[i])) {
+                    latch(L.status, CLK_EINVAL, slot);
+                    ok = 0;
+                    break;
+                }
+        }
+        sm_flag[0] = ok;
+        sm_flag[1] = n;
+    }
+    __syncthreads();
+    if (!sm_flag[0]) {
+        __syncthreads();
+        return;
+    }
+    const int32_t n_old = sm_flag[1];
+    const int32_t n_new = n_old + count;
+    int32_t* h = hist_of(L, slot);
+    const clk_params& p = L.p;
+    // Window of tokens the new k-grams read: positions [wlo, n_new - 1).
+    const int32_t wlo = max(0, n_old - p.max_k);
+    if (tid < count) h[n_old + tid] = sm_tok[tid];
+    if (tid < n_new - wlo) sm_win[tid] = (wlo + tid < n_old) ? h[wlo + tid] : sm_tok[wlo + tid - n_old];
+    __syncthreads();
+    // New end positions q = n_old-1 .. n_new-2 become eligible.
+    const int32_t q_lo = max(n_old - 1, 0);
+    const int32_t nq = (n_new - 2) - q_lo + 1;
+    const uint64_t mask = L.tsize - 1;
+    for (int task = tid; task < nq * L.nlev; task += blockDim.x) {
+        const int32_t q = q_lo + task / L.nlev;
+        const int32_t lvl = task % L.nlev;
+        const int32_t k = p.min_k + lvl;
+        if (q < k - 1) continue;
+        int32_t w[kMaxK];
+        uint64_t acc = kHashSeed;
+#pragma unroll
+        for (int l = 0; l < kMaxK; ++l) {
+            if (l < k) {
+                w[l] = sm_win[q - l - wlo];
+                acc = kg_step(acc, w[l]);
+            }
+        }
+        if (!index_insert(table_of(L, slot, lvl), mask, kg_final(acc, k), h, q, w, k))
+            latch(L.status, CLK_ECAPACITY, slot);
+    }
+    if (tid == 0) {
+        st->n = n_new;
+        const int32_t len = st->cur_len;
+        if (len != 0 && count > 0) {
+            st->accepted += count - 1;
+            st->emitted += count;
+            if (count - 1 < 16) st->accept_hist[len == long_len(p) ? 1 : 0][count - 1] += 1;
+        }
+        st->cur_len = 0;
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Step 1 (lookup) for one request, one warp.  Lane i < kBlock receives draft
+// token i; every lane receives k, j and the last committed token.
+// ---------------------------------------------------------------------------
+struct ProposeOut {
+    int32_t k, j, c, last;  // c: this lane's draft token (lanes >= kBlock: CLK_SENT)
+};
+
+__device__ __forceinline__ ProposeOut warp_propose(const LookupDev& L, int32_t slot)
+{
+    const unsigned full = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31;
+    const clk_params& p = L.p;
+    const int32_t n = L.state[slot].n;
+    const int32_t* h = hist_of(L, slot);
+    // Suffix tokens s[l] = h[n-1-l].
+    int32_t mine = (lane < p.max_k && n - 1 - lane >= 0) ? h[n - 1 - lane] : CLK_SENT;
+    int32_t s[kMaxK];
+#pragma unroll
+    for (int l = 0; l < kMaxK; ++l) s[l] = __shfl_sync(full, mine, l);
+    // Lane `lane` searches match length k = min_k + lane.
+    const int32_t k = p.min_k + lane;
+    const bool active = lane < L.nlev && n >= k + 1;
+    int32_t q = -1;
+    if (active) {
+        uint64_t acc = kHashSeed;
+#pragma unroll
+        for (int l = 0; l < kMaxK; ++l)
+            if (l < k) acc = kg_step(acc, s[l]);
+        q = index_find(table_of(L, slot, lane), L.tsize - 1, kg_final(acc, k), h, s, k);
+    }
+    const unsigned hit = __ballot_sync(full, q >= 0);
+    ProposeOut o;
+    o.last = s[0];
+    if (hit == 0u) {
+        o.k = 0;
+        o.j = -1;
+        o.c = CLK_SENT;
+        return o;
+    }
+    const int best = 31 - __clz((int)hit);
+    o.k = p.min_k + best;
+    o.j = __shfl_sync(full, q, best) + 1;
+    const int32_t period = n - o.j;
+    o.c = lane < kBlock ? h[o.j + (lane % period)] : CLK_SENT;
+    return o;
+}
+
+}  // namespace clk

@@ -1,0 +1,382 @@
+// Lookup side of the hot path: prompt ingestion with the index build,
+// incremental append, the suffix-match proposal, the scheduler and fusion
+// (HyperQwen context-lookup article, "lookup 草稿的原理：三步走", Steps 1-3).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "clk.h"
+#include "clk_device.cuh"
+#include "clk_host.h"
+
+namespace clk {
+
+constexpr int kThreads = 256;
+
+// Slot and prompt length of batch position b, validated; -1 slot if invalid.
+__device__ __forceinline__ int32_t init_slot(const LookupDev& L, const int32_t* slots, const int64_t* off, int32_t b,
+                                             int64_t* n_out)
+{
+    const int32_t slot = slots[b];
+    if (slot < 0 || slot >= L.max_slots) return -1;
+    const int64_t n = off[b + 1] - off[b];
+    *n_out = n;
+    return slot;
+}
+
+__global__ void k_init_state(LookupDev L, const int32_t* __restrict__ slots, const int64_t* __restrict__ off,
+                             int32_t B)
+{
+    const int32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int64_t n = 0;
+    const int32_t slot = init_slot(L, slots, off, b, &n);
+    if (slot < 0) {
+        latch(L.status, CLK_EINVAL, b);
+        return;
+    }
+    SlotState* st = L.state + slot;
+    int32_t nn = (int32_t)n;
+    if (n < 1) {
+        latch(L.status, CLK_EINVAL, slot);
+        nn = 0;
+    } else if (n > L.cap) {
+        latch(L.status, CLK_ECAPACITY, slot);
+        nn = 0;
+    }
+    SlotState z = {};
+    z.n = nn;
+    *st = z;
+}
+
+// Grid: B * chunks blocks; chunk c of batch position b copies positions
+// [c*kThreads*4, (c+1)*kThreads*4).
+__global__ void k_copy_prompt(LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ prompt,
+                              const int64_t* __restrict__ off, int32_t chunks)
+{
+    const int32_t b = blockIdx.x / chunks;
+    const int64_t c = blockIdx.x % chunks;
+    int64_t n = 0;
+    const int32_t slot = init_slot(L, slots, off, b, &n);
+    if (slot < 0 || n < 1 || n > L.cap) return;
+    int32_t* h = hist_of(L, slot);
+    const int32_t* src = prompt + off[b];
+    bool bad = false;
+    for (int64_t q = c * kThreads * 4 + threadIdx.x; q < min(n, (c + 1) * kThreads * 4); q += kThreads) {
+        const int32_t t = src[q];
+        bad |= !token_ok(L, t);
+        h[q] = t;
+    }
+    if (bad) latch(L.status, CLK_EINVAL, slot);
+}
+
+// Zero the tables of each slot in the batch.  Grid: B * chunks blocks.
+__global__ void k_clear_tables(LookupDev L, const int32_t* __restrict__ slots, int32_t chunks, uint64_t per_chunk)
+{
+    const int32_t b = blockIdx.x / chunks;
+    const uint64_t c = blockIdx.x % chunks;
+    const int32_t slot = slots[b];
+    if (slot < 0 || slot >= L.max_slots) return;
+    const uint64_t total = (uint64_t)L.nlev * L.tsize;  // entries, even
+    uint4* base = reinterpret_cast<uint4*>(table_of(L, slot, 0));
+    const uint64_t lo = c * per_chunk, hi = min(total / 2, (c + 1) * per_chunk);
+    for (uint64_t i = lo + threadIdx.x; i < hi; i += kThreads) base[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Insert every eligible (end position, length) of each prompt: one thread per
+// end position q <= n - 2, all lengths k <= q + 1.  Grid: B * chunks blocks.
+__global__ void k_build_index(LookupDev L, const int32_t* __restrict__ slots, const int64_t* __restrict__ off,
+                              int32_t chunks)
+{
+    const int32_t b = blockIdx.x / chunks;
+    const int64_t c = blockIdx.x % chunks;
+    int64_t n = 0;
+    const int32_t slot = init_slot(L, slots, off, b, &n);
+    if (slot < 0 || n < 1 || n > L.cap) return;
+    const int64_t q = c * kThreads + threadIdx.x;
+    if (q > n - 2) return;
+    const int32_t* h = hist_of(L, slot);
+    const clk_params& p = L.p;
+    int32_t w[kMaxK];
+#pragma unroll
+    for (int l = 0; l < kMaxK; ++l) w[l] = (l < p.max_k && q - l >= 0) ? h[q - l] : CLK_SENT;
+    const uint64_t mask = L.tsize - 1;
+    uint64_t acc = kHashSeed;
+#pragma unroll
+    for (int l = 0; l < kMaxK; ++l) {
+        const int32_t k = l + 1;
+        if (k > p.max_k || q < k - 1) break;
+        acc = kg_step(acc, w[l]);
+        if (k >= p.min_k) {
+            if (!index_insert(table_of(L, slot, k - p.min_k), mask, kg_final(acc, k), h, (int32_t)q, w, k))
+                latch(L.status, CLK_ECAPACITY, slot);
+        }
+    }
+}
+
+// One block per request: append d_tok[b][0..count) and index the new k-grams.
+__global__ void k_append(LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ tok,
+                         const int32_t* __restrict__ count)
+{
+    __shared__ int32_t sm_tok[kBlock];
+    __shared__ int32_t sm_flag[2];
+    __shared__ int32_t sm_win[kBlock + kMaxK];
+    const int32_t b = blockIdx.x;
+    const int32_t slot = slots[b];
+    if (slot < 0 || slot >= L.max_slots) {
+        if (threadIdx.x == 0) latch(L.status, CLK_EINVAL, b);
+        return;
+    }
+    const int32_t cnt = count[b];
+    if (threadIdx.x < kBlock) sm_tok[threadIdx.x] = tok[(int64_t)b * kBlock + threadIdx.x];
+    __syncthreads();
+    block_append(L, slot, sm_tok, cnt, sm_flag, sm_win);
+}
+
+__device__ __forceinline__ bool warp_slot(const LookupDev& L, const int32_t* slots, int32_t B, int32_t* b_out,
+                                          int32_t* slot_out)
+{
+    const int32_t b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (b >= B) return false;
+    const int32_t slot = slots[b];
+    *b_out = b;
+    *slot_out = slot;
+    return true;
+}
+
+// Empty or invalid slot: latch and emit the no-match proposal.
+__device__ __forceinline__ bool slot_usable(const LookupDev& L, int32_t slot, int32_t b)
+{
+    if (slot < 0 || slot >= L.max_slots) {
+        if ((threadIdx.x & 31) == 0) latch(L.status, CLK_EINVAL, b);
+        return false;
+    }
+    if (L.state[slot].n < 1) {
+        if ((threadIdx.x & 31) == 0) latch(L.status, CLK_ESTATE, slot);
+        return false;
+    }
+    return true;
+}
+
+// One warp per request.
+__global__ void k_propose(LookupDev L, const int32_t* __restrict__ slots, int32_t B, int32_t* __restrict__ draft,
+                          int32_t* __restrict__ k_out, int32_t* __restrict__ j_out)
+{
+    int32_t b, slot;
+    if (!warp_slot(L, slots, B, &b, &slot)) return;
+    const int lane = threadIdx.x & 31;
+    ProposeOut o = {0, -1, CLK_SENT, CLK_SENT};
+    if (slot_usable(L, slot, b)) o = warp_propose(L, slot);
+    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = o.c;
+    if (lane == 0) {
+        k_out[b] = o.k;
+        j_out[b] = o.j;
+    }
+}
+
+// One thread per request.
+__global__ void k_sched(LookupDev L, const int32_t* __restrict__ slots, int32_t B, const int32_t* __restrict__ k,
+                        const int32_t* prev_a, const int32_t* prev_len, int32_t* len)
+{
+    const int32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int32_t slot = slots[b];
+    if (slot < 0 || slot >= L.max_slots) {
+        latch(L.status, CLK_EINVAL, b);
+        len[b] = short_len(L.p);
+        return;
+    }
+    const int32_t pa = prev_a[b], pl = prev_len[b];
+    len[b] = sched_update(L.p, L.state + slot, k[b], pa, pl);
+}
+
+// Fusion of one request by one warp; lanes < kBlock write the block.
+__device__ __forceinline__ void warp_fuse(const clk_params& p, int32_t last, int32_t c_lane, int32_t k,
+                                          const int32_t* __restrict__ head_row, int32_t len, int32_t* block_row)
+{
+    const unsigned full = 0xFFFFFFFFu;
+    const int lane = threadIdx.x & 31;
+    const int32_t m_lane = lane < p.head ? head_row[lane] : CLK_SENT;
+    const unsigned agree = __ballot_sync(full, lane < p.head && c_lane == m_lane);
+    const bool take_head = fuse_take_head(p, k, agree);
+    const bool fill_tail = fuse_fill_tail(p, k, len);
+    // slot i takes draft/head token i-1
+    const int32_t c_prev = __shfl_up_sync(full, c_lane, 1);
+    const int32_t m_prev = __shfl_up_sync(full, m_lane, 1);
+    if (lane < kBlock) block_row[lane] = fuse_slot(p, lane, last, take_head, fill_tail, c_prev, m_prev);
+}
+
+// Stateless fusion: one warp per request.
+__global__ void k_fuse(clk_params p, int32_t B, const int32_t* __restrict__ last_tok,
+                       const int32_t* __restrict__ draft, const int32_t* __restrict__ k,
+                       const int32_t* __restrict__ head, const int32_t* __restrict__ len,
+                       int32_t* __restrict__ block)
+{
+    const int32_t b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (b >= B) return;
+    const int lane = threadIdx.x & 31;
+    const int32_t c_lane = lane < kBlock ? draft[(int64_t)b * kBlock + lane] : CLK_SENT;
+    warp_fuse(p, last_tok[b], c_lane, k[b], head + (int64_t)b * p.head, len[b], block + (int64_t)b * kBlock);
+}
+
+// Scheduler then fusion: one warp per request.
+__global__ void k_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int32_t B,
+                             const int32_t* __restrict__ draft, const int32_t* __restrict__ k,
+                             const int32_t* __restrict__ head, const int32_t* prev_a, const int32_t* prev_len,
+                             int32_t* len, int32_t* __restrict__ block)
+{
+    int32_t b, slot;
+    if (!warp_slot(L, slots, B, &b, &slot)) return;
+    const int lane = threadIdx.x & 31;
+    const bool ok = slot >= 0 && slot < L.max_slots;
+    int32_t l = short_len(L.p);
+    const int32_t kk = k[b];
+    if (lane == 0) {
+        if (ok)
+            l = sched_update(L.p, L.state + slot, kk, prev_a[b], prev_len[b]);
+        else
+            latch(L.status, CLK_EINVAL, b);
+        len[b] = l;
+    }
+    l = __shfl_sync(0xFFFFFFFFu, l, 0);
+    int32_t last = CLK_SENT;
+    if (ok) {
+        const int32_t n = L.state[slot].n;
+        last = n >= 1 ? hist_of(L, slot)[n - 1] : CLK_SENT;
+    }
+    const int32_t c_lane = lane < kBlock ? draft[(int64_t)b * kBlock + lane] : CLK_SENT;
+    warp_fuse(L.p, last, c_lane, kk, head + (int64_t)b * L.p.head, l, block + (int64_t)b * kBlock);
+}
+
+// Proposal, scheduler and fusion: one warp per request.
+__global__ void k_propose_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int32_t B,
+                                     const int32_t* __restrict__ head, const int32_t* prev_a,
+                                     const int32_t* prev_len, int32_t* __restrict__ draft, int32_t* __restrict__ k_out,
+                                     int32_t* __restrict__ j_out, int32_t* len, int32_t* __restrict__ block)
+{
+    int32_t b, slot;
+    if (!warp_slot(L, slots, B, &b, &slot)) return;
+    const int lane = threadIdx.x & 31;
+    const bool valid = slot >= 0 && slot < L.max_slots;
+    ProposeOut o = {0, -1, CLK_SENT, CLK_SENT};
+    if (slot_usable(L, slot, b)) o = warp_propose(L, slot);
+    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = o.c;
+    int32_t l = short_len(L.p);
+    if (lane == 0) {
+        k_out[b] = o.k;
+        j_out[b] = o.j;
+        if (valid) l = sched_update(L.p, L.state + slot, o.k, prev_a[b], prev_len[b]);
+        len[b] = l;
+    }
+    l = __shfl_sync(0xFFFFFFFFu, l, 0);
+    warp_fuse(L.p, o.last, o.c, o.k, head + (int64_t)b * L.p.head, l, block + (int64_t)b * kBlock);
+}
+
+}  // namespace clk
+
+using namespace clk;
+
+extern "C" int clk_lookup_init(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_prompt,
+                               const int64_t* d_prompt_off, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_prompt) || d_prompt_off == nullptr || !aligned(d_prompt_off, 8))
+        return CLK_EINVAL;
+    const LookupDev& L = h->dev;
+    cudaStream_t st = (cudaStream_t)s;
+    k_init_state<<<(B + 127) / 128, 128, 0, st>>>(L, d_slots, d_prompt_off, B);
+    if ((rc = launch_status()) != CLK_OK) return rc;
+    const int64_t copy_chunks = (L.cap + kThreads * 4 - 1) / (kThreads * 4);
+    k_copy_prompt<<<(unsigned)(B * copy_chunks), kThreads, 0, st>>>(L, d_slots, d_prompt, d_prompt_off,
+                                                                     (int32_t)copy_chunks);
+    if ((rc = launch_status()) != CLK_OK) return rc;
+    const uint64_t vec_total = (uint64_t)L.nlev * L.tsize / 2;  // uint4 stores per slot
+    const uint64_t per_chunk = kThreads * 16;
+    const int64_t clear_chunks = (int64_t)((vec_total + per_chunk - 1) / per_chunk);
+    k_clear_tables<<<(unsigned)(B * clear_chunks), kThreads, 0, st>>>(L, d_slots, (int32_t)clear_chunks, per_chunk);
+    if ((rc = launch_status()) != CLK_OK) return rc;
+    const int64_t build_chunks = (L.cap + kThreads - 1) / kThreads;
+    k_build_index<<<(unsigned)(B * build_chunks), kThreads, 0, st>>>(L, d_slots, d_prompt_off,
+                                                                     (int32_t)build_chunks);
+    return launch_status();
+}
+
+extern "C" int clk_lookup_append(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_tok,
+                                 const int32_t* d_count, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_tok) || !ok_i32(d_count)) return CLK_EINVAL;
+    k_append<<<B, 192, 0, (cudaStream_t)s>>>(h->dev, d_slots, d_tok, d_count);
+    return launch_status();
+}
+
+extern "C" int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft, int32_t* d_k,
+                                  int32_t* d_j, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
+    k_propose<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_draft, d_k, d_j);
+    return launch_status();
+}
+
+extern "C" int clk_sched_step(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_k,
+                              const int32_t* d_prev_accept, const int32_t* d_prev_len, int32_t* d_len, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_k) || !ok_i32(d_prev_accept) || !ok_i32(d_prev_len) || !ok_i32(d_len))
+        return CLK_EINVAL;
+    k_sched<<<(B + 127) / 128, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_k, d_prev_accept, d_prev_len, d_len);
+    return launch_status();
+}
+
+extern "C" int clk_fuse(const clk_params* p, int32_t B, const int32_t* d_last_tok, const int32_t* d_draft,
+                        const int32_t* d_k, const int32_t* d_head, const int32_t* d_len, int32_t* d_block,
+                        clk_stream_t s)
+{
+    if (p == nullptr || clk_params_check(p) != CLK_OK) return CLK_EINVAL;
+    if (B < 0 || B > CLK_MAX_BATCH) return CLK_EINVAL;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_last_tok) || !ok_i32(d_draft) || !ok_i32(d_k) || (p->head > 0 && !ok_i32(d_head)) ||
+        !ok_i32(d_len) || !ok_i32(d_block))
+        return CLK_EINVAL;
+    k_fuse<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(*p, B, d_last_tok, d_draft, d_k, d_head, d_len, d_block);
+    return launch_status();
+}
+
+extern "C" int clk_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_draft,
+                              const int32_t* d_k, const int32_t* d_head, const int32_t* d_prev_accept,
+                              const int32_t* d_prev_len, int32_t* d_len, int32_t* d_block, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || (h->dev.p.head > 0 && !ok_i32(d_head)) ||
+        !ok_i32(d_prev_accept) || !ok_i32(d_prev_len) || !ok_i32(d_len) || !ok_i32(d_block))
+        return CLK_EINVAL;
+    k_fuse_sched<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_draft, d_k, d_head, d_prev_accept,
+                                                          d_prev_len, d_len, d_block);
+    return launch_status();
+}
+
+extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_head,
+                                      const int32_t* d_prev_accept, const int32_t* d_prev_len, int32_t* d_draft,
+                                      int32_t* d_k, int32_t* d_j, int32_t* d_len, int32_t* d_block, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || (h->dev.p.head > 0 && !ok_i32(d_head)) || !ok_i32(d_prev_accept) ||
+        !ok_i32(d_prev_len) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j) || !ok_i32(d_len) ||
+        !ok_i32(d_block))
+        return CLK_EINVAL;
+    k_propose_fuse_sched<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_head, d_prev_accept,
+                                                                  d_prev_len, d_draft, d_k, d_j, d_len, d_block);
+    return launch_status();
+}

@@ -1,0 +1,495 @@
+// Greedy verification (HyperQwen context-lookup article, "三步走", last
+// paragraph; the Polish page's "the first rejected proposal ends the run"):
+// row-wise argmax over the target logits of each verify block, fused with the
+// accepted-prefix count, the emitted tokens and (clk_verify_append) the
+// commit of those tokens into the request's history and index.
+//
+// Layout of the work: the rows that must be read (L_b rows of request b) are
+// numbered 0..R-1 in request order and seen as one flat range of R * V/W
+// 16-byte vectors (W elements each).  A grid of G CTAs, G = SMs x resident
+// CTAs, splits that range evenly; each CTA streams its contiguous share with
+// 128-bit loads (4 in flight per thread), reduces every row piece it covers
+// to a packed (order-preserving value bits << 32 | ~index) 64-bit key, and
+// merges it into the row's key with one atomicMax (max value, then lowest
+// index; independent of CTA order).  Each CTA then adds the vectors it
+// covered to the request's counter; the CTA that completes a request (its
+// add reaches L_b * V/W) reads the row keys and finishes that request:
+// argmax tokens, accepted count, emitted tokens and, fused, the append.
+// No CTA waits on another.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "clk.h"
+#include "clk_device.cuh"
+#include "clk_host.h"
+
+namespace clk {
+
+constexpr int kVThreads = 256;
+constexpr int kVWarps = kVThreads / 32;
+constexpr int kUnroll = 4;
+
+struct VerifyArgs {
+    const void* logits;
+    int64_t row_stride;
+    int64_t req_stride;
+    int32_t V;
+    int32_t B;
+    const int32_t* block;
+    const int32_t* len;
+    int32_t* argmax;
+    int32_t* accept;
+    int32_t* emitted;
+    int32_t* out_tok;
+    unsigned long long* keys;  // [B * 16]
+    unsigned long long* done;  // [B]
+    const int32_t* slots;      // fused only
+};
+
+// Order-preserving 32-bit key of a float: larger value, larger key; +0 == -0.
+__device__ __forceinline__ uint32_t ord_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if (f == 0.0f) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long pack_key(uint32_t key, uint32_t idx)
+{
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+constexpr uint32_t kNanKey = 0xFFFFFFFFu;  // any NaN beats every number
+
+__device__ __forceinline__ bool len_ok(int32_t l) { return l >= 1 && l <= kBlock; }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<CLK_DTYPE_BF16> {
+    using T = uint16_t;
+    static constexpr int W = 8;
+    __device__ static float value(T x) { return __uint_as_float((uint32_t)x << 16); }
+    // 8 values of a vector
+    __device__ static void unpack(const uint4& v, float* f)
+    {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    }
+    // Accumulates a word whose bit 15 or 31 ends up set iff the vector holds a NaN.
+    __device__ static uint32_t nan_bits(const uint4& v)
+    {
+        const uint32_t m = 0x7FFF7FFFu, c = 0x007F007Fu;
+        return ((v.x & m) + c) | ((v.y & m) + c) | ((v.z & m) + c) | ((v.w & m) + c);
+    }
+    static constexpr uint32_t kNanMask = 0x80008000u;
+};
+template <>
+struct Elem<CLK_DTYPE_F32> {
+    using T = float;
+    static constexpr int W = 4;
+    __device__ static float value(T x) { return x; }
+    __device__ static void unpack(const uint4& v, float* f)
+    {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint32_t nan_bits(const uint4& v)
+    {
+        const uint32_t m = 0x7FFFFFFFu, c = 0x007FFFFFu;
+        return ((v.x & m) + c) | ((v.y & m) + c) | ((v.z & m) + c) | ((v.w & m) + c);
+    }
+    static constexpr uint32_t kNanMask = 0x80000000u;
+};
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+
+// This thread's packed key over vectors [v0, v1) of a row (vector path).
+template <int DT>
+__device__ __forceinline__ unsigned long long scan_vec(const void* row_ptr, int64_t v0, int64_t v1)
+{
+    using E = Elem<DT>;
+    constexpr int W = E::W;
+    const uint4* row = reinterpret_cast<const uint4*>(row_ptr);
+    const int64_t first = v0 + threadIdx.x;
+    if (first >= v1) return 0ull;
+    float best = -__int_as_float(0x7F800000);  // -inf
+    int64_t bvi = -1;
+    uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t nanacc = 0u;
+    for (int64_t base = first; base < v1; base += (int64_t)kUnroll * kVThreads) {
+        uint4 x[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = base + (int64_t)u * kVThreads;
+            if (vi < v1) x[u] = ld_stream(row + vi);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = base + (int64_t)u * kVThreads;
+            if (vi < v1) {
+                float f[W];
+                E::unpack(x[u], f);
+                float m = f[0];
+#pragma unroll
+                for (int e = 1; e < W; ++e) m = fmaxf(m, f[e]);
+                nanacc |= E::nan_bits(x[u]);
+                if (m > best) {
+                    best = m;
+                    bvi = vi;
+                    bvec = x[u];
+                }
+            }
+        }
+    }
+    if (nanacc & E::kNanMask) {
+        // Rare path: the first NaN of this thread's elements.
+        for (int64_t vi = first; vi < v1; vi += kVThreads) {
+            float f[W];
+            E::unpack(row[vi], f);
+#pragma unroll
+            for (int e = 0; e < W; ++e)
+                if (f[e] != f[e]) return pack_key(kNanKey, (uint32_t)(vi * W + e));
+        }
+    }
+    if (bvi < 0) return pack_key(ord_key(best), (uint32_t)(first * W));  // every element is -inf
+    float f[W];
+    E::unpack(bvec, f);
+    int e0 = W - 1;
+#pragma unroll
+    for (int e = W - 1; e >= 0; --e)
+        if (f[e] == best) e0 = e;
+    return pack_key(ord_key(best), (uint32_t)(bvi * W + e0));
+}
+
+// This thread's packed key over elements [v0, v1) of a row (unaligned rows).
+template <int DT>
+__device__ __forceinline__ unsigned long long scan_scalar(const void* row_ptr, int64_t v0, int64_t v1)
+{
+    using E = Elem<DT>;
+    const typename E::T* row = reinterpret_cast<const typename E::T*>(row_ptr);
+    const int64_t first = v0 + threadIdx.x;
+    if (first >= v1) return 0ull;
+    float best = -__int_as_float(0x7F800000);
+    int64_t bi = first;
+    for (int64_t i = first; i < v1; i += kVThreads) {
+        const float f = E::value(row[i]);
+        if (f != f) return pack_key(kNanKey, (uint32_t)i);
+        if (f > best) {
+            best = f;
+            bi = i;
+        }
+    }
+    return pack_key(ord_key(best), (uint32_t)bi);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Max over the block; the result is valid in thread 0.
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* sm_red)
+{
+    v = warp_max_u64(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sm_red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < kVWarps ? sm_red[lane] : 0ull;
+        v = warp_max_u64(v);
+    }
+    return v;
+}
+
+// P[b] = rows of requests 0..b-1 (rows = L_b if 1 <= L_b <= 16, else 0); P[B] = R.
+__device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t* P,
+                                                 int32_t* sm_warp)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t per = (B + kVThreads - 1) / kVThreads;
+    const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int32_t local = 0;
+    for (int32_t b = b0; b < b1; ++b) {
+        const int32_t l = len[b];
+        local += len_ok(l) ? l : 0;
+    }
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t s = lane < kVWarps ? sm_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < kVWarps) sm_warp[lane] = s;  // inclusive warp totals
+    }
+    __syncthreads();
+    int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
+    for (int32_t b = b0; b < b1; ++b) {
+        P[b] = run;
+        const int32_t l = len[b];
+        run += len_ok(l) ? l : 0;
+    }
+    if (tid == kVThreads - 1) P[B] = sm_warp[kVWarps - 1];
+    __syncthreads();
+}
+
+template <int DT, bool VEC, bool FUSED>
+__global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a, LookupDev L)
+{
+    extern __shared__ int32_t sm_prefix[];  // B + 1
+    __shared__ unsigned long long sm_red[kVWarps];
+    __shared__ int32_t sm_warp[kVWarps];
+    __shared__ int32_t sm_last;
+    __shared__ int32_t sm_count;
+    __shared__ int32_t sm_tok[kBlock];
+    __shared__ int32_t sm_flag[2];
+    __shared__ int32_t sm_win[kBlock + kMaxK];
+    using E = Elem<DT>;
+    const int tid = threadIdx.x;
+    const int32_t B = a.B;
+
+    block_row_prefix(a.len, B, sm_prefix, sm_warp);
+
+    // Requests with no rows to read get their outputs here.
+    if (blockIdx.x == 0) {
+        for (int32_t b = tid; b < B; b += kVThreads) {
+            if (len_ok(a.len[b])) continue;
+            for (int r = 0; r < kBlock; ++r) {
+                a.argmax[(int64_t)b * kBlock + r] = CLK_SENT;
+                a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
+            }
+            a.accept[b] = 0;
+            a.emitted[b] = 0;
+            if (FUSED) latch(L.status, CLK_EINVAL, b);
+        }
+    }
+
+    const int64_t vpr = VEC ? (int64_t)a.V / E::W : (int64_t)a.V;
+    const int64_t total = (int64_t)sm_prefix[B] * vpr;
+    int64_t lo = total * blockIdx.x / gridDim.x;
+    const int64_t hi = total * (blockIdx.x + 1) / gridDim.x;
+    if (lo >= hi) return;
+    int64_t ri = lo / vpr;
+    // Request that owns row ri: largest b with P[b] <= ri.
+    int32_t b = 0, top = B;
+    while (b < top) {
+        const int32_t mid = (b + top + 1) >> 1;
+        if (sm_prefix[mid] <= ri) b = mid; else top = mid - 1;
+    }
+    while (lo < hi) {
+        while (sm_prefix[b + 1] <= ri) ++b;
+        const int32_t r = (int32_t)(ri - sm_prefix[b]);
+        const int64_t s0 = lo - ri * vpr;
+        const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
+        const char* row = static_cast<const char*>(a.logits) +
+                          ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(typename E::T);
+        unsigned long long key = VEC ? scan_vec<DT>(row, s0, s1) : scan_scalar<DT>(row, s0, s1);
+        key = block_max_u64(key, sm_red);
+        if (tid == 0) {
+            atomicMax(a.keys + (int64_t)b * kBlock + r, key);
+            __threadfence();
+            const unsigned long long add = (unsigned long long)(s1 - s0);
+            const unsigned long long need =
+                (unsigned long long)(sm_prefix[b + 1] - sm_prefix[b]) * (unsigned long long)vpr;
+            sm_last = (atomicAdd(a.done + b, add) + add == need) ? 1 : 0;
+        }
+        __syncthreads();
+        if (sm_last) {
+            __threadfence();
+            if (tid < 32) {
+                const int lane = tid;
+                const int32_t Lb = sm_prefix[b + 1] - sm_prefix[b];
+                unsigned long long* kp = a.keys + (int64_t)b * kBlock;
+                int32_t g = CLK_SENT;
+                if (lane < Lb) {
+                    const unsigned long long kv = atomicAdd(kp + lane, 0ull);
+                    g = (int32_t)(0xFFFFFFFFu - (uint32_t)kv);
+                }
+                if (lane < kBlock) kp[lane] = 0ull;
+                const int32_t nxt = (lane + 1 < kBlock) ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
+                const unsigned match = __ballot_sync(0xFFFFFFFFu, lane < Lb - 1 && nxt == g);
+                const int32_t acc = __ffs(~match) - 1;
+                const int32_t out = lane <= acc ? g : CLK_SENT;
+                if (lane < kBlock) {
+                    a.argmax[(int64_t)b * kBlock + lane] = g;
+                    a.out_tok[(int64_t)b * kBlock + lane] = out;
+                    sm_tok[lane] = out;
+                }
+                if (lane == 0) {
+                    a.accept[b] = acc;
+                    a.emitted[b] = acc + 1;
+                    a.done[b] = 0ull;
+                    sm_count = acc + 1;
+                }
+            }
+            __syncthreads();
+            if (FUSED) {
+                const int32_t slot = a.slots[b];
+                if (slot >= 0 && slot < L.max_slots) {
+                    block_append(L, slot, sm_tok, sm_count, sm_flag, sm_win);
+                } else if (tid == 0) {
+                    latch(L.status, CLK_EINVAL, b);
+                }
+            }
+        }
+        __syncthreads();
+        ri += 1;
+        lo = ri * vpr;
+    }
+}
+
+template <int DT, bool VEC, bool FUSED>
+int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
+{
+    auto kern = k_verify<DT, VEC, FUSED>;
+    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
+    static int occ_cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
+    int occ = (dev >= 0 && dev < 64) ? occ_cache[dev] : 0;
+    if (occ == 0) {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return CLK_ECUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kVThreads, smem) != cudaSuccess || occ < 1)
+            return CLK_ECUDA;
+        if (dev >= 0 && dev < 64 && a.B <= 1024) occ_cache[dev] = occ;
+    }
+    const int sms = num_sms();
+    if (sms <= 0) return CLK_ECUDA;
+    constexpr int W = VEC ? Elem<DT>::W : 1;
+    const int64_t vpr = (int64_t)a.V / W;
+    const int64_t max_work = (int64_t)a.B * kBlock * vpr;
+    int64_t grid = (max_work + 4 * kVThreads - 1) / (4 * kVThreads);
+    grid = grid < 1 ? 1 : grid;
+    if (grid > (int64_t)occ * sms) grid = (int64_t)occ * sms;
+    kern<<<(unsigned)grid, kVThreads, smem, s>>>(a, L);
+    return launch_status();
+}
+
+int verify_dispatch(const VerifyArgs& a, int32_t dtype, bool fused, const LookupDev& L, cudaStream_t s)
+{
+    const int64_t esz = dtype == CLK_DTYPE_BF16 ? 2 : 4;
+    const int64_t W = 16 / esz;
+    const bool vec = aligned(a.logits, 16) && a.V % W == 0 && a.row_stride % W == 0 && a.req_stride % W == 0;
+    if (dtype == CLK_DTYPE_BF16) {
+        if (vec) return fused ? launch_verify<CLK_DTYPE_BF16, true, true>(a, L, s)
+                              : launch_verify<CLK_DTYPE_BF16, true, false>(a, L, s);
+        return fused ? launch_verify<CLK_DTYPE_BF16, false, true>(a, L, s)
+                     : launch_verify<CLK_DTYPE_BF16, false, false>(a, L, s);
+    }
+    if (vec) return fused ? launch_verify<CLK_DTYPE_F32, true, true>(a, L, s)
+                          : launch_verify<CLK_DTYPE_F32, true, false>(a, L, s);
+    return fused ? launch_verify<CLK_DTYPE_F32, false, true>(a, L, s)
+                 : launch_verify<CLK_DTYPE_F32, false, false>(a, L, s);
+}
+
+int verify_check(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                 const int32_t* d_block, const int32_t* d_len, int32_t* d_argmax, int32_t* d_accept,
+                 int32_t* d_emitted, int32_t* d_out_tok)
+{
+    if (dtype != CLK_DTYPE_BF16 && dtype != CLK_DTYPE_F32) return CLK_EINVAL;
+    if (V < 1 || B < 0 || B > CLK_MAX_BATCH) return CLK_EINVAL;
+    if (row_stride < V || req_stride < 0) return CLK_EINVAL;
+    if (B > 1 && req_stride < row_stride) return CLK_EINVAL;
+    if (d_logits == nullptr || !aligned(d_logits, dtype == CLK_DTYPE_BF16 ? 2 : 4)) return CLK_EINVAL;
+    if (!ok_i32(d_block) || !ok_i32(d_len) || !ok_i32(d_argmax) || !ok_i32(d_accept) || !ok_i32(d_emitted) ||
+        !ok_i32(d_out_tok))
+        return CLK_EINVAL;
+    return CLK_OK;
+}
+
+}  // namespace clk
+
+using namespace clk;
+
+extern "C" int clk_verify_scratch_bytes(int32_t B, size_t* bytes)
+{
+    if (bytes == nullptr || B < 0 || B > CLK_MAX_BATCH) return CLK_EINVAL;
+    *bytes = (size_t)(B > 0 ? B : 1) * (kBlock + 1) * sizeof(unsigned long long);
+    return CLK_OK;
+}
+
+extern "C" int clk_verify_scratch_init(void* d_scratch, size_t bytes, clk_stream_t s)
+{
+    if (d_scratch == nullptr || !aligned(d_scratch, 8)) return CLK_EINVAL;
+    return cuda_status(cudaMemsetAsync(d_scratch, 0, bytes, (cudaStream_t)s));
+}
+
+extern "C" int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                 int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                 int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok,
+                                 void* d_scratch, size_t scratch_bytes, clk_stream_t s)
+{
+    int rc = verify_check(d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_argmax, d_accept,
+                          d_emitted, d_out_tok);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    size_t need = 0;
+    clk_verify_scratch_bytes(B, &need);
+    if (d_scratch == nullptr || !aligned(d_scratch, 8) || scratch_bytes < need) return CLK_EINVAL;
+    VerifyArgs a;
+    a.logits = d_logits;
+    a.row_stride = row_stride;
+    a.req_stride = req_stride;
+    a.V = V;
+    a.B = B;
+    a.block = d_block;
+    a.len = d_len;
+    a.argmax = d_argmax;
+    a.accept = d_accept;
+    a.emitted = d_emitted;
+    a.out_tok = d_out_tok;
+    a.keys = static_cast<unsigned long long*>(d_scratch);
+    a.done = a.keys + (size_t)B * kBlock;
+    a.slots = nullptr;
+    LookupDev none = {};
+    return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
+}
+
+extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
+                                 int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                                 const int32_t* d_block, const int32_t* d_len, int32_t* d_argmax, int32_t* d_accept,
+                                 int32_t* d_emitted, int32_t* d_out_tok, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    rc = verify_check(d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_argmax, d_accept, d_emitted,
+                      d_out_tok);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots)) return CLK_EINVAL;
+    VerifyArgs a;
+    a.logits = d_logits;
+    a.row_stride = row_stride;
+    a.req_stride = req_stride;
+    a.V = V;
+    a.B = B;
+    a.block = d_block;
+    a.len = d_len;
+    a.argmax = d_argmax;
+    a.accept = d_accept;
+    a.emitted = d_emitted;
+    a.out_tok = d_out_tok;
+    a.keys = h->dev.vkeys;
+    a.done = h->dev.vdone;
+    a.slots = d_slots;
+    return verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
+}

@@ -81,6 +81,7 @@ class RunArgs(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("gen_ctx", _P), ("logits_fn", _P), ("head_fn", _P),
                 ("rec_k", _P), ("rec_j", _P), ("rec_L", _P), ("rec_a", _P), ("rec_c", _P), ("rec_blk", _P),
                 ("rec_g", _P), ("hist_out", _P), ("hist_off", _P), ("hist_len", _P), ("counters", _P),
+                ("timed_from", ctypes.c_int32), ("pad", ctypes.c_int32),
                 ("method_ns", ctypes.c_int64), ("provider_ns", ctypes.c_int64)]
 
 
@@ -192,13 +193,15 @@ class RunResult:
 
 
 def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
-        params: Optional[Params] = None, threads: Optional[int] = None, head=None) -> RunResult:
+        params: Optional[Params] = None, threads: Optional[int] = None, head=None,
+        timed_from: int = 0) -> RunResult:
     """Run the oracle decode loop of workload `w` for the given requests.
 
     The target logits and head proposals come from the host generator of the
     `workload` package (keyed by the original request ids).  `head`, if
     given, replaces the head proposals: a Python callable (b, t, n) -> 7
-    tokens (small tests only: it runs under the GIL)."""
+    tokens (small tests only: it runs under the GIL).  `timed_from`: the
+    first step counted in method_s / provider_s (per-thread sums)."""
     import workload as wl  # the seeded input generator shared by both sides
 
     p = params or Params.default()
@@ -248,10 +251,14 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     args.hist_off = hoff.ctypes.data
     args.hist_len = hlen.ctypes.data
     args.counters = ctypes.cast(counters, _P)
+    args.timed_from = int(timed_from)
+    import time as _time
+    t0 = _time.perf_counter()
     rc = _lib().or_run(ctypes.byref(args))
+    wall = _time.perf_counter() - t0
     if rc != 0:
         raise RuntimeError(f"oracle run failed ({rc})")
     histories = [hist[hoff[i]:hoff[i] + hlen[i]].copy() for i in range(n)]
     return RunResult(req_ids=req_ids, steps=steps, threads=threads, histories=histories,
                      counters=[counters[i].as_dict() for i in range(n)],
-                     method_s=args.method_ns * 1e-9, provider_s=args.provider_ns * 1e-9, **rec)
+                     method_s=args.method_ns * 1e-9, provider_s=args.provider_ns * 1e-9, wall_s=wall, **rec)

@@ -253,7 +253,10 @@ typedef struct or_run_args {
     const int64_t* hist_off;    /* n_req + 1 */
     int64_t* hist_len;          /* n_req */
     or_counters* counters;      /* n_req */
-    /* timing (filled): nanoseconds in the method's own work and in the providers */
+    /* timing: steps before timed_from are not timed; then nanoseconds in the
+     * method's own work and in the providers (filled) */
+    int32_t timed_from;
+    int32_t pad;
     int64_t method_ns;
     int64_t provider_ns;
 } or_run_args;
@@ -295,9 +298,13 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
     const int32_t long_L = 1 + p->head + p->tail;
     int rc = 0;
 
-    const int64_t start_ns = or_now_ns();
+    int64_t start_ns = or_now_ns();
     int64_t prov = 0;
     for (int32_t t = 0; t < a->steps; ++t) {
+        if (t == a->timed_from) {
+            start_ns = or_now_ns();
+            prov = 0;
+        }
         int32_t c[OR_BLOCK], m[OR_BLOCK], blk[OR_BLOCK], g[OR_BLOCK];
         int64_t j;
         int32_t k = or_lookup(h, n, p->min_k, p->max_k, &j);

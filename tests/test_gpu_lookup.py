@@ -1,0 +1,162 @@
+"""Lookup on the GPU (index build, incremental append, proposal) against the
+oracle's full scan, element by element; error latching.  GPU."""
+import numpy as np
+import pytest
+import torch
+
+import context_lookup_speculative_gb300 as clk
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _csr(arrays):
+    off = np.zeros(len(arrays) + 1, np.int64)
+    off[1:] = np.cumsum([a.size for a in arrays])
+    tok = np.concatenate(arrays).astype(np.int32) if arrays else np.zeros(0, np.int32)
+    return torch.from_numpy(tok).cuda(), torch.from_numpy(off).cuda()
+
+
+def _setup(hists, max_hist, slots=None, vocab=0, params=None):
+    B = len(hists)
+    slots = list(range(B)) if slots is None else slots
+    lk = clk.Lookup(max_slots=max(slots) + 1, max_hist=max_hist, vocab=vocab, params=params)
+    s = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    tok, off = _csr(hists)
+    clk.lookup_init(lk, s, tok, off)
+    return lk, s
+
+
+def _propose(lk, s):
+    B = s.numel()
+    d = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
+    k = torch.zeros(B, dtype=torch.int32, device="cuda")
+    j = torch.zeros(B, dtype=torch.int32, device="cuda")
+    clk.lookup_propose(lk, s, d, k, j)
+    torch.cuda.synchronize()
+    return d.cpu().numpy(), k.cpu().numpy(), j.cpu().numpy()
+
+
+def _expect(hists, params=None):
+    return [oracle.propose(h, params) for h in hists]
+
+
+def _assert_same(got, hists, params=None):
+    d, k, j = got
+    for b, (c, kk, jj) in enumerate(_expect(hists, params)):
+        assert (k[b], j[b]) == (kk, jj), (b, hists[b][-16:], (k[b], j[b]), (kk, jj))
+        assert d[b].tolist() == c.tolist(), b
+
+
+def test_random_small_vocab_histories():
+    rng = np.random.default_rng(51)
+    hists = [rng.integers(0, int(rng.integers(2, 6)), size=int(rng.integers(1, 400))).astype(np.int32)
+             for _ in range(200)]
+    lk, s = _setup(hists, 512)
+    _assert_same(_propose(lk, s), hists)
+    assert lk.status() == (0, 0)
+
+
+def test_periodic_and_planted_histories():
+    rng = np.random.default_rng(52)
+    hists = []
+    for p in range(1, 41):
+        pat = rng.integers(0, 32000, size=p).astype(np.int32)
+        n = int(rng.integers(p + 1, 3000))
+        h = pat[np.arange(n) % p].copy()
+        noise = rng.random(n) < 0.05
+        h[noise] = rng.integers(0, 32000, size=int(noise.sum()))
+        hists.append(h)
+    for _ in range(40):
+        n = int(rng.integers(1000, 20000))
+        h = rng.zipf(1.3, size=n).astype(np.int64) % 248320
+        src = int(rng.integers(0, n // 2))
+        ln = int(rng.integers(1, 30))
+        h[n - ln:] = h[src:src + ln]
+        hists.append(h.astype(np.int32))
+    lk, s = _setup(hists, 20000)
+    _assert_same(_propose(lk, s), hists)
+
+
+def test_incremental_append_matches_full_scan():
+    """Grow histories by random counts of tokens; after every append the
+    proposal equals the oracle's full scan of the accumulated history."""
+    rng = np.random.default_rng(53)
+    B = 24
+    hists = [rng.integers(0, 4, size=int(rng.integers(1, 30))).astype(np.int32) for _ in range(B)]
+    lk, s = _setup(hists, 30 + 16 * 60, slots=[3 * b + 1 for b in range(B)])
+    for step in range(60):
+        cnt = rng.integers(0, 17, size=B).astype(np.int32)
+        tok = rng.integers(0, 4 if step % 3 else 2, size=(B, 16)).astype(np.int32)
+        # periodic bursts so long matches and overlaps occur
+        for b in range(0, B, 4):
+            tok[b] = np.resize(hists[b][-3:], 16)
+        clk.lookup_append(lk, s, torch.from_numpy(tok).cuda(), torch.from_numpy(cnt).cuda())
+        hists = [np.concatenate([h, tok[b, :cnt[b]]]) for b, h in enumerate(hists)]
+        _assert_same(_propose(lk, s), hists)
+    for b in range(B):
+        assert np.array_equal(lk.history(3 * b + 1), hists[b])
+    assert lk.status() == (0, 0)
+
+
+def test_other_match_ranges():
+    rng = np.random.default_rng(54)
+    for lo, hi in ((1, 3), (2, 16), (6, 9)):
+        p = clk.Params.default(min_k=lo, max_k=hi)
+        po = oracle.Params.default(min_k=lo, max_k=hi)
+        hists = [rng.integers(0, 3, size=int(rng.integers(1, 200))).astype(np.int32) for _ in range(50)]
+        lk, s = _setup(hists, 256, params=p)
+        _assert_same(_propose(lk, s), hists, po)
+
+
+def test_capacity_overflow_is_latched_and_skipped():
+    hists = [np.array([1, 2, 3, 4, 5], np.int32), np.array([7, 7, 7], np.int32)]
+    lk, s = _setup(hists, 20)
+    tok = torch.arange(32, dtype=torch.int32, device="cuda").reshape(2, 16)
+    cnt = torch.tensor([16, 16], dtype=torch.int32, device="cuda")
+    clk.lookup_append(lk, s, tok, cnt)   # slot 0 -> 21 > 20: refused; slot 1 -> 19: fine
+    st, det = lk.status()
+    assert st == clk.ECAPACITY and det == 0
+    assert lk.history(0).tolist() == [1, 2, 3, 4, 5]
+    assert lk.history(1).size == 19
+    lk.status_clear()
+    assert lk.status() == (0, 0)
+
+
+def test_bad_inputs_are_latched():
+    lk, s = _setup([np.array([1, 2, 3], np.int32)], 64, vocab=10)
+    tok = torch.full((1, 16), 12, dtype=torch.int32, device="cuda")   # outside [0, vocab)
+    clk.lookup_append(lk, s, tok, torch.tensor([2], dtype=torch.int32, device="cuda"))
+    assert lk.status()[0] == clk.EINVAL
+    assert lk.history(0).tolist() == [1, 2, 3]
+    lk.status_clear()
+    clk.lookup_append(lk, s, tok, torch.tensor([17], dtype=torch.int32, device="cuda"))  # count > 16
+    assert lk.status()[0] == clk.EINVAL
+    lk.status_clear()
+    # an empty prompt leaves the slot empty; proposing from it is a state error
+    lk2, s2 = _setup([np.array([], np.int32), np.array([4, 4, 4, 4, 4, 4], np.int32)], 64)
+    assert lk2.status()[0] == clk.EINVAL
+    lk2.status_clear()
+    d, k, j = _propose(lk2, s2)
+    assert lk2.status()[0] == clk.ESTATE
+    assert k.tolist() == [0, 5] and j.tolist() == [-1, 5]
+    # a prompt longer than max_hist
+    lk3, _ = _setup([np.arange(70, dtype=np.int32)], 64)
+    assert lk3.status()[0] == clk.ECAPACITY
+
+
+def test_long_history_index_build():
+    """A 262,144-token copy-heavy prompt: the index build and the proposal at
+    several points of it (truncated prompts share the prefix)."""
+    rng = np.random.default_rng(55)
+    n = 262144
+    base = (rng.zipf(1.1, size=n).astype(np.int64) % 248320).astype(np.int32)
+    for _ in range(200):
+        ln = int(rng.integers(1000, 8000))
+        src = int(rng.integers(0, n - ln))
+        dst = int(rng.integers(src + ln, n - ln + 1)) if src + ln < n - ln else src
+        base[dst:dst + ln] = base[src:src + ln]
+    cuts = [n, n - 1, n - 5000, 200000, 150001, 77777]
+    hists = [base[:c].copy() for c in cuts]
+    lk, s = _setup(hists, n + 64)
+    _assert_same(_propose(lk, s), hists)

@@ -1,0 +1,73 @@
+"""Whole decode loop on the GPU against the oracle, bit-exact on every
+per-step field (k, j, L, draft, block, argmax rows, accepted count), the
+final histories and the counters.  The full-size workloads run in the launch
+configuration the benchmark times (the fused two-kernel step).  GPU."""
+import os
+
+import pytest
+
+import context_lookup_speculative_gb300 as clk
+import oracle
+import workload as wl
+from workload import drive
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 1
+
+
+def _parity(w, steps=None, params=None, oparams=None, mode="fused", req_ids=None):
+    dev = drive.run_device(w, steps=steps, params=params, mode=mode)
+    ref = oracle.run(w, req_ids=req_ids, steps=steps, params=oparams, threads=THREADS)
+    msgs = drive.compare(dev, ref, req_ids=req_ids)
+    assert not msgs, "\n".join(msgs[:8])
+    return dev, ref
+
+
+@pytest.mark.parametrize("mode", ["fused", "semi", "unfused"])
+@pytest.mark.parametrize("kind", ["mixed", "periodic", "copy", "chat"])
+def test_small_workloads_all_modes(kind, mode):
+    w = wl.make_small(kind, seed=71, B=6, V=4096, steps=64)
+    _parity(w, mode=mode)
+
+
+@pytest.mark.parametrize("sticky", [0, 1, 3, 6])
+def test_sticky_variants(sticky):
+    w = wl.make_small("mixed", seed=72, B=8, V=2048, steps=96)
+    _parity(w, params=clk.Params.default(sticky=sticky), oparams=oracle.Params.default(sticky=sticky))
+
+
+def test_fp32_and_block_variants():
+    w = wl.make_small("copy", seed=73, B=4, V=1024, steps=64, dtype=wl.F32)
+    _parity(w)
+    kw = dict(head=3, tail=12, head_agree_n=1, head_replace_k=5)  # head <= the 7 synthetic proposals
+    _parity(w, params=clk.Params.default(**kw), oparams=oracle.Params.default(**kw))
+
+
+def test_config0_tiny():
+    _parity(wl.make("0"))
+
+
+def test_config1_restatement_25k():
+    _parity(wl.make("1"))
+
+
+def test_config2_mixed_b64():
+    dev, ref = _parity(wl.make("2"))
+    assert (ref.L == 16).any() and (ref.L == 8).any()
+
+
+def test_config3_periodic():
+    dev, ref = _parity(wl.make("3"))
+    # the noise drives flag drops, sticky exits and re-entries
+    import numpy as np
+    L = ref.L
+    assert ((L[1:] == 8) & (L[:-1] == 16)).any() and ((L[1:] == 16) & (L[:-1] == 8)).any()
+    assert (np.asarray(ref.j) > np.asarray(ref.k)).any()
+
+
+def test_config4a_long_262k():
+    _parity(wl.make("4a"))
+
+
+def test_config4b_b256():
+    _parity(wl.make("4b"))

@@ -1,0 +1,193 @@
+"""Greedy verification on the GPU against the oracle, element by element.
+
+Covers ragged block lengths, several tiles per row and a ragged tail, the
+bf16 vector path, the fp32 path, the unaligned (scalar) path, hand-built
+tie / signed-zero / infinity / NaN / last-bit rows placed so that equal
+maxima fall in different CTAs, invalid lengths, and scratch reuse.  GPU."""
+import numpy as np
+import pytest
+import torch
+
+import context_lookup_speculative_gb300 as clk
+import oracle
+import workload as wl
+
+pytestmark = pytest.mark.gpu
+SENT = -1
+
+
+def _oracle_rows(x_np, block, L):
+    B = block.shape[0]
+    g = np.full((B, 16), SENT, np.int32)
+    a = np.zeros(B, np.int32)
+    out = np.full((B, 16), SENT, np.int32)
+    e = np.zeros(B, np.int32)
+    for b in range(B):
+        if not 1 <= L[b] <= 16:
+            continue
+        for r in range(L[b]):
+            g[b, r] = oracle.argmax_row(x_np[b, r])
+        a[b] = oracle.accept(block[b], g[b], int(L[b]))
+        out[b, :a[b] + 1] = g[b, :a[b] + 1]
+        e[b] = a[b] + 1
+    return g, a, e, out
+
+
+def _gpu(logits, block, L, scratch=None):
+    B = block.shape[0]
+    dev = logits.device
+    blk = torch.from_numpy(block).to(dev)
+    ln = torch.from_numpy(L.astype(np.int32)).to(dev)
+    z = lambda *s: torch.full(s, 99, dtype=torch.int32, device=dev)  # noqa: E731
+    g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+    scratch = clk.verify_scratch(B) if scratch is None else scratch
+    clk.verify_greedy(logits, blk, ln, g, a, e, out, scratch)
+    torch.cuda.synchronize()
+    return g.cpu().numpy(), a.cpu().numpy(), e.cpu().numpy(), out.cpu().numpy()
+
+
+def _np_view(logits):
+    if logits.dtype == torch.bfloat16:
+        return logits.view(torch.int16).cpu().numpy().view(np.uint16)
+    return logits.cpu().numpy()
+
+
+def _blocks_from(x_np, L, rng, p_agree=0.8):
+    """Blocks whose drafts agree with the true argmax with probability p_agree."""
+    B = L.size
+    block = rng.integers(0, x_np.shape[2], size=(B, 16)).astype(np.int32)
+    for b in range(B):
+        for r in range(min(15, x_np.shape[1] - 1)):
+            if rng.random() < p_agree:
+                block[b, r + 1] = oracle.argmax_row(x_np[b, r])
+    return block
+
+
+def _check(logits, L, rng, **kw):
+    x_np = _np_view(logits)
+    block = _blocks_from(x_np, L, rng, **kw)
+    got = _gpu(logits, block, L)
+    want = _oracle_rows(x_np, block, L)
+    for name, gg, ww in zip(("argmax", "accept", "emitted", "out_tok"), got, want):
+        assert np.array_equal(gg, ww), (name, gg, ww)
+
+
+@pytest.mark.parametrize("V", [8, 1000, 4096, 32000, 248320, 248321])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_seeded_rows(V, dtype):
+    rng = np.random.default_rng(V)
+    B = 5
+    x = torch.from_numpy(rng.standard_normal((B, 16, V)).astype(np.float32)).to("cuda").to(dtype)
+    L = rng.integers(1, 17, size=B)
+    _check(x, L, rng)
+
+
+def test_ragged_batch_of_300():
+    rng = np.random.default_rng(3)
+    B, V = 300, 4096
+    # coarse values: many exact ties inside each row
+    x = torch.from_numpy(rng.integers(-20, 20, size=(B, 16, V)).astype(np.float32)).to("cuda").to(torch.bfloat16)
+    L = rng.choice([8, 16, 1, 2, 15], size=B)
+    _check(x, L, rng, p_agree=0.95)
+
+
+def test_generator_rows_full_width():
+    """The synthetic target's bf16 rows at V = 248,320, all 16 rows."""
+    w = wl.make_small("mixed", seed=41, B=4, V=248320, steps=4)
+    gen = wl.DevGen(w)
+    x = gen.alloc_logits()
+    gen.logits(x)
+    rng = np.random.default_rng(41)
+    _check(x, np.array([16, 8, 16, 3]), rng, p_agree=0.97)
+
+
+def _hand_rows(V, dtype):
+    ninf = float("-inf")
+    rows = np.zeros((10, V), np.float32)
+    rows[0, :] = 1.0                                   # all equal -> 0
+    rows[1, :] = (np.arange(V) % 97).astype(np.float32) / 128.0
+    rows[1, V - 1] = 2.0                               # max at the last index
+    rows[2, :] = -1.0
+    rows[2, [5, V // 2, V - 3]] = 3.0                  # equal maxima far apart -> 5
+    rows[3, :] = -1.0
+    rows[3, 7] = -0.0
+    rows[3, V - 9] = 0.0                               # -0 == +0 -> 7
+    rows[4, :] = ninf                                  # all -inf -> 0
+    rows[5, :] = ninf
+    rows[5, V - 1] = -5.0                              # -> V-1
+    rows[6, :] = 0.5
+    rows[6, V // 3] = np.inf
+    rows[6, V - 2] = np.nan                            # NaN beats +inf -> V-2
+    rows[7, :] = 0.0
+    rows[7, [3, V - 5]] = np.nan                       # first NaN -> 3
+    rows[8, :] = -2.0
+    rows[8, [11, V - 11]] = np.inf                     # -> 11
+    rows[9, :] = 0.25
+    expect = [0, V - 1, 5, 7, 0, V - 1, V - 2, 3, 11, None]
+    x = torch.from_numpy(rows)
+    if dtype == torch.bfloat16:
+        xb = x.to(torch.bfloat16)
+        bits = xb.view(torch.int16)
+        bits[9, 100] = 0x3E81   # 0.251953125: one mantissa bit above 0.25 (0x3E80)
+        bits[9, V - 7] = 0x3E81
+        expect[9] = 100
+        return xb, expect
+    x[9, 100] = float(np.nextafter(np.float32(0.25), np.float32(1.0)))
+    expect[9] = 100
+    return x, expect
+
+
+@pytest.mark.parametrize("V", [4096, 248320, 4099])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_hand_rows(V, dtype):
+    rows, expect = _hand_rows(V, dtype)
+    B = 10
+    x = torch.zeros((B, 16, V), dtype=dtype)
+    x[:, 0, :] = rows
+    x = x.to("cuda")
+    L = np.ones(B, np.int64)
+    block = np.full((B, 16), -1, np.int32)
+    g, a, e, out = _gpu(x, block, L)
+    assert g[:, 0].tolist() == expect
+    # and the oracle agrees on every one of them
+    want = _oracle_rows(_np_view(x), block, L)
+    assert np.array_equal(g, want[0])
+
+
+def test_invalid_lengths_give_empty_outputs():
+    rng = np.random.default_rng(5)
+    x = torch.randn((4, 16, 512), device="cuda").to(torch.bfloat16)
+    L = np.array([0, 17, 8, -3])
+    block = np.zeros((4, 16), np.int32)
+    g, a, e, out = _gpu(x, block, L)
+    for b in (0, 1, 3):
+        assert (g[b] == SENT).all() and (out[b] == SENT).all() and a[b] == 0 and e[b] == 0
+    assert e[2] >= 1
+
+
+def test_strided_and_unaligned_views():
+    """Rows that are slices of a wider buffer (the scalar path) give the same answers."""
+    rng = np.random.default_rng(6)
+    base = torch.randn((3, 16, 4100), device="cuda").to(torch.bfloat16)
+    x = base[:, :, 3:3 + 4093]           # row start not 16-byte aligned, V odd
+    assert x.stride(2) == 1
+    L = np.array([16, 5, 9])
+    x_np = _np_view(x.contiguous())
+    block = _blocks_from(x_np, L, rng)
+    got = _gpu(x, block, L)
+    want = _oracle_rows(x_np, block, L)
+    for gg, ww in zip(got, want):
+        assert np.array_equal(gg, ww)
+
+
+def test_scratch_is_left_clean_for_reuse():
+    rng = np.random.default_rng(7)
+    x = torch.randn((6, 16, 32000), device="cuda").to(torch.bfloat16)
+    L = rng.integers(1, 17, size=6)
+    block = _blocks_from(_np_view(x), L, rng)
+    scratch = clk.verify_scratch(6)
+    first = _gpu(x, block, L, scratch)
+    second = _gpu(x, block, L, scratch)
+    for f, s in zip(first, second):
+        assert np.array_equal(f, s)
+    assert int(scratch.count_nonzero()) == 0

@@ -474,6 +474,11 @@ class DevGen:
     def logits(self, out, pos=None):
         """Fill out[B, rows, V] for positions pos[b] + r (default: own pos)."""
         pos = self.pos if pos is None else pos
+        if out.dim() != 3 or out.shape[0] != self.w.B or out.shape[2] != self.w.V or out.shape[1] > ROWS \
+                or out.stride(2) != 1 or out.dtype != self.torch_dtype() or not out.is_cuda:
+            raise ValueError(f"logits buffer must be [{self.w.B}, <=16, {self.w.V}] {self.torch_dtype()} on the GPU")
+        if pos.shape != (self.w.B,) or pos.dtype != self.torch.int64:
+            raise ValueError("pos must be int64 [B]")
         rc = self.lib.wl_dev_logits(ctypes.addressof(self.ctx), pos.data_ptr(), out.data_ptr(),
                                     out.stride(1), out.stride(0), out.shape[1], self._stream())
         if rc != 0:
@@ -481,13 +486,21 @@ class DevGen:
         return out
 
     def head(self, t: int, out, pos=None):
+        """Fill out[B, 7] (contiguous int32) with step t's head proposals."""
         pos = self.pos if pos is None else pos
+        if tuple(out.shape) != (self.w.B, HEAD) or out.dtype != self.torch.int32 or not out.is_contiguous() \
+                or not out.is_cuda:
+            raise ValueError(f"head buffer must be contiguous int32 [{self.w.B}, {HEAD}] on the GPU")
+        if pos.shape != (self.w.B,) or pos.dtype != self.torch.int64:
+            raise ValueError("pos must be int64 [B]")
         rc = self.lib.wl_dev_head(ctypes.addressof(self.ctx), pos.data_ptr(), t, out.data_ptr(), self._stream())
         if rc != 0:
             raise RuntimeError(f"wl_dev_head failed ({rc})")
         return out
 
     def advance(self, emitted):
+        if emitted.shape != (self.w.B,) or emitted.dtype != self.torch.int32 or not emitted.is_contiguous():
+            raise ValueError("emitted must be contiguous int32 [B]")
         rc = self.lib.wl_dev_advance(self.pos.data_ptr(), emitted.data_ptr(), self.w.B, self._stream())
         if rc != 0:
             raise RuntimeError(f"wl_dev_advance failed ({rc})")
