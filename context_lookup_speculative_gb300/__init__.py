@@ -101,6 +101,7 @@ _SIGS = [
     ("clk_verify_scratch_init", ctypes.c_int, [_P, ctypes.c_size_t, _P]),
     ("clk_verify_greedy", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
+    ("clk_verify_greedy_static", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     ("clk_verify_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
     ("clk_status_clear", ctypes.c_int, [_P, _P]),
@@ -310,6 +311,18 @@ def verify_greedy(logits, block, length, argmax, accept, emitted, out_tok, scrat
                                    _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
                                    _ptr(out_tok, shape=(B, BLOCK)), _ptr(scratch, torch.uint8, name="scratch"),
                                    scratch.numel(), _stream(stream)))
+
+
+def verify_greedy_static(logits, block, length, argmax, accept, emitted, out_tok, stream=None):
+    """verify_greedy with the library's own fixed scratch (no buffer from the
+    caller, nothing allocated); B <= 1024; calls must not overlap on the GPU."""
+    dt, rs, qs, V = _logits_args(logits)
+    B = block.shape[0]
+    _check("clk_verify_greedy_static",
+           lib().clk_verify_greedy_static(logits.data_ptr(), dt, rs, qs, V, B, _ptr(block, shape=(B, BLOCK)),
+                                          _ptr(length, shape=(B,)), _ptr(argmax, shape=(B, BLOCK)),
+                                          _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
+                                          _ptr(out_tok, shape=(B, BLOCK)), _stream(stream)))
 
 
 def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None):

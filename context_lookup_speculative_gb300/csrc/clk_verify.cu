@@ -493,3 +493,74 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.slots = d_slots;
     return verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
 }
+
+// ---------------------------------------------------------------------------
+// Verification with library-owned scratch, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+// The scratch of clk_verify_greedy_static lives in this fixed device array
+// instead of a caller buffer.  Every GPU that loads the library holds it
+// until the process exits.  Device code could name it directly; host code
+// must not pass its name to a kernel (on the host it is only a stand-in), so
+// the entry point looks up its device address once per device.
+static __device__ __align__(256) unsigned long long
+    g_static_verify_scratch[(size_t)CLK_STATIC_VERIFY_MAX_BATCH * (kBlock + 1)];
+
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the static scratch on the current device (looked up on
+// the first call on that device), or nullptr on a CUDA error.
+void* static_scratch_on_current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
+        g_static_ptr[dev] = p;
+    }
+    return g_static_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                        int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                        int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted,
+                                        int32_t* d_out_tok, clk_stream_t s)
+{
+    int rc = verify_check(d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_argmax, d_accept,
+                          d_emitted, d_out_tok);
+    if (rc != CLK_OK) return rc;
+    if (B > CLK_STATIC_VERIFY_MAX_BATCH) return CLK_ECAPACITY;
+    if (B == 0) return CLK_OK;
+    void* scratch = static_scratch_on_current_device();
+    if (scratch == nullptr) return CLK_ECUDA;
+    // The array keeps whatever the previous call left in it: clear the part
+    // this call uses (the kernel needs its keys and counters at zero).
+    const size_t used = (size_t)B * (kBlock + 1) * sizeof(unsigned long long);
+    if (cudaMemsetAsync(scratch, 0, used, (cudaStream_t)s) != cudaSuccess) return CLK_ECUDA;
+    VerifyArgs a;
+    a.logits = d_logits;
+    a.row_stride = row_stride;
+    a.req_stride = req_stride;
+    a.V = V;
+    a.B = B;
+    a.block = d_block;
+    a.len = d_len;
+    a.argmax = d_argmax;
+    a.accept = d_accept;
+    a.emitted = d_emitted;
+    a.out_tok = d_out_tok;
+    a.keys = static_cast<unsigned long long*>(scratch);
+    a.done = a.keys + (size_t)B * kBlock;
+    a.slots = nullptr;
+    LookupDev none = {};
+    return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
+}

@@ -250,6 +250,28 @@ CLK_API int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t row_s
                               int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch,
                               size_t scratch_bytes, clk_stream_t s);
 
+/* clk_verify_greedy for callers that cannot allocate device memory at all:
+ * for example a plugin that is handed only its input and output pointers,
+ * or a serving engine whose free HBM is already committed to its own pools
+ * and which has no way to give this library a scratch buffer.  It takes
+ * the same arguments minus the scratch and computes the same outputs.  It
+ * allocates nothing: its scratch is a fixed array of
+ * CLK_STATIC_VERIFY_MAX_BATCH * 17 * 8 bytes (139,264 bytes) inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.  B above CLK_STATIC_VERIFY_MAX_BATCH returns CLK_ECAPACITY and
+ * launches nothing.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Each call clears the part of the array it uses on its
+ * stream and then launches the verify kernel.  All calls share the one
+ * array, so calls whose executions overlap on the GPU (other streams, other
+ * threads) race and corrupt each other's results: serialise them.  The
+ * pages describe no counterpart; this entry point exists for such callers. */
+#define CLK_STATIC_VERIFY_MAX_BATCH 1024
+CLK_API int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                     int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                     int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok,
+                                     clk_stream_t s);
+
 /* clk_verify_greedy followed by clk_lookup_append of its d_out_tok /
  * d_emitted, in one launch: the request's append runs as soon as its rows
  * are verified.  Uses the scratch inside the lookup workspace.  Bit-identical
