@@ -79,7 +79,7 @@ class Counters(ctypes.Structure):
 
 
 class SlotInfo(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("n", "mode", "streak", "miss", "has_prev", "cur_len")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("n", "mode", "streak", "miss", "has_prev", "cur_len", "n_indexed")]
 
 
 # (name, restype, argtypes) of every exported entry point

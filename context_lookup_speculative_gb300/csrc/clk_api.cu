@@ -224,6 +224,7 @@ extern "C" int clk_read_slot_info(clk_lookup* h, int32_t slot, clk_slot_info* ou
     out->miss = st.miss;
     out->has_prev = st.has_prev;
     out->cur_len = st.cur_len;
+    out->n_indexed = st.nidx;
     return CLK_OK;
 }
 

@@ -20,6 +20,15 @@
 // history length or its periodicity.  Entries are only ever inserted (the
 // history only grows), so concurrent inserts use a CAS to claim an empty
 // slot and an atomicMax on the same key to keep the largest q.
+//
+// Deferred inserts.  A slot records nidx, the history length up to which its
+// tables are complete: they hold every k-gram ending at q <= nidx - 2.  The
+// fused verify only writes the emitted tokens (n grows, nidx does not); the
+// next proposal launch indexes the pending end positions nidx-1 .. n-2 in
+// dedicated warps while its lookup warps check those pending positions
+// directly against the suffix (they are the most recent candidates) and the
+// tables for everything older.  The answer is the same as with a complete
+// index, and the insert latency leaves the verify kernel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -41,7 +50,8 @@ struct __align__(16) SlotState {
     int32_t miss;
     int32_t has_prev;
     int32_t cur_len;
-    int32_t pad0, pad1;
+    int32_t nidx;  // tables hold every k-gram ending at q <= nidx - 2
+    int32_t pad1;
     long long steps, hits, long_steps, drafted, accepted, emitted;
     long long accept_hist[2][16];
 };
@@ -146,32 +156,21 @@ __device__ __forceinline__ bool index_insert(unsigned long long* tab, uint64_t m
     return false;
 }
 
-// Most recent end position of k-gram w (hash H) in one table, or -1.
-__device__ __forceinline__ int32_t index_find(const unsigned long long* tab, uint64_t mask, uint64_t H,
-                                              const int32_t* h, const int32_t* w, int32_t k)
-{
-    const uint32_t fp = (uint32_t)(H >> 32);
-    uint64_t s = H & mask;
-    for (uint64_t probe = 0; probe <= mask; ++probe, s = (s + 1) & mask) {
-        unsigned long long cur = tab[s];
-        if (cur == 0ull) return -1;
-        if ((uint32_t)(cur >> 32) == fp) {
-            int32_t p = (int32_t)(uint32_t)cur - 1;
-            if (kgram_at(h, p, w, k)) return p;
-        }
-    }
-    return -1;
-}
+// ---------------------------------------------------------------------------
+// Step 3 (long-block scheduler).  sched_apply takes the slot's state fields
+// already loaded, stores the new state and counters, and returns the block
+// length; sched_update loads them first.
+// ---------------------------------------------------------------------------
+struct SchedFields {
+    int32_t mode, streak, miss, has_prev;
+};
 
-// ---------------------------------------------------------------------------
-// Step 3 (long-block scheduler) on one slot's state; returns the block length.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int32_t sched_update(const clk_params& p, SlotState* st, int32_t k, int32_t prev_a,
-                                                int32_t prev_len)
+__device__ __forceinline__ int32_t sched_apply(const clk_params& p, SlotState* st, SchedFields f, int32_t k,
+                                               int32_t prev_a, int32_t prev_len)
 {
     const bool flag = k >= p.tail_k;
-    const bool near_full = st->has_prev && prev_a >= prev_len - 1 - p.near_full_slack;
-    int32_t mode = st->mode, streak = st->streak, miss = st->miss;
+    const bool near_full = f.has_prev && prev_a >= prev_len - 1 - p.near_full_slack;
+    int32_t mode = f.mode, streak = f.streak, miss = f.miss;
     if (mode == kShort) {
         streak = (flag && near_full) ? streak + 1 : 0;
         if (streak >= p.enter_streak) {
@@ -196,6 +195,17 @@ __device__ __forceinline__ int32_t sched_update(const clk_params& p, SlotState* 
     st->long_steps += (len == long_len(p)) ? 1 : 0;
     st->drafted += p.head + ((len == long_len(p) && k >= p.tail_k) ? p.tail : 0);
     return len;
+}
+
+__device__ __forceinline__ SchedFields sched_load(const SlotState* st)
+{
+    return SchedFields{st->mode, st->streak, st->miss, st->has_prev};
+}
+
+__device__ __forceinline__ int32_t sched_update(const clk_params& p, SlotState* st, int32_t k, int32_t prev_a,
+                                                int32_t prev_len)
+{
+    return sched_apply(p, st, sched_load(st), k, prev_a, prev_len);
 }
 
 // ---------------------------------------------------------------------------
@@ -226,12 +236,14 @@ __device__ __forceinline__ int32_t fuse_slot(const clk_params& p, int32_t i, int
 }
 
 // ---------------------------------------------------------------------------
-// Block-wide append of `count` tokens (in shared memory) to one slot, with the
-// index inserts of every k-gram the new tokens complete.  All threads of the
-// block call it with the same arguments.  sm_win needs kBlock + kMaxK ints.
+// Commit of `count` tokens (in shared memory) to one slot: validation, the
+// history write, the new length and the step counters.  The k-grams that the
+// tokens complete are left for the index (nidx stays).  All threads of the
+// block call it with the same arguments; returns true if the tokens were
+// written (uniform across the block).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void block_append(const LookupDev& L, int32_t slot, const int32_t* sm_tok, int32_t count,
-                                             int32_t* sm_flag, int32_t* sm_win)
+__device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t slot, const int32_t* sm_tok,
+                                                    int32_t count, int32_t* sm_flag)
 {
     const int tid = threadIdx.x;
     SlotState* st = L.state + slot;
@@ -256,26 +268,40 @@ __device__ __forceinline__ void block_append(const LookupDev& L, int32_t slot, c
         sm_flag[1] = n;
     }
     __syncthreads();
-    if (!sm_flag[0]) {
-        __syncthreads();
-        return;
+    const bool ok = sm_flag[0] != 0;
+    if (ok) {
+        const int32_t n_old = sm_flag[1];
+        int32_t* h = hist_of(L, slot);
+        if (tid < count) h[n_old + tid] = sm_tok[tid];
+        if (tid == 0) {
+            st->n = n_old + count;
+            const int32_t len = st->cur_len;
+            if (len != 0 && count > 0) {
+                st->accepted += count - 1;
+                st->emitted += count;
+                if (count - 1 < 16) st->accept_hist[len == long_len(L.p) ? 1 : 0][count - 1] += 1;
+            }
+            st->cur_len = 0;
+        }
     }
-    const int32_t n_old = sm_flag[1];
-    const int32_t n_new = n_old + count;
-    int32_t* h = hist_of(L, slot);
-    const clk_params& p = L.p;
-    // Window of tokens the new k-grams read: positions [wlo, n_new - 1).
-    const int32_t wlo = max(0, n_old - p.max_k);
-    if (tid < count) h[n_old + tid] = sm_tok[tid];
-    if (tid < n_new - wlo) sm_win[tid] = (wlo + tid < n_old) ? h[wlo + tid] : sm_tok[wlo + tid - n_old];
     __syncthreads();
-    // New end positions q = n_old-1 .. n_new-2 become eligible.
-    const int32_t q_lo = max(n_old - 1, 0);
-    const int32_t nq = (n_new - 2) - q_lo + 1;
+    return ok;
+}
+
+// Index every k-gram (all levels) that ends at q in [q_lo, q_hi], reading the
+// tokens from the history.  Work items (q, level) are spread over the
+// `nthr` threads whose rank is `rank`.
+__device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, int32_t q_lo, int32_t q_hi,
+                                            int32_t rank, int32_t nthr)
+{
+    if (q_hi < q_lo) return;
+    const clk_params& p = L.p;
+    const int32_t* h = hist_of(L, slot);
     const uint64_t mask = L.tsize - 1;
-    for (int task = tid; task < nq * L.nlev; task += blockDim.x) {
-        const int32_t q = q_lo + task / L.nlev;
-        const int32_t lvl = task % L.nlev;
+    const int64_t tasks = (int64_t)(q_hi - q_lo + 1) * L.nlev;
+    for (int64_t task = rank; task < tasks; task += nthr) {
+        const int32_t q = q_lo + (int32_t)(task / L.nlev);
+        const int32_t lvl = (int32_t)(task % L.nlev);
         const int32_t k = p.min_k + lvl;
         if (q < k - 1) continue;
         int32_t w[kMaxK];
@@ -283,72 +309,13 @@ __device__ __forceinline__ void block_append(const LookupDev& L, int32_t slot, c
 #pragma unroll
         for (int l = 0; l < kMaxK; ++l) {
             if (l < k) {
-                w[l] = sm_win[q - l - wlo];
+                w[l] = __ldcg(h + q - l);
                 acc = kg_step(acc, w[l]);
             }
         }
         if (!index_insert(table_of(L, slot, lvl), mask, kg_final(acc, k), h, q, w, k))
             latch(L.status, CLK_ECAPACITY, slot);
     }
-    if (tid == 0) {
-        st->n = n_new;
-        const int32_t len = st->cur_len;
-        if (len != 0 && count > 0) {
-            st->accepted += count - 1;
-            st->emitted += count;
-            if (count - 1 < 16) st->accept_hist[len == long_len(p) ? 1 : 0][count - 1] += 1;
-        }
-        st->cur_len = 0;
-    }
-    __syncthreads();
-}
-
-// ---------------------------------------------------------------------------
-// Step 1 (lookup) for one request, one warp.  Lane i < kBlock receives draft
-// token i; every lane receives k, j and the last committed token.
-// ---------------------------------------------------------------------------
-struct ProposeOut {
-    int32_t k, j, c, last;  // c: this lane's draft token (lanes >= kBlock: CLK_SENT)
-};
-
-__device__ __forceinline__ ProposeOut warp_propose(const LookupDev& L, int32_t slot)
-{
-    const unsigned full = 0xFFFFFFFFu;
-    const int lane = threadIdx.x & 31;
-    const clk_params& p = L.p;
-    const int32_t n = L.state[slot].n;
-    const int32_t* h = hist_of(L, slot);
-    // Suffix tokens s[l] = h[n-1-l].
-    int32_t mine = (lane < p.max_k && n - 1 - lane >= 0) ? h[n - 1 - lane] : CLK_SENT;
-    int32_t s[kMaxK];
-#pragma unroll
-    for (int l = 0; l < kMaxK; ++l) s[l] = __shfl_sync(full, mine, l);
-    // Lane `lane` searches match length k = min_k + lane.
-    const int32_t k = p.min_k + lane;
-    const bool active = lane < L.nlev && n >= k + 1;
-    int32_t q = -1;
-    if (active) {
-        uint64_t acc = kHashSeed;
-#pragma unroll
-        for (int l = 0; l < kMaxK; ++l)
-            if (l < k) acc = kg_step(acc, s[l]);
-        q = index_find(table_of(L, slot, lane), L.tsize - 1, kg_final(acc, k), h, s, k);
-    }
-    const unsigned hit = __ballot_sync(full, q >= 0);
-    ProposeOut o;
-    o.last = s[0];
-    if (hit == 0u) {
-        o.k = 0;
-        o.j = -1;
-        o.c = CLK_SENT;
-        return o;
-    }
-    const int best = 31 - __clz((int)hit);
-    o.k = p.min_k + best;
-    o.j = __shfl_sync(full, q, best) + 1;
-    const int32_t period = n - o.j;
-    o.c = lane < kBlock ? h[o.j + (lane % period)] : CLK_SENT;
-    return o;
 }
 
 }  // namespace clk

@@ -45,6 +45,7 @@ __global__ void k_init_state(LookupDev L, const int32_t* __restrict__ slots, con
     }
     SlotState z = {};
     z.n = nn;
+    z.nidx = nn;  // k_build_index indexes the whole prompt
     *st = z;
 }
 
@@ -113,13 +114,14 @@ __global__ void k_build_index(LookupDev L, const int32_t* __restrict__ slots, co
     }
 }
 
-// One block per request: append d_tok[b][0..count) and index the new k-grams.
+// One block per request: append d_tok[b][0..count) and index every k-gram
+// not yet in the tables (the pending positions and the new ones).
 __global__ void k_append(LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ tok,
                          const int32_t* __restrict__ count)
 {
     __shared__ int32_t sm_tok[kBlock];
     __shared__ int32_t sm_flag[2];
-    __shared__ int32_t sm_win[kBlock + kMaxK];
+    __shared__ int32_t sm_nidx;
     const int32_t b = blockIdx.x;
     const int32_t slot = slots[b];
     if (slot < 0 || slot >= L.max_slots) {
@@ -128,8 +130,13 @@ __global__ void k_append(LookupDev L, const int32_t* __restrict__ slots, const i
     }
     const int32_t cnt = count[b];
     if (threadIdx.x < kBlock) sm_tok[threadIdx.x] = tok[(int64_t)b * kBlock + threadIdx.x];
+    if (threadIdx.x == 0) sm_nidx = L.state[slot].nidx;
     __syncthreads();
-    block_append(L, slot, sm_tok, cnt, sm_flag, sm_win);
+    if (!block_commit_tokens(L, slot, sm_tok, cnt, sm_flag)) return;
+    const int32_t n_new = sm_flag[1] + cnt;
+    index_range(L, slot, max(sm_nidx - 1, 0), n_new - 2, threadIdx.x, blockDim.x);
+    __syncthreads();
+    if (threadIdx.x == 0) L.state[slot].nidx = n_new;
 }
 
 __device__ __forceinline__ bool warp_slot(const LookupDev& L, const int32_t* slots, int32_t B, int32_t* b_out,
@@ -141,36 +148,6 @@ __device__ __forceinline__ bool warp_slot(const LookupDev& L, const int32_t* slo
     *b_out = b;
     *slot_out = slot;
     return true;
-}
-
-// Empty or invalid slot: latch and emit the no-match proposal.
-__device__ __forceinline__ bool slot_usable(const LookupDev& L, int32_t slot, int32_t b)
-{
-    if (slot < 0 || slot >= L.max_slots) {
-        if ((threadIdx.x & 31) == 0) latch(L.status, CLK_EINVAL, b);
-        return false;
-    }
-    if (L.state[slot].n < 1) {
-        if ((threadIdx.x & 31) == 0) latch(L.status, CLK_ESTATE, slot);
-        return false;
-    }
-    return true;
-}
-
-// One warp per request.
-__global__ void k_propose(LookupDev L, const int32_t* __restrict__ slots, int32_t B, int32_t* __restrict__ draft,
-                          int32_t* __restrict__ k_out, int32_t* __restrict__ j_out)
-{
-    int32_t b, slot;
-    if (!warp_slot(L, slots, B, &b, &slot)) return;
-    const int lane = threadIdx.x & 31;
-    ProposeOut o = {0, -1, CLK_SENT, CLK_SENT};
-    if (slot_usable(L, slot, b)) o = warp_propose(L, slot);
-    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = o.c;
-    if (lane == 0) {
-        k_out[b] = o.k;
-        j_out[b] = o.j;
-    }
 }
 
 // One thread per request.
@@ -189,13 +166,13 @@ __global__ void k_sched(LookupDev L, const int32_t* __restrict__ slots, int32_t 
     len[b] = sched_update(L.p, L.state + slot, k[b], pa, pl);
 }
 
-// Fusion of one request by one warp; lanes < kBlock write the block.
+// Fusion of one request by one warp; lanes < kBlock write the block.  Lane i
+// holds lookup draft token i (c_lane) and draft-model proposal i (m_lane).
 __device__ __forceinline__ void warp_fuse(const clk_params& p, int32_t last, int32_t c_lane, int32_t k,
-                                          const int32_t* __restrict__ head_row, int32_t len, int32_t* block_row)
+                                          int32_t m_lane, int32_t len, int32_t* block_row)
 {
     const unsigned full = 0xFFFFFFFFu;
     const int lane = threadIdx.x & 31;
-    const int32_t m_lane = lane < p.head ? head_row[lane] : CLK_SENT;
     const unsigned agree = __ballot_sync(full, lane < p.head && c_lane == m_lane);
     const bool take_head = fuse_take_head(p, k, agree);
     const bool fill_tail = fuse_fill_tail(p, k, len);
@@ -215,7 +192,8 @@ __global__ void k_fuse(clk_params p, int32_t B, const int32_t* __restrict__ last
     if (b >= B) return;
     const int lane = threadIdx.x & 31;
     const int32_t c_lane = lane < kBlock ? draft[(int64_t)b * kBlock + lane] : CLK_SENT;
-    warp_fuse(p, last_tok[b], c_lane, k[b], head + (int64_t)b * p.head, len[b], block + (int64_t)b * kBlock);
+    const int32_t m_lane = lane < p.head ? head[(int64_t)b * p.head + lane] : CLK_SENT;
+    warp_fuse(p, last_tok[b], c_lane, k[b], m_lane, len[b], block + (int64_t)b * kBlock);
 }
 
 // Scheduler then fusion: one warp per request.
@@ -244,31 +222,183 @@ __global__ void k_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int
         last = n >= 1 ? hist_of(L, slot)[n - 1] : CLK_SENT;
     }
     const int32_t c_lane = lane < kBlock ? draft[(int64_t)b * kBlock + lane] : CLK_SENT;
-    warp_fuse(L.p, last, c_lane, kk, head + (int64_t)b * L.p.head, l, block + (int64_t)b * kBlock);
+    const int32_t m_lane = lane < L.p.head ? head[(int64_t)b * L.p.head + lane] : CLK_SENT;
+    warp_fuse(L.p, last, c_lane, kk, m_lane, l, block + (int64_t)b * kBlock);
 }
 
-// Proposal, scheduler and fusion: one warp per request.
-__global__ void k_propose_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int32_t B,
-                                     const int32_t* __restrict__ head, const int32_t* prev_a,
-                                     const int32_t* prev_len, int32_t* __restrict__ draft, int32_t* __restrict__ k_out,
-                                     int32_t* __restrict__ j_out, int32_t* len, int32_t* __restrict__ block)
+constexpr int kMaxPending = 32;                  // pending end positions checked directly
+constexpr int kWin = kMaxPending + kMaxK + 1;    // window of history tokens in shared memory
+constexpr int kInsertWarps = 5;                  // warps that index the pending positions
+
+// Step 1 (and with FUSE, Steps 3 and 2) for one request per CTA.
+//   warps 0..nlev-1: one match length k = min_k + warp each.  The pending end
+//     positions (not yet in the tables) are checked against the suffix from a
+//     shared-memory window, most recent first; if none matches, the table of
+//     length k is probed, and one warp-wide load both verifies the stored
+//     occurrence token by token and fetches the 16 tokens that follow it.
+//   the last kInsertWarps warps: index the pending positions meanwhile.
+//   warp 0 then takes the longest level that matched (ballot), builds the
+//   LZ77 draft, and with FUSE runs the scheduler and the fusion rule.
+template <bool FUSE>
+__global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ head,
+                              const int32_t* prev_a, const int32_t* prev_len, int32_t* __restrict__ draft,
+                              int32_t* __restrict__ k_out, int32_t* __restrict__ j_out, int32_t* len_out,
+                              int32_t* __restrict__ block)
 {
-    int32_t b, slot;
-    if (!warp_slot(L, slots, B, &b, &slot)) return;
-    const int lane = threadIdx.x & 31;
-    const bool valid = slot >= 0 && slot < L.max_slots;
-    ProposeOut o = {0, -1, CLK_SENT, CLK_SENT};
-    if (slot_usable(L, slot, b)) o = warp_propose(L, slot);
-    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = o.c;
-    int32_t l = short_len(L.p);
-    if (lane == 0) {
-        k_out[b] = o.k;
-        j_out[b] = o.j;
-        if (valid) l = sched_update(L.p, L.state + slot, o.k, prev_a[b], prev_len[b]);
-        len[b] = l;
+    __shared__ int32_t sm_tok[kWin];
+    __shared__ int32_t sm_q[kMaxK];
+    __shared__ int32_t sm_follow[kMaxK][kBlock];
+    __shared__ int32_t sm_info[4];
+    const unsigned full = 0xFFFFFFFFu;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t b = blockIdx.x;
+    const clk_params& p = L.p;
+
+    // Inputs that do not depend on the history, loaded first.
+    int32_t m_lane = CLK_SENT, pa = 0, pl = 0;
+    SchedFields sf = {0, 0, 0, 0};
+    if (FUSE && warp == 0) {
+        if (lane < p.head) m_lane = head[(int64_t)b * p.head + lane];
+        if (lane == 0) {
+            pa = prev_a[b];
+            pl = prev_len[b];
+        }
     }
-    l = __shfl_sync(0xFFFFFFFFu, l, 0);
-    warp_fuse(L.p, o.last, o.c, o.k, head + (int64_t)b * L.p.head, l, block + (int64_t)b * kBlock);
+    if (tid == 0) {
+        const int32_t slot = slots[b];
+        int32_t ok = 1, n = 0, nidx = 0;
+        if (slot < 0 || slot >= L.max_slots) {
+            latch(L.status, CLK_EINVAL, b);
+            ok = 0;
+        } else {
+            const SlotState* st = L.state + slot;
+            n = st->n;
+            nidx = st->nidx;
+            sf = sched_load(st);
+            if (n < 1) {
+                latch(L.status, CLK_ESTATE, slot);
+                ok = 2;  // a valid but empty slot: no proposal, the scheduler still steps
+            }
+        }
+        sm_info[0] = slot;
+        sm_info[1] = n;
+        sm_info[2] = min(nidx, n);
+        sm_info[3] = ok;
+    }
+    if (tid < kMaxK) sm_q[tid] = -1;
+    __syncthreads();
+    const int32_t slot = sm_info[0], n = sm_info[1], ok = sm_info[3];
+    int32_t nidx = sm_info[2];
+    const int32_t* h = ok == 1 ? hist_of(L, slot) : nullptr;
+    if (ok == 1 && n - nidx > kMaxPending) {
+        // Many commits without a lookup in between: index them all first.
+        index_range(L, slot, max(nidx - 1, 0), n - 2, tid, blockDim.x);
+        nidx = n;
+        __syncthreads();
+    }
+    const int32_t pend_lo = max(nidx - 1, 0);         // first end position not in the tables
+    const int32_t wlo = max(0, pend_lo - (p.max_k - 1));  // window = history [wlo, n)
+    if (ok == 1 && tid < n - wlo) sm_tok[tid] = h[wlo + tid];
+    __syncthreads();
+
+    if (ok == 1) {
+        if (warp < L.nlev) {
+            const int32_t k = p.min_k + warp;
+            int32_t q = -1, fol = CLK_SENT;
+            if (n >= k + 1) {
+                const int32_t cand = n - 2 - lane;
+                bool m = cand >= max(pend_lo, k - 1);
+                for (int l = 0; m && l < k; ++l) m = sm_tok[cand - l - wlo] == sm_tok[n - 1 - l - wlo];
+                const unsigned hits = __ballot_sync(full, m);
+                if (hits) {
+                    q = n - 2 - (__ffs(hits) - 1);
+                } else {
+                    uint64_t acc = kHashSeed;
+                    for (int l = 0; l < k; ++l) acc = kg_step(acc, sm_tok[n - 1 - l - wlo]);
+                    const uint64_t H = kg_final(acc, k);
+                    const uint32_t fp = (uint32_t)(H >> 32);
+                    const uint64_t mask = L.tsize - 1;
+                    const unsigned long long* tab = table_of(L, slot, warp);
+                    const int32_t sl = lane < k ? sm_tok[n - 1 - lane - wlo] : 0;
+                    uint64_t sidx = H & mask;
+                    for (uint64_t probe = 0; probe <= mask; ++probe, sidx = (sidx + 1) & mask) {
+                        unsigned long long e = 0ull;
+                        if (lane == 0) e = tab[sidx];
+                        e = __shfl_sync(full, e, 0);
+                        if (e == 0ull) break;
+                        if ((uint32_t)(e >> 32) != fp) continue;
+                        const int32_t pp = (int32_t)(uint32_t)e - 1;
+                        bool same = true;
+                        if (lane < k) same = pp - lane >= 0 && h[pp - lane] == sl;
+                        int32_t f = CLK_SENT;
+                        if (lane >= 16 && pp + 1 + (lane - 16) < n) f = h[pp + 1 + (lane - 16)];
+                        if (__all_sync(full, same)) {
+                            q = pp;
+                            fol = f;
+                            break;
+                        }
+                    }
+                }
+            }
+            if (lane == 0) sm_q[warp] = q;
+            if (lane >= 16) sm_follow[warp][lane - 16] = fol;
+        } else if (n - 2 >= pend_lo) {
+            // Index the pending end positions, tokens from the window.
+            const int32_t rank = tid - L.nlev * 32, nthr = (int32_t)blockDim.x - L.nlev * 32;
+            const uint64_t mask = L.tsize - 1;
+            const int32_t tasks = (n - 1 - pend_lo) * L.nlev;
+            for (int32_t task = rank; task < tasks; task += nthr) {
+                const int32_t q = pend_lo + task / L.nlev;
+                const int32_t lvl = task % L.nlev;
+                const int32_t k = p.min_k + lvl;
+                if (q < k - 1) continue;
+                int32_t w[kMaxK];
+                uint64_t acc = kHashSeed;
+#pragma unroll
+                for (int l = 0; l < kMaxK; ++l) {
+                    if (l < k) {
+                        w[l] = sm_tok[q - l - wlo];
+                        acc = kg_step(acc, w[l]);
+                    }
+                }
+                if (!index_insert(table_of(L, slot, lvl), mask, kg_final(acc, k), h, q, w, k))
+                    latch(L.status, CLK_ECAPACITY, slot);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    if (ok == 1 && lane == 0) L.state[slot].nidx = n;
+    int32_t kbest = 0, j = -1, c = CLK_SENT;
+    if (ok == 1) {
+        const int32_t lv = lane < L.nlev ? sm_q[lane] : -1;
+        const unsigned hit = __ballot_sync(full, lv >= 0);
+        if (hit) {
+            const int best = 31 - __clz((int)hit);
+            const int32_t q = __shfl_sync(full, lv, best);
+            kbest = p.min_k + best;
+            j = q + 1;
+            if (lane < kBlock) {
+                const int32_t idx = lane % (n - j);  // LZ77 copy at distance n - j
+                c = q >= pend_lo ? sm_tok[j + idx - wlo] : sm_follow[best][idx];
+            }
+        }
+    }
+    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = c;
+    if (lane == 0) {
+        k_out[b] = kbest;
+        j_out[b] = j;
+    }
+    if (FUSE) {
+        int32_t l = short_len(p);
+        if (lane == 0) {
+            if (ok != 0) l = sched_apply(p, L.state + slot, sf, kbest, pa, pl);
+            len_out[b] = l;
+        }
+        l = __shfl_sync(full, l, 0);
+        const int32_t last = ok == 1 ? sm_tok[n - 1 - wlo] : CLK_SENT;
+        warp_fuse(p, last, c, kbest, m_lane, l, block + (int64_t)b * kBlock);
+    }
 }
 
 }  // namespace clk
@@ -320,7 +450,9 @@ extern "C" int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t
     if (rc != CLK_OK) return rc;
     if (B == 0) return CLK_OK;
     if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
-    k_propose<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_draft, d_k, d_j);
+    const unsigned threads = 32u * (unsigned)(h->dev.nlev + kInsertWarps);
+    k_lookup_step<false><<<B, threads, 0, (cudaStream_t)s>>>(h->dev, d_slots, nullptr, nullptr, nullptr, d_draft,
+                                                             d_k, d_j, nullptr, nullptr);
     return launch_status();
 }
 
@@ -376,7 +508,8 @@ extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int
         !ok_i32(d_prev_len) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j) || !ok_i32(d_len) ||
         !ok_i32(d_block))
         return CLK_EINVAL;
-    k_propose_fuse_sched<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_head, d_prev_accept,
-                                                                  d_prev_len, d_draft, d_k, d_j, d_len, d_block);
+    const unsigned threads = 32u * (unsigned)(h->dev.nlev + kInsertWarps);
+    k_lookup_step<true><<<B, threads, 0, (cudaStream_t)s>>>(h->dev, d_slots, d_head, d_prev_accept, d_prev_len,
+                                                            d_draft, d_k, d_j, d_len, d_block);
     return launch_status();
 }

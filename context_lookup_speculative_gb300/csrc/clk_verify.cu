@@ -2,22 +2,25 @@
 // paragraph; the Polish page's "the first rejected proposal ends the run"):
 // row-wise argmax over the target logits of each verify block, fused with the
 // accepted-prefix count, the emitted tokens and (clk_verify_append) the
-// commit of those tokens into the request's history and index.
+// commit of those tokens into the request's history (the next proposal
+// launch indexes them).
 //
 // Layout of the work: the rows that must be read (L_b rows of request b) are
 // numbered 0..R-1 in request order and seen as one flat range of R * V/W
 // 16-byte vectors (W elements each).  A grid of G CTAs, G = SMs x resident
 // CTAs, splits that range evenly; each CTA streams its contiguous share with
-// 128-bit loads (4 in flight per thread), reduces every row piece it covers
+// 128-bit loads (up to 8 in flight per thread), reduces every row piece it covers
 // to a packed (order-preserving value bits << 32 | ~index) 64-bit key, and
 // merges it into the row's key with one atomicMax (max value, then lowest
 // index; independent of CTA order).  Each CTA then adds the vectors it
 // covered to the request's counter; the CTA that completes a request (its
 // add reaches L_b * V/W) reads the row keys and finishes that request:
-// argmax tokens, accepted count, emitted tokens and, fused, the append.
+// argmax tokens, accepted count, emitted tokens and, fused, the token commit.
 // No CTA waits on another.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "clk.h"
 #include "clk_device.cuh"
@@ -66,6 +69,17 @@ __device__ __forceinline__ bool len_ok(int32_t l) { return l >= 1 && l <= kBlock
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ uint32_t hmax2_nan_u32(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x, y;
+    memcpy(&x, &a, 4);
+    memcpy(&y, &b, 4);
+    const __nv_bfloat162 m = __hmax2_nan(x, y);
+    uint32_t r;
+    memcpy(&r, &m, 4);
+    return r;
+}
+
 template <int DT>
 struct Elem;
 template <>
@@ -73,17 +87,18 @@ struct Elem<CLK_DTYPE_BF16> {
     using T = uint16_t;
     static constexpr int W = 8;
     __device__ static float value(T x) { return __uint_as_float((uint32_t)x << 16); }
-    // 8 values of a vector
     __device__ static void unpack(const uint4& v, float* f)
     {
         f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
         f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
     }
-    // Accumulates a word whose bit 15 or 31 ends up set iff the vector holds a NaN.
-    __device__ static uint32_t nan_bits(const uint4& v)
+    // Max of the 8 values by packed bf16x2 max that propagates NaN; any NaN of
+    // the vector sets bit 15 or 31 of `nanacc` (then the max value is unused).
+    __device__ static float vec_max(const uint4& v, uint32_t& nanacc)
     {
-        const uint32_t m = 0x7FFF7FFFu, c = 0x007F007Fu;
-        return ((v.x & m) + c) | ((v.y & m) + c) | ((v.z & m) + c) | ((v.w & m) + c);
+        const uint32_t m2 = hmax2_nan_u32(hmax2_nan_u32(v.x, v.y), hmax2_nan_u32(v.z, v.w));
+        nanacc |= (m2 & 0x7FFF7FFFu) + 0x007F007Fu;
+        return fmaxf(bf16_lo(m2), bf16_hi(m2));
     }
     static constexpr uint32_t kNanMask = 0x80008000u;
 };
@@ -97,72 +112,92 @@ struct Elem<CLK_DTYPE_F32> {
         f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
         f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
     }
-    __device__ static uint32_t nan_bits(const uint4& v)
+    __device__ static float vec_max(const uint4& v, uint32_t& nanacc)
     {
         const uint32_t m = 0x7FFFFFFFu, c = 0x007FFFFFu;
-        return ((v.x & m) + c) | ((v.y & m) + c) | ((v.z & m) + c) | ((v.w & m) + c);
+        nanacc |= ((v.x & m) + c) | ((v.y & m) + c) | ((v.z & m) + c) | ((v.w & m) + c);
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
     }
     static constexpr uint32_t kNanMask = 0x80000000u;
 };
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
-// This thread's packed key over vectors [v0, v1) of a row (vector path).
-template <int DT>
-__device__ __forceinline__ unsigned long long scan_vec(const void* row_ptr, int64_t v0, int64_t v1)
+// Loads vectors base + u * kVThreads (u < kUnroll) that lie below v1.
+// Vector indices inside a row fit in 32 bits (V < 2^31).
+__device__ __forceinline__ void load_group(const uint4* row, int32_t base, int32_t v1, uint4* x)
 {
-    using E = Elem<DT>;
-    constexpr int W = E::W;
-    const uint4* row = reinterpret_cast<const uint4*>(row_ptr);
-    const int64_t first = v0 + threadIdx.x;
-    if (first >= v1) return 0ull;
-    float best = -__int_as_float(0x7F800000);  // -inf
-    int64_t bvi = -1;
-    uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t nanacc = 0u;
-    for (int64_t base = first; base < v1; base += (int64_t)kUnroll * kVThreads) {
-        uint4 x[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = base + (int64_t)u * kVThreads;
-            if (vi < v1) x[u] = ld_stream(row + vi);
-        }
+    for (int u = 0; u < kUnroll; ++u) {
+        const int32_t vi = base + u * kVThreads;
+        if (vi < v1) x[u] = ld_stream(row + vi);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void reduce_group(const uint4* x, int32_t base, int32_t v1, float& best, int32_t& bvi,
+                                             uint4& bvec, uint32_t& nanacc)
+{
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = base + (int64_t)u * kVThreads;
-            if (vi < v1) {
-                float f[W];
-                E::unpack(x[u], f);
-                float m = f[0];
-#pragma unroll
-                for (int e = 1; e < W; ++e) m = fmaxf(m, f[e]);
-                nanacc |= E::nan_bits(x[u]);
-                if (m > best) {
-                    best = m;
-                    bvi = vi;
-                    bvec = x[u];
-                }
+    for (int u = 0; u < kUnroll; ++u) {
+        const int32_t vi = base + u * kVThreads;
+        if (vi < v1) {
+            const float m = Elem<DT>::vec_max(x[u], nanacc);
+            if (m > best) {
+                best = m;
+                bvi = vi;
+                bvec = x[u];
             }
         }
     }
+}
+
+// This thread's packed key over vectors [v0, v1) of a row (vector path).
+// Two register groups alternate: the next group's loads are issued before
+// the current group is reduced, so up to 2 x kUnroll 16-byte loads per
+// thread are in flight.  The index inside the winning vector is recovered
+// from the vector kept in registers.
+template <int DT>
+__device__ __forceinline__ unsigned long long scan_vec(const void* row_ptr, int32_t v0, int32_t v1)
+{
+    using E = Elem<DT>;
+    constexpr int W = E::W;
+    constexpr int32_t S = kUnroll * kVThreads;
+    const uint4* row = reinterpret_cast<const uint4*>(row_ptr);
+    const int32_t first = v0 + (int32_t)threadIdx.x;
+    if (first >= v1) return 0ull;
+    float best = -__int_as_float(0x7F800000);  // -inf
+    int32_t bvi = -1;
+    uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t nanacc = 0u;
+    uint4 a[kUnroll], b[kUnroll];
+    load_group(row, first, v1, a);
+    for (int32_t base = first; base < v1; base += 2 * S) {
+        load_group(row, base + S, v1, b);
+        reduce_group<DT>(a, base, v1, best, bvi, bvec, nanacc);
+        if (base + S >= v1) break;
+        load_group(row, base + 2 * S, v1, a);
+        reduce_group<DT>(b, base + S, v1, best, bvi, bvec, nanacc);
+    }
     if (nanacc & E::kNanMask) {
         // Rare path: the first NaN of this thread's elements.
-        for (int64_t vi = first; vi < v1; vi += kVThreads) {
+        for (int32_t vi = first; vi < v1; vi += kVThreads) {
             float f[W];
             E::unpack(row[vi], f);
 #pragma unroll
             for (int e = 0; e < W; ++e)
-                if (f[e] != f[e]) return pack_key(kNanKey, (uint32_t)(vi * W + e));
+                if (f[e] != f[e]) return pack_key(kNanKey, (uint32_t)vi * W + e);
         }
     }
-    if (bvi < 0) return pack_key(ord_key(best), (uint32_t)(first * W));  // every element is -inf
+    if (bvi < 0) return pack_key(ord_key(best), (uint32_t)first * W);  // every element is -inf
     float f[W];
     E::unpack(bvec, f);
     int e0 = W - 1;
 #pragma unroll
     for (int e = W - 1; e >= 0; --e)
         if (f[e] == best) e0 = e;
-    return pack_key(ord_key(best), (uint32_t)(bvi * W + e0));
+    return pack_key(ord_key(best), (uint32_t)bvi * W + e0);
 }
 
 // This thread's packed key over elements [v0, v1) of a row (unaligned rows).
@@ -251,7 +286,7 @@ __device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len
 }
 
 template <int DT, bool VEC, bool FUSED>
-__global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a, LookupDev L)
+__global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev L)
 {
     extern __shared__ int32_t sm_prefix[];  // B + 1
     __shared__ unsigned long long sm_red[kVWarps];
@@ -260,7 +295,6 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a, LookupDev L)
     __shared__ int32_t sm_count;
     __shared__ int32_t sm_tok[kBlock];
     __shared__ int32_t sm_flag[2];
-    __shared__ int32_t sm_win[kBlock + kMaxK];
     using E = Elem<DT>;
     const int tid = threadIdx.x;
     const int32_t B = a.B;
@@ -300,7 +334,7 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a, LookupDev L)
         const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
         const char* row = static_cast<const char*>(a.logits) +
                           ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(typename E::T);
-        unsigned long long key = VEC ? scan_vec<DT>(row, s0, s1) : scan_scalar<DT>(row, s0, s1);
+        unsigned long long key = VEC ? scan_vec<DT>(row, (int32_t)s0, (int32_t)s1) : scan_scalar<DT>(row, s0, s1);
         key = block_max_u64(key, sm_red);
         if (tid == 0) {
             atomicMax(a.keys + (int64_t)b * kBlock + r, key);
@@ -343,7 +377,7 @@ __global__ void __launch_bounds__(kVThreads) k_verify(VerifyArgs a, LookupDev L)
             if (FUSED) {
                 const int32_t slot = a.slots[b];
                 if (slot >= 0 && slot < L.max_slots) {
-                    block_append(L, slot, sm_tok, sm_count, sm_flag, sm_win);
+                    block_commit_tokens(L, slot, sm_tok, sm_count, sm_flag);
                 } else if (tid == 0) {
                     latch(L.status, CLK_EINVAL, b);
                 }

@@ -111,6 +111,8 @@ typedef struct clk_slot_info {
     int32_t miss;     /* consecutive flag-down steps while long */
     int32_t has_prev; /* a scheduler step has run since the slot was set up */
     int32_t cur_len;  /* block length chosen by the last scheduler step, 0 after append */
+    int32_t n_indexed; /* the index holds every k-gram ending before position n_indexed - 1; the
+                          positions committed since are indexed by the next proposal launch */
 } clk_slot_info;
 
 typedef struct clk_lookup clk_lookup; /* opaque host handle */
