@@ -254,6 +254,12 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
     const int32_t b = blockIdx.x;
     const clk_params& p = L.p;
 
+    // Launched as a programmatic dependent of the previous step's verify
+    // launch: wait for it (it commits the tokens this launch reads), then let
+    // this step's verify launch start streaming its first rows.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // Inputs that do not depend on the history, loaded first.
     int32_t m_lane = CLK_SENT, pa = 0, pl = 0;
     SchedFields sf = {0, 0, 0, 0};
@@ -401,6 +407,27 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
     }
 }
 
+// One CTA per request, launched as a programmatic dependent of the previous
+// launch in the stream (see k_lookup_step).
+template <bool FUSE>
+int launch_lookup_step(const LookupDev& L, const int32_t* slots, int32_t B, const int32_t* head,
+                       const int32_t* prev_a, const int32_t* prev_len, int32_t* draft, int32_t* k, int32_t* j,
+                       int32_t* len, int32_t* block, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(32u * (unsigned)(L.nlev + kInsertWarps));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, k_lookup_step<FUSE>, L, slots, head, prev_a, prev_len, draft, k, j,
+                                          len, block));
+}
+
 }  // namespace clk
 
 using namespace clk;
@@ -450,10 +477,8 @@ extern "C" int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t
     if (rc != CLK_OK) return rc;
     if (B == 0) return CLK_OK;
     if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
-    const unsigned threads = 32u * (unsigned)(h->dev.nlev + kInsertWarps);
-    k_lookup_step<false><<<B, threads, 0, (cudaStream_t)s>>>(h->dev, d_slots, nullptr, nullptr, nullptr, d_draft,
-                                                             d_k, d_j, nullptr, nullptr);
-    return launch_status();
+    return launch_lookup_step<false>(h->dev, d_slots, B, nullptr, nullptr, nullptr, d_draft, d_k, d_j, nullptr,
+                                     nullptr, (cudaStream_t)s);
 }
 
 extern "C" int clk_sched_step(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_k,
@@ -508,8 +533,6 @@ extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int
         !ok_i32(d_prev_len) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j) || !ok_i32(d_len) ||
         !ok_i32(d_block))
         return CLK_EINVAL;
-    const unsigned threads = 32u * (unsigned)(h->dev.nlev + kInsertWarps);
-    k_lookup_step<true><<<B, threads, 0, (cudaStream_t)s>>>(h->dev, d_slots, d_head, d_prev_accept, d_prev_len,
-                                                            d_draft, d_k, d_j, d_len, d_block);
-    return launch_status();
+    return launch_lookup_step<true>(h->dev, d_slots, B, d_head, d_prev_accept, d_prev_len, d_draft, d_k, d_j, d_len,
+                                    d_block, (cudaStream_t)s);
 }

@@ -245,18 +245,19 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
     return v;
 }
 
-// P[b] = rows of requests 0..b-1 (rows = L_b if 1 <= L_b <= 16, else 0); P[B] = R.
-__device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t* P,
+// Rows of request b past the first `base` rows: max(0, L_b - base) for a
+// valid length 1 <= L_b <= 16, else 0.
+__device__ __forceinline__ int32_t rows_after(int32_t l, int32_t base) { return len_ok(l) ? max(0, l - base) : 0; }
+
+// P[b] = rows_after(L_b', base) summed over requests b' < b; P[B] = total.
+__device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t base, int32_t* P,
                                                  int32_t* sm_warp)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t per = (B + kVThreads - 1) / kVThreads;
     const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) {
-        const int32_t l = len[b];
-        local += len_ok(l) ? l : 0;
-    }
+    for (int32_t b = b0; b < b1; ++b) local += rows_after(len[b], base);
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -278,32 +279,147 @@ __device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len
     int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
         P[b] = run;
-        const int32_t l = len[b];
-        run += len_ok(l) ? l : 0;
+        run += rows_after(len[b], base);
     }
     if (tid == kVThreads - 1) P[B] = sm_warp[kVWarps - 1];
     __syncthreads();
 }
 
-template <int DT, bool VEC, bool FUSED>
+struct VerifySmem {
+    unsigned long long red[kVWarps];
+    int32_t warp[kVWarps];
+    int32_t last;
+    int32_t count;
+    int32_t tok[kBlock];
+    int32_t flag[2];
+};
+
+// One row piece: this CTA's maximum over vectors [s0, s1) of row r of
+// request b, merged into the row's key.
+template <int DT, bool VEC>
+__device__ __forceinline__ void piece_max(const VerifyArgs& a, int32_t b, int32_t r, int64_t s0, int64_t s1,
+                                          VerifySmem& sm)
+{
+    using T = typename Elem<DT>::T;
+    const char* row = static_cast<const char*>(a.logits) +
+                      ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(T);
+    unsigned long long key = VEC ? scan_vec<DT>(row, (int32_t)s0, (int32_t)s1) : scan_scalar<DT>(row, s0, s1);
+    key = block_max_u64(key, sm.red);
+    if (threadIdx.x == 0) atomicMax(a.keys + (int64_t)b * kBlock + r, key);
+}
+
+// Request b is complete: argmax tokens, accepted count, emitted tokens; the
+// row keys and the counter go back to zero; fused, the tokens are committed.
+// Lb outside 1..16 gives the empty result.  Block-wide.
+template <bool FUSED>
+__device__ __forceinline__ void finalize(const VerifyArgs& a, const LookupDev& L, int32_t b, int32_t Lb,
+                                         VerifySmem& sm)
+{
+    const int tid = threadIdx.x;
+    __threadfence();
+    const bool valid = len_ok(Lb);
+    if (tid < 32) {
+        const int lane = tid;
+        unsigned long long* kp = a.keys + (int64_t)b * kBlock;
+        int32_t g = CLK_SENT;
+        if (valid && lane < Lb) {
+            const unsigned long long kv = atomicAdd(kp + lane, 0ull);
+            g = (int32_t)(0xFFFFFFFFu - (uint32_t)kv);
+        }
+        if (lane < kBlock) kp[lane] = 0ull;
+        const int32_t nxt = (lane + 1 < kBlock) ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
+        const unsigned match = __ballot_sync(0xFFFFFFFFu, valid && lane < Lb - 1 && nxt == g);
+        const int32_t acc = __ffs(~match) - 1;
+        const int32_t out = (valid && lane <= acc) ? g : CLK_SENT;
+        if (lane < kBlock) {
+            a.argmax[(int64_t)b * kBlock + lane] = g;
+            a.out_tok[(int64_t)b * kBlock + lane] = out;
+            sm.tok[lane] = out;
+        }
+        if (lane == 0) {
+            a.accept[b] = valid ? acc : 0;
+            a.emitted[b] = valid ? acc + 1 : 0;
+            a.done[b] = 0ull;
+            sm.count = valid ? acc + 1 : -1;
+        }
+    }
+    __syncthreads();
+    if (FUSED) {
+        const int32_t slot = a.slots[b];
+        if (sm.count < 0 || slot < 0 || slot >= L.max_slots) {
+            if (tid == 0) latch(L.status, CLK_EINVAL, b);
+        } else {
+            block_commit_tokens(L, slot, sm.tok, sm.count, sm.flag);
+        }
+    }
+}
+
+// Adds `add` verified vectors to request b; the CTA whose addition reaches
+// `need` finishes the request.  Block-wide.
+template <bool FUSED>
+__device__ __forceinline__ void piece_count(const VerifyArgs& a, const LookupDev& L, int32_t b, unsigned long long add,
+                                            unsigned long long need, int32_t Lb, VerifySmem& sm)
+{
+    if (threadIdx.x == 0) {
+        __threadfence();
+        sm.last = (atomicAdd(a.done + b, add) + add == need) ? 1 : 0;
+    }
+    __syncthreads();
+    if (sm.last) finalize<FUSED>(a, L, b, Lb, sm);
+    __syncthreads();
+}
+
+// Largest b with P[b] <= ri.
+__device__ __forceinline__ int32_t owner_of(const int32_t* P, int32_t B, int64_t ri)
+{
+    int32_t b = 0, top = B;
+    while (b < top) {
+        const int32_t mid = (b + top + 1) >> 1;
+        if (P[mid] <= ri) b = mid; else top = mid - 1;
+    }
+    return b;
+}
+
+// Verification of the rows counted by the prefix P (rows past `base` of each
+// request) split evenly over the grid; `need_rows(b)` is the total number of
+// rows request b reads in this launch.
+template <int DT, bool VEC, bool FUSED, typename NeedRows>
+__device__ __forceinline__ void verify_rows(const VerifyArgs& a, const LookupDev& L, const int32_t* P, int32_t base,
+                                            int64_t vpr, NeedRows need_rows, VerifySmem& sm)
+{
+    const int32_t B = a.B;
+    const int64_t total = (int64_t)P[B] * vpr;
+    int64_t lo = total * blockIdx.x / gridDim.x;
+    const int64_t hi = total * (blockIdx.x + 1) / gridDim.x;
+    if (lo >= hi) return;
+    int64_t ri = lo / vpr;
+    int32_t b = owner_of(P, B, ri);
+    while (lo < hi) {
+        while (P[b + 1] <= ri) ++b;
+        const int32_t r = base + (int32_t)(ri - P[b]);
+        const int64_t s0 = lo - ri * vpr;
+        const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
+        piece_max<DT, VEC>(a, b, r, s0, s1, sm);
+        const int32_t Lb = a.len[b];
+        piece_count<FUSED>(a, L, b, (unsigned long long)(s1 - s0),
+                           (unsigned long long)need_rows(b, Lb) * (unsigned long long)vpr, Lb, sm);
+        ri += 1;
+        lo = ri * vpr;
+    }
+}
+
+// Stateless verification (clk_verify_greedy): the block lengths are inputs,
+// so the rows to read are known at launch.
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev L)
 {
     extern __shared__ int32_t sm_prefix[];  // B + 1
-    __shared__ unsigned long long sm_red[kVWarps];
-    __shared__ int32_t sm_warp[kVWarps];
-    __shared__ int32_t sm_last;
-    __shared__ int32_t sm_count;
-    __shared__ int32_t sm_tok[kBlock];
-    __shared__ int32_t sm_flag[2];
-    using E = Elem<DT>;
-    const int tid = threadIdx.x;
+    __shared__ VerifySmem sm;
     const int32_t B = a.B;
-
-    block_row_prefix(a.len, B, sm_prefix, sm_warp);
-
+    block_row_prefix(a.len, B, 0, sm_prefix, sm.warp);
     // Requests with no rows to read get their outputs here.
     if (blockIdx.x == 0) {
-        for (int32_t b = tid; b < B; b += kVThreads) {
+        for (int32_t b = threadIdx.x; b < B; b += kVThreads) {
             if (len_ok(a.len[b])) continue;
             for (int r = 0; r < kBlock; ++r) {
                 a.argmax[(int64_t)b * kBlock + r] = CLK_SENT;
@@ -311,111 +427,103 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
             }
             a.accept[b] = 0;
             a.emitted[b] = 0;
-            if (FUSED) latch(L.status, CLK_EINVAL, b);
         }
     }
+    const int64_t vpr = VEC ? (int64_t)a.V / Elem<DT>::W : (int64_t)a.V;
+    verify_rows<DT, VEC, false>(a, L, sm_prefix, 0, vpr, [](int32_t, int32_t l) { return l; }, sm);
+}
 
-    const int64_t vpr = VEC ? (int64_t)a.V / E::W : (int64_t)a.V;
-    const int64_t total = (int64_t)sm_prefix[B] * vpr;
-    int64_t lo = total * blockIdx.x / gridDim.x;
-    const int64_t hi = total * (blockIdx.x + 1) / gridDim.x;
-    if (lo >= hi) return;
-    int64_t ri = lo / vpr;
-    // Request that owns row ri: largest b with P[b] <= ri.
-    int32_t b = 0, top = B;
-    while (b < top) {
-        const int32_t mid = (b + top + 1) >> 1;
-        if (sm_prefix[mid] <= ri) b = mid; else top = mid - 1;
+// Verification fused with the commit (clk_verify_append), launched as a
+// programmatic dependent of the proposal launch that produced the blocks
+// and lengths.  Phase 1 reads rows 0 .. base-1 of every request (base =
+// 1 + head, the short block, which every block covers) while the proposal
+// may still be running; then it waits for the proposal grid, learns the
+// lengths, counts phase 1 and reads the remaining rows of the long blocks.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
+{
+    extern __shared__ int32_t sm_prefix[];  // B + 1
+    __shared__ VerifySmem sm;
+    // Let the next launch (the next proposal) be scheduled; it waits for
+    // this grid to complete before it reads anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int32_t B = a.B;
+    const int32_t base = min(kBlock, 1 + L.p.head);
+    const int64_t vpr = VEC ? (int64_t)a.V / Elem<DT>::W : (int64_t)a.V;
+    const int64_t total1 = (int64_t)B * base * vpr;
+    const int64_t lo1 = total1 * blockIdx.x / gridDim.x;
+    const int64_t hi1 = total1 * (blockIdx.x + 1) / gridDim.x;
+    for (int64_t lo = lo1; lo < hi1;) {
+        const int64_t ri = lo / vpr;
+        const int64_t s1 = min(hi1, (ri + 1) * vpr) - ri * vpr;
+        piece_max<DT, VEC>(a, (int32_t)(ri / base), (int32_t)(ri % base), lo - ri * vpr, s1, sm);
+        __syncthreads();  // sm.red is reused by the next piece
+        lo = (ri + 1) * vpr;
     }
-    while (lo < hi) {
-        while (sm_prefix[b + 1] <= ri) ++b;
-        const int32_t r = (int32_t)(ri - sm_prefix[b]);
-        const int64_t s0 = lo - ri * vpr;
-        const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
-        const char* row = static_cast<const char*>(a.logits) +
-                          ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(typename E::T);
-        unsigned long long key = VEC ? scan_vec<DT>(row, (int32_t)s0, (int32_t)s1) : scan_scalar<DT>(row, s0, s1);
-        key = block_max_u64(key, sm_red);
-        if (tid == 0) {
-            atomicMax(a.keys + (int64_t)b * kBlock + r, key);
-            __threadfence();
-            const unsigned long long add = (unsigned long long)(s1 - s0);
-            const unsigned long long need =
-                (unsigned long long)(sm_prefix[b + 1] - sm_prefix[b]) * (unsigned long long)vpr;
-            sm_last = (atomicAdd(a.done + b, add) + add == need) ? 1 : 0;
-        }
-        __syncthreads();
-        if (sm_last) {
-            __threadfence();
-            if (tid < 32) {
-                const int lane = tid;
-                const int32_t Lb = sm_prefix[b + 1] - sm_prefix[b];
-                unsigned long long* kp = a.keys + (int64_t)b * kBlock;
-                int32_t g = CLK_SENT;
-                if (lane < Lb) {
-                    const unsigned long long kv = atomicAdd(kp + lane, 0ull);
-                    g = (int32_t)(0xFFFFFFFFu - (uint32_t)kv);
-                }
-                if (lane < kBlock) kp[lane] = 0ull;
-                const int32_t nxt = (lane + 1 < kBlock) ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
-                const unsigned match = __ballot_sync(0xFFFFFFFFu, lane < Lb - 1 && nxt == g);
-                const int32_t acc = __ffs(~match) - 1;
-                const int32_t out = lane <= acc ? g : CLK_SENT;
-                if (lane < kBlock) {
-                    a.argmax[(int64_t)b * kBlock + lane] = g;
-                    a.out_tok[(int64_t)b * kBlock + lane] = out;
-                    sm_tok[lane] = out;
-                }
-                if (lane == 0) {
-                    a.accept[b] = acc;
-                    a.emitted[b] = acc + 1;
-                    a.done[b] = 0ull;
-                    sm_count = acc + 1;
-                }
-            }
-            __syncthreads();
-            if (FUSED) {
-                const int32_t slot = a.slots[b];
-                if (slot >= 0 && slot < L.max_slots) {
-                    block_commit_tokens(L, slot, sm_tok, sm_count, sm_flag);
-                } else if (tid == 0) {
-                    latch(L.status, CLK_EINVAL, b);
-                }
-            }
-        }
-        __syncthreads();
-        ri += 1;
-        lo = ri * vpr;
+    // The blocks and lengths come from the proposal grid.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+    block_row_prefix(a.len, B, base, sm_prefix, sm.warp);
+    auto need_rows = [base](int32_t, int32_t l) { return len_ok(l) ? max(l, base) : base; };
+    for (int64_t lo = lo1; lo < hi1;) {
+        const int64_t ri = lo / vpr;
+        const int64_t s1 = min(hi1, (ri + 1) * vpr) - ri * vpr;
+        const int32_t b = (int32_t)(ri / base);
+        const int32_t Lb = a.len[b];
+        piece_count<true>(a, L, b, (unsigned long long)(s1 - (lo - ri * vpr)),
+                          (unsigned long long)need_rows(b, Lb) * (unsigned long long)vpr, Lb, sm);
+        lo = (ri + 1) * vpr;
     }
+    verify_rows<DT, VEC, true>(a, L, sm_prefix, base, vpr, need_rows, sm);
+}
+
+template <typename Kern>
+int verify_grid(Kern kern, size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
+{
+    int occ = 0;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CLK_ECUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kVThreads, smem) != cudaSuccess || occ < 1)
+        return CLK_ECUDA;
+    const int sms = num_sms();
+    if (sms <= 0) return CLK_ECUDA;
+    const int64_t max_work = (int64_t)B * kBlock * vpr;
+    int64_t grid = (max_work + 4 * kVThreads - 1) / (4 * kVThreads);
+    grid = grid < 1 ? 1 : grid;
+    if (grid > (int64_t)occ * sms) grid = (int64_t)occ * sms;
+    *grid_out = grid;
+    return CLK_OK;
 }
 
 template <int DT, bool VEC, bool FUSED>
 int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
 {
-    auto kern = k_verify<DT, VEC, FUSED>;
-    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
-    static int occ_cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
-    int occ = (dev >= 0 && dev < 64) ? occ_cache[dev] : 0;
-    if (occ == 0) {
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return CLK_ECUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kVThreads, smem) != cudaSuccess || occ < 1)
-            return CLK_ECUDA;
-        if (dev >= 0 && dev < 64 && a.B <= 1024) occ_cache[dev] = occ;
-    }
-    const int sms = num_sms();
-    if (sms <= 0) return CLK_ECUDA;
     constexpr int W = VEC ? Elem<DT>::W : 1;
     const int64_t vpr = (int64_t)a.V / W;
-    const int64_t max_work = (int64_t)a.B * kBlock * vpr;
-    int64_t grid = (max_work + 4 * kVThreads - 1) / (4 * kVThreads);
-    grid = grid < 1 ? 1 : grid;
-    if (grid > (int64_t)occ * sms) grid = (int64_t)occ * sms;
-    kern<<<(unsigned)grid, kVThreads, smem, s>>>(a, L);
-    return launch_status();
+    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
+    int64_t grid = 0;
+    if (!FUSED) {
+        auto kern = k_verify<DT, VEC>;
+        int rc = verify_grid(kern, smem, a.B, vpr, &grid);
+        if (rc != CLK_OK) return rc;
+        kern<<<(unsigned)grid, kVThreads, smem, s>>>(a, L);
+        return launch_status();
+    }
+    auto kern = k_verify_step<DT, VEC>;
+    int rc = verify_grid(kern, smem, a.B, vpr, &grid);
+    if (rc != CLK_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kVThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, a, L));
 }
 
 int verify_dispatch(const VerifyArgs& a, int32_t dtype, bool fused, const LookupDev& L, cudaStream_t s)
