@@ -17,8 +17,8 @@ NVFLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcom
            f"-I{INCLUDE}", f"-I{CSRC}"]
 
 
-def _compile(src: str, extra, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra, verbose: bool, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
     cmd = ["nvcc", *NVFLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         print(" ".join(cmd), flush=True)
@@ -26,16 +26,17 @@ def _compile(src: str, extra, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra=()) -> str:
-    """Compile every source for sm_103a and link libclk.so next to this file."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra=(), out: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile every source for sm_103a and link libclk.so (next to this file
+    unless `out` names another path)."""
+    os.makedirs(build_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra), verbose), SOURCES))
-    cmd = ["nvcc", ARCH, "-shared", "-o", LIB, *objs]
+        objs = list(ex.map(lambda s: _compile(s, list(extra), verbose, build_dir), SOURCES))
+    cmd = ["nvcc", ARCH, "-shared", "-o", out, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":
