@@ -93,6 +93,7 @@ _SIGS = [
     ("clk_lookup_init", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_append", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_propose", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
+    ("clk_lookup_propose_scan", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
     ("clk_sched_step", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     ("clk_fuse", ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
     ("clk_fuse_sched", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -254,6 +255,13 @@ def lookup_propose(h: Lookup, slots, draft, k, j, stream=None):
                                                           _ptr(draft, shape=(B, BLOCK), name="draft"),
                                                           _ptr(k, shape=(B,), name="k"), _ptr(j, shape=(B,), name="j"),
                                                           _stream(stream)))
+
+
+def lookup_propose_scan(h: Lookup, slots, draft, k, j, stream=None):
+    B = slots.numel()
+    _check("clk_lookup_propose_scan",
+           lib().clk_lookup_propose_scan(h.handle, _ptr(slots, name="slots"), B, _ptr(draft, shape=(B, BLOCK)),
+                                         _ptr(k, shape=(B,)), _ptr(j, shape=(B,)), _stream(stream)))
 
 
 def sched_step(h: Lookup, slots, k, prev_accept, prev_len, length, stream=None):

@@ -15,7 +15,7 @@ using namespace clk;
 namespace {
 
 struct Layout {
-    size_t status, state, vkeys, vdone, hist, tab, total;
+    size_t status, state, vkeys, vdone, skeys, hist, tab, total;
     int64_t hstride;
     uint64_t tsize;
     int32_t nlev;
@@ -46,6 +46,8 @@ int layout_of(const clk_params* p, int32_t max_slots, int64_t max_hist, Layout* 
     L.vkeys = off;
     off = align_up(off + ns * kBlock * sizeof(unsigned long long), kAlign);
     L.vdone = off;
+    off = align_up(off + ns * sizeof(unsigned long long), kAlign);
+    L.skeys = off;
     off = align_up(off + ns * sizeof(unsigned long long), kAlign);
     L.hist = off;
     off = align_up(off + ns * (size_t)L.hstride * sizeof(int32_t), kAlign);
@@ -125,6 +127,7 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     D.state = reinterpret_cast<SlotState*>(base + L.state);
     D.vkeys = reinterpret_cast<unsigned long long*>(base + L.vkeys);
     D.vdone = reinterpret_cast<unsigned long long*>(base + L.vdone);
+    D.skeys = reinterpret_cast<unsigned long long*>(base + L.skeys);
     D.hist = reinterpret_cast<int32_t*>(base + L.hist);
     D.tab = reinterpret_cast<unsigned long long*>(base + L.tab);
     D.hstride = L.hstride;

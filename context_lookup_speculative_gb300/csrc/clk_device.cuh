@@ -5,6 +5,7 @@
 //   state   SlotState[max_slots]        scheduler state, history length, counters
 //   vkeys   u64[max_slots * 16]         fused verify: per-row packed (value, index) maxima
 //   vdone   u64[max_slots]              fused verify: vectors verified per request
+//   skeys   u64[max_slots]              full-scan lookup: best (length, position) per request
 //   hist    int32[max_slots][hstride]   token histories
 //   tab     u64[max_slots][nlev][tsize] k-gram index, one table per match length
 //
@@ -61,6 +62,7 @@ struct LookupDev {
     SlotState* state;
     unsigned long long* vkeys;
     unsigned long long* vdone;
+    unsigned long long* skeys;  // full-scan lookup: packed (length, end + 1) per batch position
     int32_t* hist;
     unsigned long long* tab;
     int64_t hstride;  // int32 elements per history

@@ -226,6 +226,85 @@ __global__ void k_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int
     warp_fuse(L.p, last, c_lane, kk, m_lane, l, block + (int64_t)b * kBlock);
 }
 
+// ---------------------------------------------------------------------------
+// Full-scan lookup (the pages' own design, Step 1 of "三步走": scan the
+// request's whole history; most candidates fail on their first tokens, the
+// rest are extended up to max_k).  For every end position q <= n - 2 the
+// match length m(q) = the number of tokens h[q - l] == h[n - 1 - l], l = 0..,
+// capped at max_k; the answer is the largest (m, q) with m >= min_k, and
+// j = q + 1.  Grid: B x chunks CTAs; each merges its best packed
+// (m << 32 | q + 1) into skeys[b] with one atomicMax; k_scan_finish builds the
+// draft and clears skeys.
+// ---------------------------------------------------------------------------
+constexpr int kScanPerCta = 4096;
+
+__global__ void k_scan_match(LookupDev L, const int32_t* __restrict__ slots, int32_t chunks)
+{
+    __shared__ int32_t sm_suf[kMaxK];
+    __shared__ unsigned long long sm_red[kThreads / 32];
+    const int32_t b = blockIdx.x / chunks;
+    const int32_t c = blockIdx.x % chunks;
+    const int32_t slot = slots[b];
+    if (slot < 0 || slot >= L.max_slots) return;
+    const int32_t n = L.state[slot].n;
+    const int32_t lo = c * kScanPerCta, hi = min(n - 1, lo + kScanPerCta);  // end positions [lo, hi)
+    if (n < 2 || lo >= hi) return;
+    const clk_params& p = L.p;
+    const int32_t* h = hist_of(L, slot);
+    if (threadIdx.x < p.max_k) sm_suf[threadIdx.x] = threadIdx.x < n ? h[n - 1 - threadIdx.x] : CLK_SENT;
+    __syncthreads();
+    unsigned long long best = 0ull;
+    for (int32_t q = lo + (int32_t)threadIdx.x; q < hi; q += kThreads) {
+        int32_t m = 0;
+        while (m < p.max_k && q - m >= 0 && h[q - m] == sm_suf[m]) ++m;
+        if (m >= p.min_k) {
+            const unsigned long long key = ((unsigned long long)m << 32) | (uint32_t)(q + 1);
+            best = key > best ? key : best;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long v = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = v > best ? v : best;
+    }
+    if ((threadIdx.x & 31) == 0) sm_red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kThreads / 32; ++w) best = sm_red[w] > best ? sm_red[w] : best;
+        if (best != 0ull) atomicMax(L.skeys + b, best);
+    }
+}
+
+// One warp per request: (k, j) from the merged key, the LZ77 draft.
+__global__ void k_scan_finish(LookupDev L, const int32_t* __restrict__ slots, int32_t B, int32_t* __restrict__ draft,
+                              int32_t* __restrict__ k_out, int32_t* __restrict__ j_out)
+{
+    const int32_t b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (b >= B) return;
+    const int lane = threadIdx.x & 31;
+    const int32_t slot = slots[b];
+    const bool valid = slot >= 0 && slot < L.max_slots;
+    const int32_t n = valid ? L.state[slot].n : 0;
+    if (lane == 0) {
+        if (!valid) latch(L.status, CLK_EINVAL, b);
+        else if (n < 1) latch(L.status, CLK_ESTATE, slot);
+    }
+    const unsigned long long key = L.skeys[b];
+    __syncwarp();
+    if (lane == 0) L.skeys[b] = 0ull;
+    int32_t k = 0, j = -1, c = CLK_SENT;
+    if (valid && n >= 1 && key != 0ull) {
+        k = (int32_t)(key >> 32);
+        j = (int32_t)(uint32_t)key;
+        if (lane < kBlock) c = hist_of(L, slot)[j + lane % (n - j)];
+    }
+    if (lane < kBlock) draft[(int64_t)b * kBlock + lane] = c;
+    if (lane == 0) {
+        k_out[b] = k;
+        j_out[b] = j;
+    }
+}
+
 constexpr int kMaxPending = 32;                  // pending end positions checked directly
 constexpr int kWin = kMaxPending + kMaxK + 1;    // window of history tokens in shared memory
 constexpr int kInsertWarps = 5;                  // warps that index the pending positions
@@ -535,4 +614,19 @@ extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int
         return CLK_EINVAL;
     return launch_lookup_step<true>(h->dev, d_slots, B, d_head, d_prev_accept, d_prev_len, d_draft, d_k, d_j, d_len,
                                     d_block, (cudaStream_t)s);
+}
+
+extern "C" int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft,
+                                       int32_t* d_k, int32_t* d_j, clk_stream_t s)
+{
+    int rc = check_batch(h, B);
+    if (rc != CLK_OK) return rc;
+    if (B == 0) return CLK_OK;
+    if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
+    const int64_t chunks = (h->dev.cap + kScanPerCta - 1) / kScanPerCta;
+    if ((int64_t)B * chunks > 0x7FFFFFFF) return CLK_EINVAL;
+    k_scan_match<<<(unsigned)(B * chunks), kThreads, 0, (cudaStream_t)s>>>(h->dev, d_slots, (int32_t)chunks);
+    if ((rc = launch_status()) != CLK_OK) return rc;
+    k_scan_finish<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_draft, d_k, d_j);
+    return launch_status();
 }

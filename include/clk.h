@@ -180,9 +180,20 @@ CLK_API int clk_lookup_append(clk_lookup* h, const int32_t* d_slots, int32_t B, 
  * when none.  The draft is d_draft[b][i] = h[j + (i mod (n - j))] for
  * i = 0..15: the tokens that followed the occurrence, continued as an LZ77
  * copy at distance n - j past the end of the history (all CLK_SENT when
- * k = 0).  Outputs: d_draft [B,16], d_k [B], d_j [B]. */
+ * k = 0).  Outputs: d_draft [B,16], d_k [B], d_j [B].  The launch also
+ * indexes any tokens committed by clk_verify_append since the slot's last
+ * proposal. */
 CLK_API int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft, int32_t* d_k,
                                int32_t* d_j, clk_stream_t s);
+
+/* The same proposal as clk_lookup_propose, by the pages' own method: a scan
+ * of the whole history h[0..n) for every earlier occurrence of the suffix
+ * ("三步走", Step 1: one scan per request; most candidates fail on their first
+ * tokens, the survivors are extended up to max_k), without the index.  Cost
+ * O(n) per request per call; kept as the ablation of the incremental index.
+ * Outputs and errors as clk_lookup_propose; the index is not touched. */
+CLK_API int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft,
+                                    int32_t* d_k, int32_t* d_j, clk_stream_t s);
 
 /* Step 3 of "三步走" (the long-block scheduler), one step per request.  The
  * flag is k >= tail_k (the lookup can fill the tail); nearly full means the
@@ -213,8 +224,11 @@ CLK_API int clk_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, con
                            const int32_t* d_head, const int32_t* d_prev_accept, const int32_t* d_prev_len, int32_t* d_len,
                            int32_t* d_block, clk_stream_t s);
 
-/* clk_lookup_propose, clk_sched_step and clk_fuse in one launch (one warp per
- * request).  Bit-identical to the three calls. */
+/* clk_lookup_propose, clk_sched_step and clk_fuse in one launch (one CTA per
+ * request).  Bit-identical to the three calls.  Like clk_lookup_propose it
+ * first waits for the preceding launch on the stream (programmatic dependent
+ * launch) and indexes the tokens that clk_verify_append committed since the
+ * slot's last proposal. */
 CLK_API int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_head,
                                    const int32_t* d_prev_accept, const int32_t* d_prev_len, int32_t* d_draft,
                                    int32_t* d_k, int32_t* d_j, int32_t* d_len, int32_t* d_block, clk_stream_t s);
@@ -275,9 +289,19 @@ CLK_API int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_
                                      clk_stream_t s);
 
 /* clk_verify_greedy followed by clk_lookup_append of its d_out_tok /
- * d_emitted, in one launch: the request's append runs as soon as its rows
- * are verified.  Uses the scratch inside the lookup workspace.  Bit-identical
- * to the two calls. */
+ * d_emitted, in one launch: each request's tokens are committed to its
+ * history as soon as its rows are verified; the k-grams they complete are
+ * indexed by the next clk_lookup_propose / clk_propose_fuse_sched /
+ * clk_lookup_append on the slot (which see the same answers as with an
+ * immediate index update).  Uses the scratch inside the lookup workspace.
+ * Results are bit-identical to the two calls.
+ * Launch order: the launch is a programmatic dependent of the preceding
+ * launch on the stream.  It reads rows 0 .. head of every request (the rows
+ * every block covers) before it waits for that launch, so the logits must
+ * already be complete when this call is made (as after any ordinary kernel
+ * or copy on the stream) and must hold at least min(16, 1 + head) rows per
+ * request; d_block and d_len may come from the preceding launch
+ * (clk_propose_fuse_sched). */
 CLK_API int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                               int64_t row_stride, int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block,
                               const int32_t* d_len, int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted,

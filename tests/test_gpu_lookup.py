@@ -160,3 +160,104 @@ def test_long_history_index_build():
     hists = [base[:c].copy() for c in cuts]
     lk, s = _setup(hists, n + 64)
     _assert_same(_propose(lk, s), hists)
+
+
+def _commit_by_verify(lk, s, rows_tokens):
+    """Commit tokens through clk_verify_append: fp32 logits whose row r peaks at
+    rows_tokens[b][r] and blocks that accept all 15 drafts (16 tokens)."""
+    B = s.numel()
+    V = 8
+    x = torch.zeros((B, 16, V), dtype=torch.float32)
+    blk = torch.full((B, 16), -1, dtype=torch.int32)
+    for b in range(B):
+        for r in range(16):
+            x[b, r, rows_tokens[b][r]] = 1.0
+            if r + 1 < 16:
+                blk[b, r + 1] = int(rows_tokens[b][r])
+    z = lambda *sh: torch.zeros(sh, dtype=torch.int32, device="cuda")  # noqa: E731
+    g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+    L = torch.full((B,), 16, dtype=torch.int32, device="cuda")
+    clk.verify_append(lk, s, x.cuda(), blk.cuda(), L, g, a, e, out)
+    torch.cuda.synchronize()
+    assert e.cpu().tolist() == [16] * B
+
+
+@pytest.mark.parametrize("commits", [1, 2, 3, 5])
+def test_commits_without_lookup_in_between(commits):
+    """Several fused commits before the next proposal leave 16 x commits
+    positions unindexed (more than the 32 the proposal checks directly for 3
+    and more); the proposal must still equal the full scan, and so must a
+    later unfused append."""
+    rng = np.random.default_rng(56 + commits)
+    B = 12
+    hists = [rng.integers(0, 8, size=int(rng.integers(20, 120))).astype(np.int32) for _ in range(B)]
+    lk, s = _setup(hists, 120 + 16 * 12, vocab=8)
+    for _ in range(commits):
+        toks = rng.integers(0, 8, size=(B, 16))
+        toks[::3] = np.resize([1, 2, 3], 16)  # periodic runs: long, overlapping matches
+        _commit_by_verify(lk, s, toks)
+        hists = [np.concatenate([h, toks[b].astype(np.int32)]) for b, h in enumerate(hists)]
+    assert lk.slot_info(0)["n_indexed"] < lk.slot_info(0)["n"]
+    _assert_same(_propose(lk, s), hists)
+    assert lk.slot_info(0)["n_indexed"] == lk.slot_info(0)["n"]
+    # commit again, then an unfused append on top of the pending positions
+    toks = rng.integers(0, 8, size=(B, 16))
+    _commit_by_verify(lk, s, toks)
+    hists = [np.concatenate([h, toks[b].astype(np.int32)]) for b, h in enumerate(hists)]
+    more = rng.integers(0, 8, size=(B, 16)).astype(np.int32)
+    cnt = rng.integers(0, 17, size=B).astype(np.int32)
+    clk.lookup_append(lk, s, torch.from_numpy(more).cuda(), torch.from_numpy(cnt).cuda())
+    hists = [np.concatenate([h, more[b, :cnt[b]]]) for b, h in enumerate(hists)]
+    _assert_same(_propose(lk, s), hists)
+    for b in range(B):
+        assert np.array_equal(lk.history(b), hists[b])
+    assert lk.status() == (0, 0)
+
+
+def _propose_scan(lk, s):
+    B = s.numel()
+    d = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
+    k = torch.zeros(B, dtype=torch.int32, device="cuda")
+    j = torch.zeros(B, dtype=torch.int32, device="cuda")
+    clk.lookup_propose_scan(lk, s, d, k, j)
+    torch.cuda.synchronize()
+    return d.cpu().numpy(), k.cpu().numpy(), j.cpu().numpy()
+
+
+@pytest.mark.parametrize("kind", ["small_vocab", "periodic", "zipf_long"])
+def test_full_scan_lookup_matches_oracle_and_index(kind):
+    """The pages' full-scan lookup (clk_lookup_propose_scan) returns exactly the
+    oracle's (k, j, draft), and the same as the index path."""
+    rng = np.random.default_rng({"small_vocab": 61, "periodic": 62, "zipf_long": 63}[kind])
+    if kind == "small_vocab":
+        hists = [rng.integers(0, int(rng.integers(2, 6)), size=int(rng.integers(1, 9000))).astype(np.int32)
+                 for _ in range(60)]
+    elif kind == "periodic":
+        hists = []
+        for p in range(1, 41):
+            pat = rng.integers(0, 32000, size=p).astype(np.int32)
+            n = int(rng.integers(p + 1, 9000))
+            h = pat[np.arange(n) % p].copy()
+            noise = rng.random(n) < 0.05
+            h[noise] = rng.integers(0, 32000, size=int(noise.sum()))
+            hists.append(h)
+    else:
+        hists = []
+        for _ in range(16):
+            n = int(rng.integers(20000, 70000))
+            h = (rng.zipf(1.1, size=n).astype(np.int64) % 248320).astype(np.int32)
+            src = int(rng.integers(0, n // 2))
+            ln = int(rng.integers(1, 40))
+            h[n - ln:] = h[src:src + ln]
+            hists.append(h)
+    lk, s = _setup(hists, max(h.size for h in hists) + 32)
+    got = _propose_scan(lk, s)
+    _assert_same(got, hists)
+    idx = _propose(lk, s)
+    for a, b in zip(got, idx):
+        assert np.array_equal(a, b)
+    # the scan leaves no state behind: a second call gives the same answer
+    again = _propose_scan(lk, s)
+    for a, b in zip(got, again):
+        assert np.array_equal(a, b)
+    assert lk.status() == (0, 0)
