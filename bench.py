@@ -165,7 +165,8 @@ def run_ours(args, world, rank, local, dist):
     clk.lib()
     w = wl.make(args.config, seed=shard_seed(int(wl.DEFAULT_SEED[args.config]), rank))
     W, K = args.warmup, args.steps
-    assert W + K <= w.steps, f"warmup + steps must be <= {w.steps} for this workload"
+    if W + K > w.steps:  # the workload's streams cover w.steps steps
+        K = w.steps - W
     B, V = w.B, w.V
     params = clk.Params.default()
     stream = torch.cuda.current_stream(device)
@@ -232,31 +233,60 @@ def run_ours(args, world, rank, local, dist):
         flush.zero_()  # no step may find its logits in L2
         torch.cuda.synchronize()
 
+    def capture(n, events=None, lens=None):
+        """The n steps of a chunk as one CUDA graph (launched with one call, so
+        no host time falls inside the timed region); `events` get recorded
+        around every launch, `lens` receives each step's block lengths."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                if events is not None:
+                    events[3 * i].record()
+                st.pre(heads[i])
+                if events is not None:
+                    events[3 * i + 1].record()
+                st.post(bufs[i])
+                if events is not None:
+                    events[3 * i + 2].record()
+                if lens is not None:
+                    lens[i].copy_(st.length)
+        return g
+
     # Pass B: the first steps once more with an event around every launch, for
     # each kernel's own duration (launches serialised by the events).
     warmup()
     nb = min(chunk, K)
     generate(W, nb)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nb + 1)]
     lens_b = torch.zeros((nb, B), dtype=torch.int32, device=device)
-    for i in range(nb):
-        ev[2 * i].record(stream)
-        st.pre(heads[i])
-        ev[2 * i + 1].record(stream)
-        st.post(bufs[i])
-        lens_b[i].copy_(st.length)
-    ev[2 * nb].record(stream)
-    torch.cuda.synchronize()
-    pre_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(nb))
-    verify_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(nb))
+    try:
+        # events recorded inside a graph must be "external" to be timed
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 * nb)]
+        graph = capture(nb, ev, lens_b)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        del graph
+    except TypeError:  # a torch without external events: launch pass B directly
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * nb)]
+        for i in range(nb):
+            ev[3 * i].record(stream)
+            st.pre(heads[i])
+            ev[3 * i + 1].record(stream)
+            st.post(bufs[i])
+            ev[3 * i + 2].record(stream)
+            lens_b[i].copy_(st.length)
+        torch.cuda.synchronize()
+    pre_ms = sum(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(nb))
+    verify_ms = sum(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(nb))
     cb = lk.counters(-1)
     # logits bytes each pass-B verify launch had to read (for the ncu traffic comparison)
     esz_b = 2 if w.dtype == wl.BF16 else 4
     passb_bytes = [int(x) * V * esz_b for x in lens_b.sum(dim=1).tolist()]
     # Pass A (the measurement): warm-up again from the reset state, then the
     # timed steps back to back in chunks whose inputs are generated beforehand
-    # into HBM; the two launches of a step overlap (programmatic dependent
-    # launch) and nothing is recorded between them.
+    # into HBM, each chunk replayed as one CUDA graph; the two launches of a
+    # step overlap (programmatic dependent launch) and nothing is recorded
+    # between them.
     warmup()
     c_w = lk.counters(-1)
     rows_b = 8 * (cb["steps"] - c_w["steps"]) + 8 * (cb["long_steps"] - c_w["long_steps"])
@@ -271,16 +301,16 @@ def run_ours(args, world, rank, local, dist):
         generate(t, n)
         if world > 1:
             dist.barrier()
+        graph = capture(n)
         torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for i in range(n):
-            st.pre(heads[i])
-            st.post(bufs[i])
-            launches += 2
+        graph.replay()
         end.record(stream)
         torch.cuda.synchronize()
+        launches += 2 * n
+        del graph
         if world > 1:
             dist.barrier()
         total_ms += start.elapsed_time(end)
@@ -308,6 +338,7 @@ def run_ours(args, world, rank, local, dist):
     path_gbs = path_bytes / (total_ms * 1e-3) / 1e9
     ratio = _traffic_ratio()
 
+    ablation = run_lookup_ablation(lk, slots, w, device) if args.ablation else None
     e2e = run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device) if (rank == 0 and not args.no_e2e) else None
     cpu = run_cpu_baseline(args, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -345,10 +376,55 @@ def run_ours(args, world, rank, local, dist):
                      "duration_us": round(verify_ms * 1e3 / nb, 3)},
         "clocks": clocks.summary(),
         "gpu_launches": launches,
+        "lookup_ablation": ablation,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
     return out
+
+
+def run_lookup_ablation(lk, slots, w, device, reps: int = 20):
+    """The proposal by the incremental index against the pages' full history
+    scan, on the GPU (same state, same answers), and the CPU oracle's full
+    scan; per batch step.  The state is the one the timed steps left."""
+    import time as _t
+
+    import numpy as np
+    import torch
+
+    import context_lookup_speculative_gb300 as clk
+    import oracle
+
+    B = w.B
+    z = lambda *sh: torch.zeros(sh, dtype=torch.int32, device=device)  # noqa: E731
+    outs = {m: (z(B, 16), z(B), z(B)) for m in ("index", "scan")}
+    clk.lookup_propose(lk, slots, *outs["index"])  # indexes the last step's tokens first
+    torch.cuda.synchronize()
+    res = {}
+    for mode, fn in (("index", clk.lookup_propose), ("scan", clk.lookup_propose_scan)):
+        fn(lk, slots, *outs[mode])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn(lk, slots, *outs[mode])
+        b.record()
+        torch.cuda.synchronize()
+        res[f"gpu_{mode}_us"] = round(a.elapsed_time(b) * 1e3 / reps, 3)
+    same = all(torch.equal(x, y) for x, y in zip(outs["index"], outs["scan"]))
+    hists = [lk.history(int(s)) for s in slots.tolist()]
+    t0 = _t.perf_counter()
+    ref = [oracle.lookup(h) for h in hists]
+    cpu_s = _t.perf_counter() - t0
+    k_idx = outs["index"][1].cpu().tolist()
+    res.update({
+        "answers_identical": bool(same and [r[0] for r in ref] == k_idx),
+        "cpu_oracle_full_scan_us": round(cpu_s * 1e6, 1),
+        "cpu_note": "oracle full scan of every request's history, one core, per batch step",
+        "history_tokens_mean": int(np.mean([h.size for h in hists])),
+        "batch": B,
+    })
+    return res
 
 
 def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
@@ -475,6 +551,8 @@ def main(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", action="store_true",
+                    help="also time the proposal by index vs by full history scan (GPU and CPU oracle)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -347,11 +347,15 @@ def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitt
 # Step driver: two launches per decode step
 # ---------------------------------------------------------------------------
 class Step:
-    """Per-step buffers of one batch and the two fused launches of a step.
+    """Per-step buffers of one batch and the two launches of a step.
 
-    ``pre(head)``   -> propose + scheduler + fusion: draft, k, j, length, block
-    ``post(logits)``-> verify + commit: argmax, accept, emitted, out_tok
-    The previous step's accept/length feed the scheduler (in place)."""
+    ``pre(head)``    -> propose + scheduler + fusion: draft, k, j, length, block
+    ``post(logits)`` -> verify + commit: argmax, accept, emitted, out_tok
+    The previous step's accept/length feed the scheduler (in place).  The
+    buffers are owned here, so their pointers are resolved once; a call only
+    checks the tensor it is given.  ``post`` reads rows 0..head of every
+    request before the proposal launch has finished (programmatic dependent
+    launch), so the logits must hold all 1 + head + tail rows of every request."""
 
     def __init__(self, lookup: Lookup, slots: torch.Tensor):
         self.h = lookup
@@ -363,11 +367,29 @@ class Step:
         self.draft, self.k, self.j = z(B, BLOCK), z(B), z(B)
         self.length, self.block = z(B), z(B, BLOCK)
         self.argmax, self.accept, self.emitted, self.out_tok = z(B, BLOCK), z(B), z(B), z(B, BLOCK)
+        _ptr(slots, shape=(B,), name="slots")
+        self._p = {n: getattr(self, n).data_ptr() for n in
+                   ("slots", "draft", "k", "j", "length", "block", "argmax", "accept", "emitted", "out_tok")}
+        self._head_shape = (B, lookup.params.head)
+        self._rows = lookup.params.long_len
+        self._lib = lib()
 
     def pre(self, head, stream=None):
-        propose_fuse_sched(self.h, self.slots, head, self.accept, self.length, self.draft, self.k, self.j,
-                           self.length, self.block, stream)
+        if tuple(head.shape) != self._head_shape or head.dtype != torch.int32 or not head.is_cuda \
+                or not head.is_contiguous():
+            raise ValueError(f"head must be contiguous int32 {self._head_shape} on the GPU")
+        p = self._p
+        _check("clk_propose_fuse_sched",
+               self._lib.clk_propose_fuse_sched(self.h.handle, p["slots"], self.B, head.data_ptr(), p["accept"],
+                                                p["length"], p["draft"], p["k"], p["j"], p["length"], p["block"],
+                                                _stream(stream)))
 
     def post(self, logits, stream=None):
-        verify_append(self.h, self.slots, logits, self.block, self.length, self.argmax, self.accept,
-                      self.emitted, self.out_tok, stream)
+        dt, rs, qs, V = _logits_args(logits)
+        if logits.shape[0] != self.B or logits.shape[1] < self._rows:
+            raise ValueError(f"logits must be [{self.B}, >= {self._rows}, V]")
+        p = self._p
+        _check("clk_verify_append",
+               self._lib.clk_verify_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V, self.B,
+                                           p["block"], p["length"], p["argmax"], p["accept"], p["emitted"],
+                                           p["out_tok"], _stream(stream)))

@@ -477,17 +477,44 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     verify_rows<DT, VEC, true>(a, L, sm_prefix, base, vpr, need_rows, sm);
 }
 
+// Resident CTAs per SM of `kern` (times 1024, plus the SM count), cached per
+// device and kernel for dynamic shared memory sizes up to 4 KB (B < 1,024),
+// which almost every call uses; larger sizes are queried each time.
 template <typename Kern>
-int verify_grid(Kern kern, size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
+int occupancy(Kern kern, size_t smem, int* packed)
 {
+    constexpr int kDevices = 64;
+    static int cache[kDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
+    const bool cacheable = dev >= 0 && dev < kDevices && smem <= 4096;
+    if (cacheable && cache[dev] > 0) {
+        *packed = cache[dev];
+        return CLK_OK;
+    }
     int occ = 0;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CLK_ECUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kVThreads, smem) != cudaSuccess || occ < 1)
+    // Sized for 4 KB so that the cached value holds for every cacheable size.
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kVThreads, cacheable ? 4096 : smem) !=
+            cudaSuccess ||
+        occ < 1)
         return CLK_ECUDA;
     const int sms = num_sms();
-    if (sms <= 0) return CLK_ECUDA;
+    if (sms <= 0 || sms >= 1024) return CLK_ECUDA;
+    *packed = occ * 1024 + sms;
+    if (cacheable) cache[dev] = *packed;
+    return CLK_OK;
+}
+
+template <typename Kern>
+int verify_grid(Kern kern, size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
+{
+    int packed = 0;
+    const int rc = occupancy(kern, smem, &packed);
+    if (rc != CLK_OK) return rc;
+    const int occ = packed / 1024, sms = packed % 1024;
     const int64_t max_work = (int64_t)B * kBlock * vpr;
     int64_t grid = (max_work + 4 * kVThreads - 1) / (4 * kVThreads);
     grid = grid < 1 ? 1 : grid;
