@@ -184,8 +184,7 @@ def run_ours(args, world, rank, local, dist):
     def reinit():
         clk.lookup_init(lk, slots, d_ptok, d_poff)
         gen.reset()
-        for t_ in (st.accept, st.length):
-            t_.zero_()
+        st.reset()
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()

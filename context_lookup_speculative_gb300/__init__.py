@@ -103,7 +103,8 @@ _SIGS = [
     ("clk_verify_greedy", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
     ("clk_verify_greedy_static", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
-    ("clk_verify_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    ("clk_verify_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                         _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
     ("clk_status_clear", ctypes.c_int, [_P, _P]),
     ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
@@ -333,12 +334,14 @@ def verify_greedy_static(logits, block, length, argmax, accept, emitted, out_tok
                                           _ptr(out_tok, shape=(B, BLOCK)), _stream(stream)))
 
 
-def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None):
+def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None,
+                  length_hint=None):
     dt, rs, qs, V = _logits_args(logits)
     B = slots.numel()
     _check("clk_verify_append",
            lib().clk_verify_append(h.handle, _ptr(slots), logits.data_ptr(), dt, rs, qs, V, B,
                                    _ptr(block, shape=(B, BLOCK)), _ptr(length, shape=(B,)),
+                                   _ptr(length_hint, shape=(B,), name="length_hint"),
                                    _ptr(argmax, shape=(B, BLOCK)), _ptr(accept, shape=(B,)),
                                    _ptr(emitted, shape=(B,)), _ptr(out_tok, shape=(B, BLOCK)), _stream(stream)))
 
@@ -351,11 +354,13 @@ class Step:
 
     ``pre(head)``    -> propose + scheduler + fusion: draft, k, j, length, block
     ``post(logits)`` -> verify + commit: argmax, accept, emitted, out_tok
-    The previous step's accept/length feed the scheduler (in place).  The
-    buffers are owned here, so their pointers are resolved once; a call only
-    checks the tensor it is given.  ``post`` reads rows 0..head of every
-    request before the proposal launch has finished (programmatic dependent
-    launch), so the logits must hold all 1 + head + tail rows of every request."""
+    The previous step's accept/length feed the scheduler.  The block lengths
+    alternate between two buffers, so that ``post`` can pass the previous
+    step's lengths as the verify launch's prediction while ``pre`` writes the
+    new ones; ``length`` is the buffer of the latest ``pre``.  The buffers are
+    owned here, so their pointers are resolved once; a call only checks the
+    tensor it is given.  The logits must hold all 1 + head + tail rows of
+    every request."""
 
     def __init__(self, lookup: Lookup, slots: torch.Tensor):
         self.h = lookup
@@ -365,24 +370,38 @@ class Step:
         z = lambda *s: torch.zeros(s, dtype=torch.int32, device=dev)  # noqa: E731
         self.B = B
         self.draft, self.k, self.j = z(B, BLOCK), z(B), z(B)
-        self.length, self.block = z(B), z(B, BLOCK)
+        self._len = [z(B), z(B)]
+        self._cur = 0
+        self.block = z(B, BLOCK)
         self.argmax, self.accept, self.emitted, self.out_tok = z(B, BLOCK), z(B), z(B), z(B, BLOCK)
         _ptr(slots, shape=(B,), name="slots")
         self._p = {n: getattr(self, n).data_ptr() for n in
-                   ("slots", "draft", "k", "j", "length", "block", "argmax", "accept", "emitted", "out_tok")}
+                   ("slots", "draft", "k", "j", "block", "argmax", "accept", "emitted", "out_tok")}
+        self._lp = [t.data_ptr() for t in self._len]
         self._head_shape = (B, lookup.params.head)
         self._rows = lookup.params.long_len
         self._lib = lib()
+
+    @property
+    def length(self) -> torch.Tensor:
+        return self._len[self._cur]
+
+    def reset(self):
+        """Forget the previous step (after the slots are set up again)."""
+        for t in self._len:
+            t.zero_()
+        self.accept.zero_()
 
     def pre(self, head, stream=None):
         if tuple(head.shape) != self._head_shape or head.dtype != torch.int32 or not head.is_cuda \
                 or not head.is_contiguous():
             raise ValueError(f"head must be contiguous int32 {self._head_shape} on the GPU")
-        p = self._p
+        p, prev, new = self._p, self._cur, self._cur ^ 1
         _check("clk_propose_fuse_sched",
                self._lib.clk_propose_fuse_sched(self.h.handle, p["slots"], self.B, head.data_ptr(), p["accept"],
-                                                p["length"], p["draft"], p["k"], p["j"], p["length"], p["block"],
-                                                _stream(stream)))
+                                                self._lp[prev], p["draft"], p["k"], p["j"], self._lp[new],
+                                                p["block"], _stream(stream)))
+        self._cur = new
 
     def post(self, logits, stream=None):
         dt, rs, qs, V = _logits_args(logits)
@@ -391,5 +410,5 @@ class Step:
         p = self._p
         _check("clk_verify_append",
                self._lib.clk_verify_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V, self.B,
-                                           p["block"], p["length"], p["argmax"], p["accept"], p["emitted"],
-                                           p["out_tok"], _stream(stream)))
+                                           p["block"], self._lp[self._cur], self._lp[self._cur ^ 1], p["argmax"],
+                                           p["accept"], p["emitted"], p["out_tok"], _stream(stream)))

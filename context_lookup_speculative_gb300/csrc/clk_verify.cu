@@ -40,6 +40,7 @@ struct VerifyArgs {
     int32_t B;
     const int32_t* block;
     const int32_t* len;
+    const int32_t* len_hint;  // fused: predicted block lengths (may be null)
     int32_t* argmax;
     int32_t* accept;
     int32_t* emitted;
@@ -249,15 +250,15 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
 // valid length 1 <= L_b <= 16, else 0.
 __device__ __forceinline__ int32_t rows_after(int32_t l, int32_t base) { return len_ok(l) ? max(0, l - base) : 0; }
 
-// P[b] = rows_after(L_b', base) summed over requests b' < b; P[B] = total.
-__device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t base, int32_t* P,
-                                                 int32_t* sm_warp)
+// P[b] = rows(b') summed over requests b' < b; P[B] = total.  Block-wide.
+template <typename Rows>
+__device__ __forceinline__ void block_prefix(int32_t B, Rows rows, int32_t* P, int32_t* sm_warp)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t per = (B + kVThreads - 1) / kVThreads;
     const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) local += rows_after(len[b], base);
+    for (int32_t b = b0; b < b1; ++b) local += rows(b);
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -279,10 +280,17 @@ __device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len
     int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
         P[b] = run;
-        run += rows_after(len[b], base);
+        run += rows(b);
     }
     if (tid == kVThreads - 1) P[B] = sm_warp[kVWarps - 1];
     __syncthreads();
+}
+
+// P[b] = rows_after(L_b', base) summed over requests b' < b; P[B] = total.
+__device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t base, int32_t* P,
+                                                 int32_t* sm_warp)
+{
+    block_prefix(B, [len, base](int32_t b) { return rows_after(len[b], base); }, P, sm_warp);
 }
 
 struct VerifySmem {
@@ -434,52 +442,113 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 }
 
 // Verification fused with the commit (clk_verify_append), launched as a
-// programmatic dependent of the proposal launch that produced the blocks
-// and lengths.  Phase 1 reads rows 0 .. base-1 of every request (base =
-// 1 + head, the short block, which every block covers) while the proposal
-// may still be running; then it waits for the proposal grid, learns the
-// lengths, counts phase 1 and reads the remaining rows of the long blocks.
+// programmatic dependent of the proposal launch that produces the blocks and
+// lengths.  Before it waits for that launch it reads, for every request, the
+// rows of a predicted length (the short block, or the caller's hint, e.g. the
+// previous step's length, when that is longer); after the wait it reads the
+// rows the prediction missed.  Every addition to a request's vector counter
+// returns the new count; a count that equals the request's total (known only
+// after the wait, max(predicted, true length) rows) finishes the request, so
+// additions made before the wait are checked after it.  The answer does not
+// depend on the prediction; a wrong one costs only reads.
+constexpr int kVMaxDefer = 32;
+
+// Rows read before the wait for request b.
+__device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b, int32_t base)
+{
+    const int32_t h = a.len_hint != nullptr ? a.len_hint[b] : 0;
+    return len_ok(h) ? max(h, base) : base;
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
 {
     extern __shared__ int32_t sm_prefix[];  // B + 1
     __shared__ VerifySmem sm;
+    __shared__ int32_t sm_db[kVMaxDefer];              // deferred checks: request
+    __shared__ unsigned long long sm_dc[kVMaxDefer];   // and the count its addition returned
+    __shared__ int32_t sm_nd;
+    __shared__ int32_t sm_waited;
     // Let the next launch (the next proposal) be scheduled; it waits for
     // this grid to complete before it reads anything this grid writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
     const int32_t B = a.B;
     const int32_t base = min(kBlock, 1 + L.p.head);
     const int64_t vpr = VEC ? (int64_t)a.V / Elem<DT>::W : (int64_t)a.V;
-    const int64_t total1 = (int64_t)B * base * vpr;
-    const int64_t lo1 = total1 * blockIdx.x / gridDim.x;
-    const int64_t hi1 = total1 * (blockIdx.x + 1) / gridDim.x;
-    for (int64_t lo = lo1; lo < hi1;) {
-        const int64_t ri = lo / vpr;
-        const int64_t s1 = min(hi1, (ri + 1) * vpr) - ri * vpr;
-        piece_max<DT, VEC>(a, (int32_t)(ri / base), (int32_t)(ri % base), lo - ri * vpr, s1, sm);
-        __syncthreads();  // sm.red is reused by the next piece
-        lo = (ri + 1) * vpr;
+    if (tid == 0) {
+        sm_nd = 0;
+        sm_waited = 0;
     }
-    // The blocks and lengths come from the proposal grid.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    block_prefix(B, [&a, base](int32_t b) { return predicted_rows(a, b, base); }, sm_prefix, sm.warp);
+
+    // Phase 1: the predicted rows.
+    const int64_t total1 = (int64_t)sm_prefix[B] * vpr;
+    int64_t lo = total1 * blockIdx.x / gridDim.x;
+    int64_t hi = total1 * (blockIdx.x + 1) / gridDim.x;
+    if (lo < hi) {
+        int64_t ri = lo / vpr;
+        int32_t b = owner_of(sm_prefix, B, ri);
+        while (lo < hi) {
+            while (sm_prefix[b + 1] <= ri) ++b;
+            const int64_t s0 = lo - ri * vpr;
+            const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
+            piece_max<DT, VEC>(a, b, (int32_t)(ri - sm_prefix[b]), s0, s1, sm);
+            if (tid == 0) {
+                __threadfence();
+                const unsigned long long add = (unsigned long long)(s1 - s0);
+                sm_db[sm_nd] = b;
+                sm_dc[sm_nd] = atomicAdd(a.done + b, add) + add;
+                sm_nd += 1;
+            }
+            __syncthreads();
+            if (sm_nd == kVMaxDefer || lo + (s1 - s0) >= hi) {
+                // Check the deferred counts (needs the lengths: wait first).
+                if (!sm_waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+                __syncthreads();
+                const int32_t nd = sm_nd;
+                if (tid == 0) sm_waited = 1;
+                for (int32_t i = 0; i < nd; ++i) {
+                    const int32_t db = sm_db[i];
+                    const int32_t Lb = a.len[db];
+                    const int32_t rows = len_ok(Lb) ? max(Lb, predicted_rows(a, db, base)) : predicted_rows(a, db, base);
+                    if (sm_dc[i] == (unsigned long long)rows * (unsigned long long)vpr) finalize<true>(a, L, db, Lb, sm);
+                    __syncthreads();
+                }
+                if (tid == 0) sm_nd = 0;
+                __syncthreads();
+            }
+            ri += 1;
+            lo = ri * vpr;
+        }
+    }
+    if (!sm_waited) asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
-    block_row_prefix(a.len, B, base, sm_prefix, sm.warp);
-    auto need_rows = [base](int32_t, int32_t l) { return len_ok(l) ? max(l, base) : base; };
-    for (int64_t lo = lo1; lo < hi1;) {
-        const int64_t ri = lo / vpr;
-        const int64_t s1 = min(hi1, (ri + 1) * vpr) - ri * vpr;
-        const int32_t b = (int32_t)(ri / base);
+    // Phase 2: rows the prediction missed (true length beyond the prediction).
+    block_prefix(B, [&a, base](int32_t b) {
         const int32_t Lb = a.len[b];
-        piece_count<true>(a, L, b, (unsigned long long)(s1 - (lo - ri * vpr)),
-                          (unsigned long long)need_rows(b, Lb) * (unsigned long long)vpr, Lb, sm);
-        lo = (ri + 1) * vpr;
+        return len_ok(Lb) ? max(0, Lb - predicted_rows(a, b, base)) : 0;
+    }, sm_prefix, sm.warp);
+    const int64_t total2 = (int64_t)sm_prefix[B] * vpr;
+    lo = total2 * blockIdx.x / gridDim.x;
+    hi = total2 * (blockIdx.x + 1) / gridDim.x;
+    if (lo >= hi) return;
+    int64_t ri = lo / vpr;
+    int32_t b = owner_of(sm_prefix, B, ri);
+    while (lo < hi) {
+        while (sm_prefix[b + 1] <= ri) ++b;
+        const int32_t pr = predicted_rows(a, b, base);
+        const int64_t s0 = lo - ri * vpr;
+        const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
+        piece_max<DT, VEC>(a, b, pr + (int32_t)(ri - sm_prefix[b]), s0, s1, sm);
+        const int32_t Lb = a.len[b];
+        piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), (unsigned long long)Lb * (unsigned long long)vpr,
+                          Lb, sm);
+        ri += 1;
+        lo = ri * vpr;
     }
-    verify_rows<DT, VEC, true>(a, L, sm_prefix, base, vpr, need_rows, sm);
 }
 
-// Resident CTAs per SM of `kern` (times 1024, plus the SM count), cached per
-// device and kernel for dynamic shared memory sizes up to 4 KB (B < 1,024),
-// which almost every call uses; larger sizes are queried each time.
 template <typename Kern>
 int occupancy(Kern kern, size_t smem, int* packed)
 {
@@ -622,6 +691,7 @@ extern "C" int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t ro
     a.B = B;
     a.block = d_block;
     a.len = d_len;
+    a.len_hint = nullptr;
     a.argmax = d_argmax;
     a.accept = d_accept;
     a.emitted = d_emitted;
@@ -635,8 +705,9 @@ extern "C" int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t ro
 
 extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                                  int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
-                                 const int32_t* d_block, const int32_t* d_len, int32_t* d_argmax, int32_t* d_accept,
-                                 int32_t* d_emitted, int32_t* d_out_tok, clk_stream_t s)
+                                 const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
+                                 int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok,
+                                 clk_stream_t s)
 {
     int rc = check_batch(h, B);
     if (rc != CLK_OK) return rc;
@@ -644,7 +715,7 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
                       d_out_tok);
     if (rc != CLK_OK) return rc;
     if (B == 0) return CLK_OK;
-    if (!ok_i32(d_slots)) return CLK_EINVAL;
+    if (!ok_i32(d_slots) || (d_len_hint != nullptr && !aligned(d_len_hint, 4))) return CLK_EINVAL;
     VerifyArgs a;
     a.logits = d_logits;
     a.row_stride = row_stride;
@@ -653,6 +724,7 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.B = B;
     a.block = d_block;
     a.len = d_len;
+    a.len_hint = d_len_hint;
     a.argmax = d_argmax;
     a.accept = d_accept;
     a.emitted = d_emitted;
@@ -723,6 +795,7 @@ extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int
     a.B = B;
     a.block = d_block;
     a.len = d_len;
+    a.len_hint = nullptr;
     a.argmax = d_argmax;
     a.accept = d_accept;
     a.emitted = d_emitted;

@@ -296,16 +296,21 @@ CLK_API int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_
  * immediate index update).  Uses the scratch inside the lookup workspace.
  * Results are bit-identical to the two calls.
  * Launch order: the launch is a programmatic dependent of the preceding
- * launch on the stream.  It reads rows 0 .. head of every request (the rows
- * every block covers) before it waits for that launch, so the logits must
+ * launch on the stream, and d_block / d_len may come from that launch
+ * (clk_propose_fuse_sched).  Before it waits for it, it reads the rows of a
+ * predicted length of every request: max(1 + head, d_len_hint[b]) when the
+ * hint is a valid length, else 1 + head (the short block, which every block
+ * covers); after the wait it reads the rows the prediction missed.
+ * d_len_hint (nullable) is only a prediction, e.g. the previous step's
+ * lengths in a buffer the preceding launch does not write: any value gives
+ * the same results, a good one saves a second pass.  So the logits must
  * already be complete when this call is made (as after any ordinary kernel
- * or copy on the stream) and must hold at least min(16, 1 + head) rows per
- * request; d_block and d_len may come from the preceding launch
- * (clk_propose_fuse_sched). */
+ * or copy on the stream) and must hold every predicted row (16 rows per
+ * request serve any hint). */
 CLK_API int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                               int64_t row_stride, int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block,
-                              const int32_t* d_len, int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted,
-                              int32_t* d_out_tok, clk_stream_t s);
+                              const int32_t* d_len, const int32_t* d_len_hint, int32_t* d_argmax,
+                              int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok, clk_stream_t s);
 
 /* ---------------------------------------------------------------------- */
 /* Status, counters, inspection (these synchronise the stream)             */

@@ -191,3 +191,36 @@ def test_scratch_is_left_clean_for_reuse():
     for f, s in zip(first, second):
         assert np.array_equal(f, s)
     assert int(scratch.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("hint", ["none", "short", "long", "mixed", "garbage"])
+def test_fused_verify_results_do_not_depend_on_the_length_hint(hint):
+    """clk_verify_append reads the rows of a predicted length before the
+    proposal launch has finished; the prediction changes only what is read
+    early, never the outputs or the committed tokens."""
+    rng = np.random.default_rng(8)
+    B, V = 40, 4096
+    x = torch.from_numpy(rng.integers(-20, 20, size=(B, 16, V)).astype(np.float32)).to("cuda").to(torch.bfloat16)
+    L = rng.choice([8, 16], size=B).astype(np.int32)
+    L[::7] = 0  # invalid lengths take the empty result
+    block = _blocks_from(_np_view(x), np.where(L > 0, L, 1), rng, p_agree=0.9)
+    want = _oracle_rows(_np_view(x), block, L)
+    hints = {"none": None, "short": np.full(B, 8), "long": np.full(B, 16),
+             "mixed": rng.choice([8, 16], size=B), "garbage": rng.integers(-5, 40, size=B)}
+    h = hints[hint]
+    lk = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+    s = torch.arange(B, dtype=torch.int32, device="cuda")
+    clk.lookup_init(lk, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                    torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+    z = lambda *sh: torch.full(sh, 77, dtype=torch.int32, device="cuda")  # noqa: E731
+    g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+    hint_t = None if h is None else torch.from_numpy(h.astype(np.int32)).cuda()
+    clk.verify_append(lk, s, x, torch.from_numpy(block).cuda(), torch.from_numpy(L).cuda(), g, a, e, out,
+                      length_hint=hint_t)
+    torch.cuda.synchronize()
+    for name, gg, ww in zip(("argmax", "accept", "emitted", "out_tok"), (g, a, e, out), want):
+        assert np.array_equal(gg.cpu().numpy(), ww), name
+    for b in range(B):
+        committed = want[3][b][:want[2][b]].tolist()
+        assert lk.history(b).tolist() == [1] + committed
+    assert lk.status()[0] == (clk.EINVAL if (L == 0).any() else 0)
