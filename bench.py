@@ -168,7 +168,9 @@ def run_ours(args, world, rank, local, dist):
     if W + K > w.steps:  # the workload's streams cover w.steps steps
         K = w.steps - W
     B, V = w.B, w.V
-    params = clk.Params.default()
+    params = clk.Params.default(**getattr(args, "overrides", {}))
+    if params.head > wl.HEAD:
+        raise ValueError(f"head {params.head}: the synthetic draft model proposes {wl.HEAD} tokens")
     stream = torch.cuda.current_stream(device)
 
     # Lookup state; the prompt ingestion (index build) is timed on its own.
@@ -177,8 +179,17 @@ def run_ours(args, world, rank, local, dist):
     d_ptok, d_poff = torch.from_numpy(ptok).to(device), torch.from_numpy(poff).to(device)
     gen = wl.DevGen(w, device=device)
     st = clk.Step(lk, slots)
-    head = torch.zeros((B, wl.HEAD), dtype=torch.int32, device=device)
-    assert params.head == wl.HEAD
+    head = torch.zeros((B, params.head), dtype=torch.int32, device=device)
+    head7 = torch.zeros((B, wl.HEAD), dtype=torch.int32, device=device)
+
+    def gen_head(t, out, pos=None):
+        """The first params.head of the synthetic model's proposals for step t."""
+        if params.head == wl.HEAD:
+            gen.head(t, out, pos=pos)
+        else:
+            gen.head(t, head7, pos=pos)
+            out.copy_(head7[:, :params.head])
+
     logits = gen.alloc_logits()
 
     def reinit():
@@ -199,7 +210,7 @@ def run_ours(args, world, rank, local, dist):
     pos_hist = torch.zeros((W + K + 1, B), dtype=torch.int64, device=device)
     for t in range(W + K):
         pos_hist[t].copy_(gen.pos)
-        gen.head(t, head)
+        gen_head(t, head)
         st.pre(head)
         gen.logits(logits)
         st.post(logits)
@@ -209,7 +220,7 @@ def run_ours(args, world, rank, local, dist):
 
     per_step = B * 16 * V * (2 if w.dtype == wl.BF16 else 4)
     chunk = max(1, min(K, int(args.input_gb * 2 ** 30 // per_step)))
-    heads = torch.zeros((chunk, B, wl.HEAD), dtype=torch.int32, device=device)
+    heads = torch.zeros((chunk, B, params.head), dtype=torch.int32, device=device)
     bufs = torch.empty((chunk, B, 16, V), dtype=gen.torch_dtype(), device=device)
     flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=device)  # > 2x the 129 MB L2
     del logits
@@ -218,7 +229,7 @@ def run_ours(args, world, rank, local, dist):
         reinit()
         lg = bufs[0]
         for t in range(W):
-            gen.head(t, head)
+            gen_head(t, head)
             st.pre(head)
             gen.logits(lg)
             st.post(lg)
@@ -227,7 +238,7 @@ def run_ours(args, world, rank, local, dist):
 
     def generate(t0, n):
         for i in range(n):
-            gen.head(t0 + i, heads[i], pos=pos_hist[t0 + i])
+            gen_head(t0 + i, heads[i], pos=pos_hist[t0 + i])
             gen.logits(bufs[i], pos=pos_hist[t0 + i])
         flush.zero_()  # no step may find its logits in L2
         torch.cuda.synchronize()
@@ -288,12 +299,15 @@ def run_ours(args, world, rank, local, dist):
     # between them.
     warmup()
     c_w = lk.counters(-1)
-    rows_b = 8 * (cb["steps"] - c_w["steps"]) + 8 * (cb["long_steps"] - c_w["long_steps"])
+    rows_b = params.short_len * (cb["steps"] - c_w["steps"]) + \
+        (params.long_len - params.short_len) * (cb["long_steps"] - c_w["long_steps"])
     clocks = ClockSampler(local)
     time.sleep(0.3)
     total_ms = 0.0
     launches = 0
     c_before = lk.counters(-1)
+    slot_list = [int(x) for x in slots.tolist()]
+    per_before = [lk.counters(x) for x in slot_list]
     t = W
     while t < W + K:
         n = min(chunk, W + K - t)
@@ -316,6 +330,7 @@ def run_ours(args, world, rank, local, dist):
         t += n
     clocks.stop()
     c_after = lk.counters(-1)
+    per_after = [lk.counters(x) for x in slot_list]
     status = lk.status()
     # Determinism check: the timed steps ended where the dry run did.
     if status[0] != 0:
@@ -327,7 +342,7 @@ def run_ours(args, world, rank, local, dist):
 
     total_s = max_over_ranks(total_ms * 1e-3, dist, world, device)
     dc = {k: c_after[k] - c_before[k] for k in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")}
-    rows = 8 * dc["steps"] + (params.long_len - params.short_len) * dc["long_steps"]
+    rows = params.short_len * dc["steps"] + (params.long_len - params.short_len) * dc["long_steps"]
     esz = 2 if w.dtype == wl.BF16 else 4
     verify_bytes = rows * V * esz                       # logits rows read, all timed steps
     path_bytes = verify_bytes + LOOKUP_BYTES_PER_REQ * B * K
@@ -356,7 +371,8 @@ def run_ours(args, world, rank, local, dist):
                    "emitted_tok_s": round(world * dc["emitted"] / total_s, 1),
                    "emitted_per_request_step": round(dc["emitted"] / max(1, dc["steps"]), 4),
                    "accepted_per_request_step": round(dc["accepted"] / max(1, dc["steps"]), 4),
-                   "long_block_share": round(dc["long_steps"] / max(1, dc["steps"]), 4)},
+                   "long_block_share": round(dc["long_steps"] / max(1, dc["steps"]), 4),
+                   "by_kind": _kind_metrics(per_after, per_before, w.kinds, params.head)},
         "path": {"bytes_per_step": int(path_bytes // K), "verify_bytes_per_step": int(verify_bytes // K),
                  "achieved_gbs": round(path_gbs, 1), "frac": round(path_gbs / peak, 4),
                  "alone_us": {"propose_fuse_sched": round(pre_ms * 1e3 / nb, 3),
@@ -380,6 +396,48 @@ def run_ours(args, world, rank, local, dist):
         "cpu_baseline": cpu,
     }
     return out
+
+
+# Draft-block variants: the pages' 15-draft long block against 7 drafts only,
+# the sticky exit on and off, and other splits of the block between the
+# draft model's head and the lookup tail.
+SWEEP = [
+    ("15 drafts (7 head + 8 tail), sticky 3", {}),
+    ("15 drafts, sticky 0 (exit on the first flag drop)", {"sticky": 0}),
+    ("15 drafts, sticky 6", {"sticky": 6}),
+    ("7 drafts (short blocks only)", {"tail": 0}),
+    ("15 drafts as 5 head + 10 tail", {"head": 5, "tail": 10}),
+    ("15 drafts as 3 head + 12 tail", {"head": 3, "tail": 12}),
+]
+
+
+def run_sweep(args, world, rank, local, dist):
+    """The measured step (same timing as the headline) once per variant."""
+    import copy
+
+    rows = []
+    for name, over in SWEEP:
+        a = copy.copy(args)
+        a.overrides, a.no_e2e, a.no_cpu_baseline, a.ablation = over, True, True, False
+        r = run_ours(a, world, rank, local, dist)
+        tk = r["tokens"]
+        rows.append({"variant": name, "params": over, "value": r["value"], "ms_per_step": r["ms_per_step"],
+                     "emitted_per_request_step": tk["emitted_per_request_step"],
+                     "emitted_tok_s": tk["emitted_tok_s"], "long_block_share": tk["long_block_share"],
+                     "tail_share": {k: v["tail_share"] for k, v in tk["by_kind"].items()},
+                     "path_frac": r["path"]["frac"]})
+    return {"metric": METRIC, "unit": UNIT, "n_gpus": world, "steps": r["steps"], "warmup": r["warmup"],
+            "config": r["config"], "sweep": rows, "clocks": r.get("clocks")}
+
+
+def _kind_metrics(after, before, kinds, head):
+    """Hit rate, mean accepted length, tail share of the accepted drafts and
+    accepted-length histograms over the timed steps, per workload kind."""
+    from context_lookup_speculative_gb300 import metrics
+    out = metrics.by_kind(metrics.delta(after, before), kinds, head)
+    keep = ("requests", "steps", "hit_rate", "long_share", "mean_accepted", "tokens_per_step",
+            "draft_acceptance", "tail_share", "accept_hist")
+    return {k: {f: v[f] for f in keep} for k, v in out.items()}
 
 
 def run_lookup_ablation(lk, slots, w, device, reps: int = 20):
@@ -540,6 +598,8 @@ def main(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="block-size and sticky variants of the measured step on --config, one JSON line")
     ap.add_argument("--ablation", action="store_true",
                     help="also time the proposal by index vs by full history scan (GPU and CPU oracle)")
     args = ap.parse_args(argv)
@@ -554,7 +614,7 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group(backend="nccl")
     try:
-        out = run_ours(args, world, rank, local, dist)
+        out = run_sweep(args, world, rank, local, dist) if args.sweep else run_ours(args, world, rank, local, dist)
         if rank == 0:
             print(json.dumps(out), flush=True)
     finally:

@@ -194,7 +194,7 @@ __device__ __forceinline__ int32_t sched_apply(const clk_params& p, SlotState* s
     st->cur_len = len;
     st->steps += 1;
     st->hits += (k >= p.min_k) ? 1 : 0;
-    st->long_steps += (len == long_len(p)) ? 1 : 0;
+    st->long_steps += (p.tail > 0 && len == long_len(p)) ? 1 : 0;  // no tail: no long block
     st->drafted += p.head + ((len == long_len(p) && k >= p.tail_k) ? p.tail : 0);
     return len;
 }
@@ -281,7 +281,7 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
             if (len != 0 && count > 0) {
                 st->accepted += count - 1;
                 st->emitted += count;
-                if (count - 1 < 16) st->accept_hist[len == long_len(L.p) ? 1 : 0][count - 1] += 1;
+                if (count - 1 < 16) st->accept_hist[(L.p.tail > 0 && len == long_len(L.p)) ? 1 : 0][count - 1] += 1;
             }
             st->cur_len = 0;
         }

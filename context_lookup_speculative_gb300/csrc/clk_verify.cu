@@ -445,13 +445,23 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 // programmatic dependent of the proposal launch that produces the blocks and
 // lengths.  Before it waits for that launch it reads, for every request, the
 // rows of a predicted length (the short block, or the caller's hint, e.g. the
-// previous step's length, when that is longer); after the wait it reads the
-// rows the prediction missed.  Every addition to a request's vector counter
-// returns the new count; a count that equals the request's total (known only
-// after the wait, max(predicted, true length) rows) finishes the request, so
-// additions made before the wait are checked after it.  The answer does not
-// depend on the prediction; a wrong one costs only reads.
+// previous step's length, when that is longer); after the wait it also reads
+// the rows the prediction missed.  Every addition to a request's vector
+// counter returns the new count; a count that equals the request's total
+// (known only after the wait, max(predicted, true length) rows) finishes the
+// request, so additions made before the wait are checked after it.  The
+// answer does not depend on the prediction; a wrong one costs only reads.
+//
+// Each CTA streams its even share of the predicted rows in two halves.
+// Between them it waits for the proposal launch (done by then in the steady
+// state, where this launch overlaps it), checks the counts it deferred, lays
+// out the missed rows and streams its share of them; the second half of the
+// predicted rows follows with every count checked at once.  The latency-
+// bound work (the checks, the missed rows' short pieces) thus runs while the
+// other CTAs stream, and the launch ends soon after its last bytes arrive.
+// A CTA with a short share (small batches) streams all of it first.
 constexpr int kVMaxDefer = 32;
+constexpr int64_t kVSplitMin = 16 * kVThreads;  // vectors: shares below this are not split
 
 // Rows read before the wait for request b.
 __device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b, int32_t base)
@@ -460,100 +470,129 @@ __device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b
     return len_ok(h) ? max(h, base) : base;
 }
 
+struct StepSmem {
+    int32_t db[kVMaxDefer];             // deferred checks: request,
+    unsigned long long dc[kVMaxDefer];  // the count its addition returned,
+    int32_t dl[kVMaxDefer];             // and (after the wait) its length
+    int32_t nd;
+    int32_t waited;
+};
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
 {
-    extern __shared__ int32_t sm_prefix[];  // B + 1
+    extern __shared__ int32_t sm_prefix[];  // P1[B + 1] (predicted rows), then P2[B + 1] (missed rows)
     __shared__ VerifySmem sm;
-    __shared__ int32_t sm_db[kVMaxDefer];              // deferred checks: request
-    __shared__ unsigned long long sm_dc[kVMaxDefer];   // and the count its addition returned
-    __shared__ int32_t sm_nd;
-    __shared__ int32_t sm_waited;
+    __shared__ StepSmem ss;
     // Let the next launch (the next proposal) be scheduled; it waits for
     // this grid to complete before it reads anything this grid writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int32_t B = a.B;
+    int32_t* P1 = sm_prefix;
+    int32_t* P2 = sm_prefix + (B + 1);
     const int32_t base = min(kBlock, 1 + L.p.head);
     const int64_t vpr = VEC ? (int64_t)a.V / Elem<DT>::W : (int64_t)a.V;
     if (tid == 0) {
-        sm_nd = 0;
-        sm_waited = 0;
+        ss.nd = 0;
+        ss.waited = 0;
     }
-    block_prefix(B, [&a, base](int32_t b) { return predicted_rows(a, b, base); }, sm_prefix, sm.warp);
+    block_prefix(B, [&a, base](int32_t b) { return predicted_rows(a, b, base); }, P1, sm.warp);
 
-    // Phase 1: the predicted rows.
-    const int64_t total1 = (int64_t)sm_prefix[B] * vpr;
-    int64_t lo = total1 * blockIdx.x / gridDim.x;
-    int64_t hi = total1 * (blockIdx.x + 1) / gridDim.x;
-    if (lo < hi) {
-        int64_t ri = lo / vpr;
-        int32_t b = owner_of(sm_prefix, B, ri);
-        while (lo < hi) {
-            while (sm_prefix[b + 1] <= ri) ++b;
-            const int64_t s0 = lo - ri * vpr;
-            const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
-            piece_max<DT, VEC>(a, b, (int32_t)(ri - sm_prefix[b]), s0, s1, sm);
-            if (tid == 0) {
-                __threadfence();
-                const unsigned long long add = (unsigned long long)(s1 - s0);
-                sm_db[sm_nd] = b;
-                sm_dc[sm_nd] = atomicAdd(a.done + b, add) + add;
-                sm_nd += 1;
-            }
+    // Vectors read for request b: its predicted rows, or its true length
+    // when that is longer (valid lengths only).
+    auto total = [&](int32_t b, int32_t Lb) -> unsigned long long {
+        const int32_t pr = P1[b + 1] - P1[b];
+        return (unsigned long long)(len_ok(Lb) ? max(Lb, pr) : pr) * (unsigned long long)vpr;
+    };
+    // Block-wide: wait for the proposal launch (first call: also lay out the
+    // missed rows in P2), then decide the deferred counts.
+    auto flush = [&]() {
+        if (!ss.waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            block_prefix(B, [&a, P1](int32_t b) {
+                const int32_t Lb = __ldcg(a.len + b);
+                return len_ok(Lb) ? max(0, Lb - (P1[b + 1] - P1[b])) : 0;
+            }, P2, sm.warp);
+            if (tid == 0) ss.waited = 1;
+        }
+        const int32_t nd = ss.nd;
+        if (tid < nd) ss.dl[tid] = __ldcg(a.len + ss.db[tid]);
+        __syncthreads();
+        for (int32_t i = 0; i < nd; ++i) {
+            if (ss.dc[i] == total(ss.db[i], ss.dl[i])) finalize<true>(a, L, ss.db[i], ss.dl[i], sm);
             __syncthreads();
-            if (sm_nd == kVMaxDefer || lo + (s1 - s0) >= hi) {
-                // Check the deferred counts (needs the lengths: wait first).
-                if (!sm_waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-                __syncthreads();
-                const int32_t nd = sm_nd;
-                if (tid == 0) sm_waited = 1;
-                for (int32_t i = 0; i < nd; ++i) {
-                    const int32_t db = sm_db[i];
-                    const int32_t Lb = a.len[db];
-                    const int32_t rows = len_ok(Lb) ? max(Lb, predicted_rows(a, db, base)) : predicted_rows(a, db, base);
-                    if (sm_dc[i] == (unsigned long long)rows * (unsigned long long)vpr) finalize<true>(a, L, db, Lb, sm);
-                    __syncthreads();
+        }
+        if (tid == 0) ss.nd = 0;
+        __syncthreads();
+    };
+    // The predicted-row vectors [from, to) of the flat range, piece by piece
+    // (one piece per row).  Before the wait the counts are deferred.
+    auto phase1 = [&](int64_t from, int64_t to) {
+        if (from >= to) return;
+        int64_t ri = from / vpr;
+        int32_t b = owner_of(P1, B, ri);
+        int64_t lo = from;
+        while (lo < to) {
+            while (P1[b + 1] <= ri) ++b;
+            const int64_t s0 = lo - ri * vpr;
+            const int64_t s1 = min(to, (ri + 1) * vpr) - ri * vpr;
+            piece_max<DT, VEC>(a, b, (int32_t)(ri - P1[b]), s0, s1, sm);
+            if (ss.waited) {
+                piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, __ldcg(a.len + b)),
+                                  __ldcg(a.len + b), sm);
+            } else {
+                if (tid == 0) {
+                    __threadfence();
+                    const unsigned long long add = (unsigned long long)(s1 - s0);
+                    ss.db[ss.nd] = b;
+                    ss.dc[ss.nd] = atomicAdd(a.done + b, add) + add;
+                    ss.nd += 1;
                 }
-                if (tid == 0) sm_nd = 0;
                 __syncthreads();
+                if (ss.nd == kVMaxDefer) flush();
             }
             ri += 1;
             lo = ri * vpr;
         }
+    };
+
+    const int64_t total1 = (int64_t)P1[B] * vpr;
+    const int64_t lo = total1 * blockIdx.x / gridDim.x;
+    const int64_t hi = total1 * (blockIdx.x + 1) / gridDim.x;
+    const int64_t mid = (hi - lo >= kVSplitMin) ? lo + (hi - lo) / 2 : hi;
+    phase1(lo, mid);
+    flush();
+    // This CTA's share of the rows the prediction missed.
+    const int64_t total2 = (int64_t)P2[B] * vpr;
+    int64_t lo2 = total2 * blockIdx.x / gridDim.x;
+    const int64_t hi2 = total2 * (blockIdx.x + 1) / gridDim.x;
+    if (lo2 < hi2) {
+        int64_t ri = lo2 / vpr;
+        int32_t b = owner_of(P2, B, ri);
+        while (lo2 < hi2) {
+            while (P2[b + 1] <= ri) ++b;
+            const int32_t pr = P1[b + 1] - P1[b];
+            const int64_t s0 = lo2 - ri * vpr;
+            const int64_t s1 = min(hi2, (ri + 1) * vpr) - ri * vpr;
+            piece_max<DT, VEC>(a, b, pr + (int32_t)(ri - P2[b]), s0, s1, sm);
+            const int32_t Lb = __ldcg(a.len + b);
+            piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, Lb), Lb, sm);
+            ri += 1;
+            lo2 = ri * vpr;
+        }
     }
-    if (!sm_waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-    __syncthreads();
-    // Phase 2: rows the prediction missed (true length beyond the prediction).
-    block_prefix(B, [&a, base](int32_t b) {
-        const int32_t Lb = a.len[b];
-        return len_ok(Lb) ? max(0, Lb - predicted_rows(a, b, base)) : 0;
-    }, sm_prefix, sm.warp);
-    const int64_t total2 = (int64_t)sm_prefix[B] * vpr;
-    lo = total2 * blockIdx.x / gridDim.x;
-    hi = total2 * (blockIdx.x + 1) / gridDim.x;
-    if (lo >= hi) return;
-    int64_t ri = lo / vpr;
-    int32_t b = owner_of(sm_prefix, B, ri);
-    while (lo < hi) {
-        while (sm_prefix[b + 1] <= ri) ++b;
-        const int32_t pr = predicted_rows(a, b, base);
-        const int64_t s0 = lo - ri * vpr;
-        const int64_t s1 = min(hi, (ri + 1) * vpr) - ri * vpr;
-        piece_max<DT, VEC>(a, b, pr + (int32_t)(ri - sm_prefix[b]), s0, s1, sm);
-        const int32_t Lb = a.len[b];
-        piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), (unsigned long long)Lb * (unsigned long long)vpr,
-                          Lb, sm);
-        ri += 1;
-        lo = ri * vpr;
-    }
+    phase1(mid, hi);
 }
 
-template <typename Kern>
-int occupancy(Kern kern, size_t smem, int* packed)
+// Resident CTAs per SM of kernel `Kern` and the SM count, packed as
+// occ * 1024 + sms; cached per kernel and device for small shared memory.
+template <auto Kern>
+int occupancy(size_t smem, int* packed)
 {
     constexpr int kDevices = 64;
-    static int cache[kDevices] = {0};
+    static int cache[kDevices] = {0};  // one table per kernel (template argument)
+    const auto kern = Kern;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
     const bool cacheable = dev >= 0 && dev < kDevices && smem <= 4096;
@@ -577,11 +616,11 @@ int occupancy(Kern kern, size_t smem, int* packed)
     return CLK_OK;
 }
 
-template <typename Kern>
-int verify_grid(Kern kern, size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
+template <auto Kern>
+int verify_grid(size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
 {
     int packed = 0;
-    const int rc = occupancy(kern, smem, &packed);
+    const int rc = occupancy<Kern>(smem, &packed);
     if (rc != CLK_OK) return rc;
     const int occ = packed / 1024, sms = packed % 1024;
     const int64_t max_work = (int64_t)B * kBlock * vpr;
@@ -597,17 +636,17 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
 {
     constexpr int W = VEC ? Elem<DT>::W : 1;
     const int64_t vpr = (int64_t)a.V / W;
-    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
+    const size_t smem = (size_t)(FUSED ? 2 : 1) * (a.B + 1) * sizeof(int32_t);
     int64_t grid = 0;
     if (!FUSED) {
         auto kern = k_verify<DT, VEC>;
-        int rc = verify_grid(kern, smem, a.B, vpr, &grid);
+        int rc = verify_grid<k_verify<DT, VEC>>(smem, a.B, vpr, &grid);
         if (rc != CLK_OK) return rc;
         kern<<<(unsigned)grid, kVThreads, smem, s>>>(a, L);
         return launch_status();
     }
     auto kern = k_verify_step<DT, VEC>;
-    int rc = verify_grid(kern, smem, a.B, vpr, &grid);
+    int rc = verify_grid<k_verify_step<DT, VEC>>(smem, a.B, vpr, &grid);
     if (rc != CLK_OK) return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);

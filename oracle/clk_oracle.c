@@ -330,11 +330,11 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
         n += acc + 1;
         cnt->steps += 1;
         cnt->hits += (k >= p->min_k);
-        cnt->long_steps += (L == long_L);
+        cnt->long_steps += (p->tail > 0 && L == long_L); /* with no tail there is no long block */
         cnt->drafted += p->head + ((L == long_L && k >= p->tail_k) ? p->tail : 0);
         cnt->accepted += acc;
         cnt->emitted += acc + 1;
-        cnt->accept_hist[L == long_L][acc] += 1;
+        cnt->accept_hist[p->tail > 0 && L == long_L][acc] += 1;
         prev_a = acc;
         prev_L = L;
 

@@ -43,6 +43,15 @@ def test_fp32_and_block_variants():
     _parity(w, params=clk.Params.default(**kw), oparams=oracle.Params.default(**kw))
 
 
+@pytest.mark.parametrize("kw", [{"tail": 0}, {"head": 5, "tail": 10}, {"head": 3, "tail": 12},
+                                {"sticky": 6}])
+def test_draft_block_variants(kw):
+    """The variants the benchmark's sweep times: short blocks only, other
+    head/tail splits of the 15 drafts, a longer sticky exit."""
+    w = wl.make_small("mixed", seed=74, B=8, V=2048, steps=96)
+    _parity(w, params=clk.Params.default(**kw), oparams=oracle.Params.default(**kw))
+
+
 def test_config0_tiny():
     _parity(wl.make("0"))
 

@@ -70,3 +70,15 @@ def test_tail_share_hand_counts():
     assert s["tail_accepted"] == 8 + 2  # slots 8..15 of the first step, 8..9 of the second
     assert s["tail_share"] == pytest.approx(10 / 33, abs=1e-6)
     assert s["tokens_per_step"] == pytest.approx(37 / 4, abs=1e-6)
+
+
+def test_short_blocks_only_count_no_long_steps():
+    # with no tail (7 drafts, the pages' short setting) every block has
+    # 1 + head slots, so no step is a long block whatever the scheduler's mode
+    w = wl.make_small("copy", seed=92, B=4, V=2048, steps=48)
+    ref = oracle.run(w, params=oracle.Params.default(tail=0), threads=4)
+    s = metrics.summarize(ref.counters)
+    assert s["long_steps"] == 0 and s["long_share"] == 0
+    assert sum(s["accept_hist"]["long"]) == 0 and sum(s["accept_hist"]["short"]) == s["steps"]
+    assert s["tail_accepted"] == 0 and (np.asarray(ref.L) == 8).all()
+    assert s["drafted"] == 7 * s["steps"]
