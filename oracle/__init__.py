@@ -105,6 +105,11 @@ def _lib() -> ctypes.CDLL:
     lib.or_argmax_bf16.restype = ctypes.c_int32
     lib.or_accept.argtypes = [_P, _P, ctypes.c_int32]
     lib.or_accept.restype = ctypes.c_int32
+    lib.or_sample_weights.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_double]
+    lib.or_sample_weights.restype = ctypes.c_int32
+    lib.or_sample_verify.argtypes = [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int32,
+                                     ctypes.c_float, _P, _P]
+    lib.or_sample_verify.restype = ctypes.c_int32
     lib.or_run.argtypes = [ctypes.POINTER(RunArgs)]
     lib.or_run.restype = ctypes.c_int
     lib.or_counters_size.restype = ctypes.c_size_t
@@ -180,6 +185,33 @@ def accept(blk, g, L: int) -> int:
     blk = _i32(blk)
     g = _i32(g)
     return int(_lib().or_accept(blk.ctypes.data, g.ctypes.data, L))
+
+
+def sample_weights(e, excl: int, u: float) -> int:
+    """Inverse-CDF sample of the weights e (float64) without token `excl`."""
+    e = np.ascontiguousarray(e, dtype=np.float64)
+    return int(_lib().or_sample_weights(e.ctypes.data, e.size, int(excl), float(u)))
+
+
+def sample_verify(rows: np.ndarray, blk, L: int, inv_temp: float, u) -> tuple:
+    """Sampling verification of one request with point-mass drafts.
+
+    rows: [R >= L, V] float32 logits or bf16 bits (uint16); blk: 16 tokens;
+    inv_temp: 1 / temperature (float32); u: [16, 2] float32 uniforms
+    (acceptance, sample) per row.  Returns (accepted drafts a, out_tok[16]);
+    a = -1 for an invalid L."""
+    rows = np.ascontiguousarray(rows)
+    if rows.dtype == np.uint16:
+        dtype = 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.float32)
+        dtype = 1
+    blk = _i32(blk)
+    u = np.ascontiguousarray(u, dtype=np.float32).reshape(BLOCK, 2)
+    out = np.empty(BLOCK, np.int32)
+    a = _lib().or_sample_verify(rows.ctypes.data, dtype, rows.shape[1], rows.shape[1], blk.ctypes.data, int(L),
+                                float(inv_temp), u.ctypes.data, out.ctypes.data)
+    return int(a), out
 
 
 # --------------------------------------------------------------------------

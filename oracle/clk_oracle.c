@@ -27,6 +27,10 @@
  *   Greedy verification: row-wise argmax over the target logits (lowest
  *     index on ties), the accepted prefix up to the first mismatch, plus the
  *     target's own token at the first mismatch (the bonus token).
+ *   Sampling verification (same section, closing paragraph): each draft is
+ *     a point mass, accepted with the target's probability of it; the first
+ *     rejection emits a sample of the target without that token, and a fully
+ *     accepted block emits a sample of the last row (see or_sample_verify).
  *
  * Readings adopted where the pages are silent (each one a parameter):
  *   - ties on length go to the most recent occurrence; length first;
@@ -217,6 +221,112 @@ int32_t or_accept(const int32_t* blk, const int32_t* g, int32_t L)
 {
     int32_t a = 0;
     while (a < L - 1 && blk[a + 1] == g[a]) a += 1;
+    return a;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sampling verification with point-mass drafts.                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * HyperQwen context-lookup article, closing paragraph of "lookup 草稿的原理：
+ * 三步走": for a sampled request every position the lookup filled is treated
+ * as a point mass on its proposed token, which the standard speculative
+ * rejection sampler accepts as a proposal distribution, so the output has
+ * exactly the distribution of sampling without speculation.
+ *
+ * Per row r (r < L) the target distribution is p_r = softmax(x_r * inv_temp).
+ * With the proposal q = point mass on the draft c = blk[r + 1]:
+ *   the draft is accepted with probability min(1, p_r(c) / q(c)) = p_r(c),
+ *   i.e. iff u_acc[r] < p_r(c);
+ *   at the first rejection the emitted token is a sample of the residual
+ *   max(p_r - q, 0), normalised: p_r with c removed, drawn with u_smp[r];
+ *   if all L - 1 drafts are accepted, the bonus token is a sample of p_{L-1}
+ *   drawn with u_smp[L - 1].
+ * A draft outside [0, V) (the sentinel: no proposal) has p_r(c) = 0: it is
+ * rejected, and the residual is p_r itself.
+ * A sample of weights w_0..w_{V-1} with the uniform u is the smallest v whose
+ * running sum w_0 + .. + w_v exceeds u * (w_0 + .. + w_{V-1}); if rounding
+ * leaves none, the last v of nonzero weight.
+ * Everything is computed in double from the logits as given (float32, or
+ * bf16 widened exactly); the logits are finite.
+ */
+
+/* Row r of the logits as doubles. */
+static void or_row_values(const void* row, int32_t dtype, int64_t V, double* y)
+{
+    for (int64_t v = 0; v < V; ++v)
+        y[v] = dtype == 0 ? (double)or_bf16_value(((const uint16_t*)row)[v]) : (double)((const float*)row)[v];
+}
+
+/* Unnormalised softmax weights e_v = exp(x_v * inv_temp - max) and their sum. */
+static double or_softmax_weights(const void* row, int32_t dtype, int64_t V, double inv_temp, double* e)
+{
+    or_row_values(row, dtype, V, e);
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        e[v] *= inv_temp;
+        if (e[v] > m) m = e[v];
+    }
+    double z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        e[v] = exp(e[v] - m);
+        z += e[v];
+    }
+    return z;
+}
+
+/* Inverse-CDF sample of the weights e with token `excl` removed (excl outside
+ * [0, V): nothing removed). */
+int32_t or_sample_weights(const double* e, int64_t V, int32_t excl, double u)
+{
+    double total = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        if (v != excl) total += e[v];
+    const double target = u * total;
+    double run = 0.0;
+    int64_t last = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        if (v == excl) continue;
+        run += e[v];
+        if (e[v] > 0.0) last = v;
+        if (run > target) return (int32_t)v;
+    }
+    return (int32_t)last;
+}
+
+/* One request: rows[r * row_stride ..] for r < L, block blk[16], uniforms
+ * u[2 * r] (acceptance) and u[2 * r + 1] (sample).  Writes out_tok[16]
+ * (emitted tokens, then OR_SENT) and returns the number of accepted drafts;
+ * L outside 1..16 gives -1 and no tokens. */
+int32_t or_sample_verify(const void* rows, int32_t dtype, int64_t row_stride, int64_t V, const int32_t* blk,
+                         int32_t L, float inv_temp, const float* u, int32_t* out_tok)
+{
+    for (int i = 0; i < OR_BLOCK; ++i) out_tok[i] = OR_SENT;
+    if (L < 1 || L > OR_BLOCK) return -1;
+    const size_t esz = dtype == 0 ? sizeof(uint16_t) : sizeof(float);
+    double* e = (double*)malloc((size_t)V * sizeof(double));
+    if (e == NULL) return -1;
+    int32_t a = 0;
+    int32_t tok = OR_SENT;
+    for (int32_t r = 0; r < L; ++r) {
+        const void* row = (const char*)rows + (size_t)r * (size_t)row_stride * esz;
+        const double z = or_softmax_weights(row, dtype, V, (double)inv_temp, e);
+        if (r == L - 1) {
+            tok = or_sample_weights(e, V, -1, (double)u[2 * r + 1]);
+            break;
+        }
+        const int32_t c = blk[r + 1];
+        const double pc = (c >= 0 && c < V) ? e[c] / z : 0.0;
+        if ((double)u[2 * r] < pc) {
+            out_tok[r] = c;
+            a += 1;
+            continue;
+        }
+        tok = or_sample_weights(e, V, c, (double)u[2 * r + 1]);
+        break;
+    }
+    out_tok[a] = tok;
+    free(e);
     return a;
 }
 
