@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libclk.so")
-SOURCES = ["clk_api.cu", "clk_lookup.cu", "clk_verify.cu"]
+SOURCES = ["clk_api.cu", "clk_lookup.cu", "clk_verify.cu", "clk_sample.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVFLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
            f"-I{INCLUDE}", f"-I{CSRC}"]

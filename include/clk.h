@@ -312,6 +312,49 @@ CLK_API int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void*
                               const int32_t* d_len, const int32_t* d_len_hint, int32_t* d_argmax,
                               int32_t* d_accept, int32_t* d_emitted, int32_t* d_out_tok, clk_stream_t s);
 
+/* Sampling verification with point-mass drafts (HyperQwen context-lookup
+ * article, closing paragraph of "lookup 草稿的原理：三步走": for sampled
+ * requests every drafted position is a point mass on its proposed token,
+ * a proposal the standard speculative rejection sampler accepts, so the
+ * emitted tokens follow plain sampling from the target).
+ *
+ * For request b, row r < L_b of the logits gives the target distribution
+ * p_r = softmax(x_r * inv_temp[b]).  The draft c = block[b][r + 1] is
+ * accepted iff u[b][r][0] < p_r(c).  At the first rejected row the emitted
+ * token is drawn from p_r with c removed (renormalised) using u[b][r][1]; if
+ * all L_b - 1 drafts are accepted, the bonus token is drawn from p_{L_b - 1}
+ * using u[b][L_b - 1][1].  A draw with uniform u is the first token whose
+ * running probability sum exceeds u.  A draft outside [0, V) (CLK_SENT) is
+ * rejected and its row's whole distribution is drawn from.
+ *
+ * Layouts are those of clk_verify_greedy: logits [B, rows >= L_b, V] with
+ * element strides, block [B, 16], len [B].  inv_temp: float32 [B], 1 /
+ * temperature, > 0 and finite.  uniform: float32 [B, 16, 2] in [0, 1), the
+ * acceptance and the draw uniform of every row (the caller's random
+ * numbers; rows past L_b are not read).  Outputs: d_accept [B] (accepted
+ * drafts a), d_emitted [B] (a + 1), d_out_tok [B, 16] (the a accepted drafts,
+ * the drawn token, then CLK_SENT).  A request with L_b outside 1..16 or an
+ * invalid inv_temp gets accept 0, emitted 0 and all CLK_SENT.  Logits must
+ * be finite (-inf entries have weight 0).
+ *
+ * Computation is in float32; the results do not depend on the launch
+ * configuration or on timing.  Only the L_b rows are read, once, plus one
+ * 16,384-element segment of the drawn row.
+ *
+ * Scratch: a caller-owned device buffer of at least
+ * clk_verify_sample_scratch_bytes(dtype, V, B) bytes, 16-byte aligned,
+ * zeroed once before its first use (e.g. clk_verify_scratch_init); every
+ * call leaves it ready for the next.  Calls sharing a scratch buffer must
+ * not overlap on the GPU.  Errors: CLK_EINVAL for a bad dtype, size,
+ * stride, pointer or scratch size (nothing is launched); CLK_ECUDA for a
+ * launch failure. */
+CLK_API int clk_verify_sample_scratch_bytes(int32_t dtype, int32_t V, int32_t B, size_t* bytes);
+CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                              int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                              const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                              int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                              clk_stream_t s);
+
 /* ---------------------------------------------------------------------- */
 /* Status, counters, inspection (these synchronise the stream)             */
 /* ---------------------------------------------------------------------- */
