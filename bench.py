@@ -430,6 +430,79 @@ def run_sweep(args, world, rank, local, dist):
             "config": r["config"], "sweep": rows, "clocks": r.get("clocks")}
 
 
+def run_sample_verify(args, world, rank, local, dist):
+    """Sampling verification (clk_verify_sample) on the workload's shapes:
+    each launch reads its own pre-generated logits (larger than L2) at
+    temperature 0.3, with drafts that follow the synthetic target's favoured
+    token except for 20 % random ones; long blocks for the copy-heavy
+    requests, short ones for the chat-like.  CUDA events around every launch."""
+    import numpy as np
+    import torch
+
+    import context_lookup_speculative_gb300 as clk
+    import workload as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    clk.lib()
+    w = wl.make(args.config, seed=shard_seed(int(wl.DEFAULT_SEED[args.config]), rank))
+    B, V = w.B, w.V
+    gen = wl.DevGen(w, device=device)
+    per = B * 16 * V * (2 if w.dtype == wl.BF16 else 4)
+    K = max(1, min(args.steps, int(args.input_gb * 2 ** 30 // per)))
+    W = args.warmup
+    g = torch.Generator(device=device).manual_seed(1234 + rank)
+    bufs = torch.empty((K, B, 16, V), dtype=gen.torch_dtype(), device=device)
+    blks = torch.empty((K, B, 16), dtype=torch.int32, device=device)
+    for i in range(K):
+        gen.logits(bufs[i], pos=gen.pos + 16 * i)
+        fav = bufs[i].float().argmax(dim=2).int()
+        noise = torch.rand((B, 16), generator=g, device=device) < 0.2
+        rnd = torch.randint(0, V, (B, 16), generator=g, device=device, dtype=torch.int32)
+        blks[i, :, 0] = 0
+        blks[i, :, 1:] = torch.where(noise[:, 1:], rnd[:, 1:], fav[:, :15])
+    long = torch.tensor([k == "copy" for k in w.kinds], device=device)
+    L = torch.where(long, 16, 8).int()
+    t = torch.full((B,), 1.0 / 0.3, device=device)
+    u = torch.rand((K, B, 16, 2), generator=g, device=device)
+    acc = torch.zeros(B, dtype=torch.int32, device=device)
+    em, out = torch.zeros_like(acc), torch.zeros((B, 16), dtype=torch.int32, device=device)
+    scratch = clk.verify_sample_scratch(bufs.dtype, V, B, device=device)
+    flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    for i in range(W):
+        clk.verify_sample(bufs[i % K], blks[i % K], L, t, u[i % K], acc, em, out, scratch)
+    flush.zero_()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    emitted = torch.zeros(B, dtype=torch.int64, device=device)
+    clocks = ClockSampler(local)
+    for i in range(K):
+        ev[2 * i].record(stream)
+        clk.verify_sample(bufs[i], blks[i], L, t, u[i], acc, em, out, scratch)
+        ev[2 * i + 1].record(stream)
+        emitted += em
+    torch.cuda.synchronize()
+    clocks.stop()
+    us = [ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(K)]
+    mean_us = float(np.mean(us))
+    esz = 2 if w.dtype == wl.BF16 else 4
+    rows = int(L.sum().item())
+    alg = rows * V * esz + B * min(V, 16384) * esz  # the verified rows, plus the drawn row's segment
+    peak, peak_kind = _peaks()
+    return {"metric": "sampled verify launches/s (point-mass drafts)", "value": round(1e6 / mean_us, 2),
+            "unit": "launches/s", "n_gpus": world, "steps": K, "warmup": W, "us_per_launch": round(mean_us, 3),
+            "higher_is_better": True, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}", "batch": B, "vocab": V,
+                       "temperature": 0.3, "block": "16 for copy-heavy requests, 8 for chat-like",
+                       "l2": "every launch reads its own pre-generated logits (larger than L2)"},
+            "roofline": {"bound": "hbm", "kernel": "k_sample (verify_sample)", "achieved": round(alg / mean_us / 1e3, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(alg / mean_us / 1e3 / peak, 4),
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
+            "exp_per_launch": rows * V, "tokens_per_request_launch": round(emitted.sum().item() / (B * K), 4),
+            "clocks": clocks.summary(), "gpu_launches": K}
+
+
 def _kind_metrics(after, before, kinds, head):
     """Hit rate, mean accepted length, tail share of the accepted drafts and
     accepted-length histograms over the timed steps, per workload kind."""
@@ -598,6 +671,8 @@ def main(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sample-verify", action="store_true",
+                    help="time the sampling verification (point-mass drafts) on --config's shapes, one JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="block-size and sticky variants of the measured step on --config, one JSON line")
     ap.add_argument("--ablation", action="store_true",
@@ -614,7 +689,12 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group(backend="nccl")
     try:
-        out = run_sweep(args, world, rank, local, dist) if args.sweep else run_ours(args, world, rank, local, dist)
+        if args.sample_verify:
+            out = run_sample_verify(args, world, rank, local, dist)
+        elif args.sweep:
+            out = run_sweep(args, world, rank, local, dist)
+        else:
+            out = run_ours(args, world, rank, local, dist)
         if rank == 0:
             print(json.dumps(out), flush=True)
     finally:

@@ -14,9 +14,11 @@
 //
 // The work is HBM-bound: every verified row is read once.  Each row is cut
 // into segments of kSegElems elements; the grid takes an even share of the
-// flat list of (request, row, segment) triples.  Each thread keeps a running
-// maximum m and sum s = sum exp(x t - m) over its strided vectors of a
-// segment; each warp combines its 32 threads' pairs with shuffles in a fixed
+// flat list of (request, row, segment) triples.  Each thread keeps, in base
+// 2, a running maximum m of z = x * t * log2(e) and the sum s = sum 2^(z - m)
+// over its strided vectors of a segment (one fused multiply-add and one
+// hardware exp2 per element: the PTX ex2.approx.ftz.f32 instruction, whose
+// relative error the PTX ISA bounds by 2^-22); each warp combines its 32 threads' pairs with shuffles in a fixed
 // order and stores one (m, s) pair per segment and warp in the scratch, so no
 // barrier is needed per segment.  When a CTA leaves a request it adds the
 // number of that request's segments it finished to the request's counter;
@@ -31,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "clk.h"
 #include "clk_device.cuh"
@@ -39,6 +42,9 @@
 namespace clk {
 namespace {
 
+#ifndef CLK_SAMPLE_CTAS
+#define CLK_SAMPLE_CTAS 4  // resident CTAs per SM the kernel is compiled for
+#endif
 constexpr int kSThreads = 256;
 constexpr int kSWarpsPerCta = kSThreads / 32;
 constexpr int kSUnroll = 4;
@@ -79,6 +85,18 @@ struct SElem<CLK_DTYPE_BF16> {
     using T = uint16_t;
     static constexpr int W = 8;  // elements per 16-byte vector
     __device__ static float value(T x) { return __uint_as_float((uint32_t)x << 16); }
+    // maximum of the 8 values by packed bf16x2 maxima
+    __device__ static float vmax(const uint4& v)
+    {
+        const __nv_bfloat162 m = __hmax2(__hmax2(as2(v.x), as2(v.y)), __hmax2(as2(v.z), as2(v.w)));
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+    __device__ static __nv_bfloat162 as2(uint32_t w)
+    {
+        __nv_bfloat162 r;
+        memcpy(&r, &w, 4);
+        return r;
+    }
     __device__ static void unpack(const uint4& v, float* f)
     {
         f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
@@ -92,6 +110,10 @@ struct SElem<CLK_DTYPE_F32> {
     using T = float;
     static constexpr int W = 4;
     __device__ static float value(T x) { return x; }
+    __device__ static float vmax(const uint4& v)
+    {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
     __device__ static void unpack(const uint4& v, float* f)
     {
         f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
@@ -99,7 +121,18 @@ struct SElem<CLK_DTYPE_F32> {
     }
 };
 
-// Running (max, sum of exp(y - max)) of a set of values y.
+// 2^x by the hardware's base-2 exponential (flushes results below 2^-126
+// to zero: weights that small against the maximum do not count).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Running (max, sum of 2^(z - max)) of a set of values z (base 2).
 struct MS {
     float m;
     float s;
@@ -113,29 +146,54 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b)
     if (b.s == 0.0f) return a;
     if (a.s == 0.0f) return b;
     const float m = fmaxf(a.m, b.m);
-    return MS{m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
+    return MS{m, a.s * ex2(a.m - m) + b.s * ex2(b.m - m)};
 }
 
-// Adds W values y_i = x_i * t.
-template <int W>
-__device__ __forceinline__ void ms_add(MS& r, const float* x, float t)
+// Two floats in one 64-bit register pair, for the packed f32x2 arithmetic
+// (fma.rn.f32x2, add.rn.f32x2: two independent float operations each,
+// rounded as the scalar ones).
+__device__ __forceinline__ unsigned long long pk(float lo, float hi)
 {
-    float y[W];
-    float vm = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-        y[i] = x[i] * t;
-        vm = fmaxf(vm, y[i]);
-    }
+    return ((unsigned long long)__float_as_uint(hi) << 32) | (unsigned long long)__float_as_uint(lo);
+}
+__device__ __forceinline__ float pk_lo(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float pk_hi(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ unsigned long long fma2(unsigned long long x, unsigned long long y, unsigned long long z)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+    return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long x, unsigned long long y)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return r;
+}
+
+// Adds the W values z_i = x_i * c of one vector (c = t log2 e > 0, so the
+// largest x gives the largest z).  The weights 2^(z_i - m) are summed in
+// pairs, then the two halves.
+template <int DT>
+__device__ __forceinline__ void ms_add_vec(MS& r, const uint4& v, float c)
+{
+    using E = SElem<DT>;
+    const float vm = E::vmax(v) * c;
     if (vm > r.m) {
-        r.s = r.s == 0.0f ? 0.0f : r.s * __expf(r.m - vm);
+        r.s = r.s == 0.0f ? 0.0f : r.s * ex2(r.m - vm);
         r.m = vm;
     }
     if (r.m == -INFINITY) return;  // every value so far is -inf: weight 0
-    float acc = 0.0f;
+    float f[E::W];
+    E::unpack(v, f);
+    const unsigned long long c2 = pk(c, c), nm2 = pk(-r.m, -r.m);
+    unsigned long long acc = 0ull;  // (+0, +0)
 #pragma unroll
-    for (int i = 0; i < W; ++i) acc += __expf(y[i] - r.m);
-    r.s += acc;
+    for (int i = 0; i < E::W; i += 2) {
+        const unsigned long long z = fma2(pk(f[i], f[i + 1]), c2, nm2);
+        acc = add2(acc, pk(ex2(pk_lo(z)), ex2(pk_hi(z))));
+    }
+    r.s += pk_lo(acc) + pk_hi(acc);
 }
 
 // Warp-wide merge in a fixed (butterfly) order; every lane gets the result.
@@ -152,15 +210,15 @@ __device__ __forceinline__ MS ms_warp(MS r)
     return r;
 }
 
-// Adds one value y = x * t.
-__device__ __forceinline__ void ms_add1(MS& r, float x, float t)
+// Adds one value z = x * c.
+__device__ __forceinline__ void ms_add1(MS& r, float x, float c)
 {
-    const float y = x * t;
-    if (y > r.m) {
-        r.s = r.s == 0.0f ? 0.0f : r.s * __expf(r.m - y);
-        r.m = y;
+    const float z = x * c;
+    if (z > r.m) {
+        r.s = r.s == 0.0f ? 0.0f : r.s * ex2(r.m - z);
+        r.m = z;
     }
-    if (r.m != -INFINITY) r.s += __expf(y - r.m);
+    if (r.m != -INFINITY) r.s += ex2(fmaf(x, c, -r.m));
 }
 
 // P[b] = rows of requests b' < b; P[B] = total.  Block-wide.
@@ -236,77 +294,85 @@ __device__ __forceinline__ void seg_range(const SampleArgs& a, const int32_t* P,
 // Streams segments [k0, k1) of request b and stores one (m, s) pair per
 // segment and warp.  Vector path: two groups of kSUnroll 16-byte loads per
 // thread alternate, and the next segment's first group is issued before the
-// current segment's last group is reduced.
+// current segment's last group is reduced.  The segment and row advance
+// incrementally (segments of a request are consecutive: row-major).
 template <int DT>
 __device__ __forceinline__ void stream_vec(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k0, int64_t k1)
 {
     using E = SElem<DT>;
-    constexpr int W = E::W;
-    constexpr int32_t G = kSUnroll * kSThreads;  // vectors per group
+    constexpr int32_t SV = (int32_t)(kSegElems / E::W);  // vectors per full segment
+    constexpr int32_t G = kSUnroll * kSThreads;          // vectors per group
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float t = a.inv_temp[b];
-    const char* rowp;
-    int32_t u0, u1, r, sg;
-    seg_range<DT, true>(a, P, b, k0, rowp, u0, u1, r, sg);
-    const uint4* row = reinterpret_cast<const uint4*>(rowp);
-    int32_t gb = u0 + tid;
-    int64_t k = k0;
+    const float c = a.inv_temp[b] * kLog2e;
+    const int32_t vpr = a.V / E::W;
+    const int64_t rsv = a.row_stride / E::W;  // row stride in vectors
+    const uint4* req = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
+                                                     (int64_t)b * a.req_stride * (int64_t)sizeof(typename E::T));
+    const int64_t ri0 = k0 / a.S;
+    int32_t r = (int32_t)(ri0 - P[b]);
+    int32_t sg = (int32_t)(k0 - ri0 * a.S);
+    int32_t left = (int32_t)(k1 - k0);  // segments still to finish, the current one included
+    // current group: row `row`, vectors [g, g + G) of segment sg (which ends at e)
+    const uint4* row = req + (int64_t)r * rsv;
+    int32_t g = sg * SV;
+    int32_t e = min(g + SV, vpr);
     MS run = ms_empty();
     uint4 X[kSUnroll], Y[kSUnroll];
-    auto load = [&](const uint4* rw, int32_t base, int32_t end, uint4* d) {
-#pragma unroll
-        for (int u = 0; u < kSUnroll; ++u) {
-            const int32_t vi = base + u * kSThreads;
-            if (vi < end) d[u] = __ldcs(rw + vi);
-        }
-    };
-    auto reduce = [&](const uint4* d, int32_t base, int32_t end) {
-#pragma unroll
-        for (int u = 0; u < kSUnroll; ++u) {
-            const int32_t vi = base + u * kSThreads;
-            if (vi < end) {
-                float f[W];
-                E::unpack(d[u], f);
-                ms_add<W>(run, f, t);
-            }
-        }
-    };
-    // One half-step: the group in C is current; the next group goes into N.
-    auto half = [&](uint4* C, uint4* N) -> bool {
+#define CLK_LOAD_GROUP(D, RW, G0, E0)                                                  \
+    if ((G0) + G <= (E0)) {                                                            \
+        _Pragma("unroll") for (int u = 0; u < kSUnroll; ++u) D[u] = __ldcs((RW) + (G0) + tid + u * kSThreads); \
+    } else {                                                                           \
+        _Pragma("unroll") for (int u = 0; u < kSUnroll; ++u) {                         \
+            const int32_t vi = (G0) + tid + u * kSThreads;                             \
+            if (vi < (E0)) D[u] = __ldcs((RW) + vi);                                   \
+        }                                                                              \
+    }
+#define CLK_REDUCE_GROUP(D, G0, E0)                                                    \
+    if ((G0) + G <= (E0)) {                                                            \
+        _Pragma("unroll") for (int u = 0; u < kSUnroll; ++u) ms_add_vec<DT>(run, D[u], c); \
+    } else {                                                                           \
+        _Pragma("unroll") for (int u = 0; u < kSUnroll; ++u)                           \
+            if ((G0) + tid + u * kSThreads < (E0)) ms_add_vec<DT>(run, D[u], c);       \
+    }
+    CLK_LOAD_GROUP(X, row, g, e)
+    for (int half = 0;; half ^= 1) {
+        // the next group: later in this segment, or the first of the next
         const uint4* nrow = row;
-        int32_t nu1 = u1, ngb = gb + G, nr = r, nsg = sg;
-        bool more = true, seg_end = false;
-        if (gb - tid + G >= u1) {
-            seg_end = true;
-            if (k + 1 < k1) {
-                int32_t nu0;
-                seg_range<DT, true>(a, P, b, k + 1, rowp, nu0, nu1, nr, nsg);
-                nrow = reinterpret_cast<const uint4*>(rowp);
-                ngb = nu0 + tid;
-            } else {
-                more = false;
+        int32_t ng = g + G, ne = e, nr = r, nsg = sg;
+        const bool seg_end = ng >= e;
+        const bool more = !seg_end || left > 1;
+        if (seg_end && more) {
+            nsg = sg + 1;
+            if (nsg == a.S) {
+                nsg = 0;
+                nr = r + 1;
+                nrow = req + (int64_t)nr * rsv;
             }
+            ng = nsg * SV;
+            ne = min(ng + SV, vpr);
         }
-        if (more) load(nrow, ngb, nu1, N);
-        reduce(C, gb, u1);
+        if (half == 0) {
+            if (more) { CLK_LOAD_GROUP(Y, nrow, ng, ne) }
+            CLK_REDUCE_GROUP(X, g, e)
+        } else {
+            if (more) { CLK_LOAD_GROUP(X, nrow, ng, ne) }
+            CLK_REDUCE_GROUP(Y, g, e)
+        }
         if (seg_end) {
             const MS w = ms_warp(run);
             if (lane == 0) part_of(a, b, r, sg)[warp] = make_float2(w.m, w.s);
             run = ms_empty();
-            ++k;
+            --left;
         }
+        if (!more) break;
         row = nrow;
-        u1 = nu1;
-        gb = ngb;
+        g = ng;
+        e = ne;
         r = nr;
         sg = nsg;
-        return more;
-    };
-    load(row, gb, u1, X);
-    for (;;) {
-        if (!half(X, Y)) break;
-        if (!half(Y, X)) break;
     }
+#undef CLK_LOAD_GROUP
+#undef CLK_REDUCE_GROUP
 }
 
 // Scalar path (rows not 16-byte aligned): one segment at a time.
@@ -316,14 +382,14 @@ __device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t
 {
     using E = SElem<DT>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float t = a.inv_temp[b];
+    const float c = a.inv_temp[b] * kLog2e;
     for (int64_t k = k0; k < k1; ++k) {
         const char* rowp;
         int32_t u0, u1, r, sg;
         seg_range<DT, false>(a, P, b, k, rowp, u0, u1, r, sg);
         const typename E::T* row = reinterpret_cast<const typename E::T*>(rowp);
         MS run = ms_empty();
-        for (int32_t i = u0 + tid; i < u1; i += kSThreads) ms_add1(run, E::value(row[i]), t);
+        for (int32_t i = u0 + tid; i < u1; i += kSThreads) ms_add1(run, E::value(row[i]), c);
         const MS w = ms_warp(run);
         if (lane == 0) part_of(a, b, r, sg)[warp] = make_float2(w.m, w.s);
     }
@@ -333,20 +399,20 @@ struct FinSmem {
     float m[kBlock], s[kBlock];  // each row's combined pair
     float ex;                    // weight exp(x_c t - m) of the removed draft
     float tgt;                   // the sample's target inside the chosen segment
-    int32_t a, excl, seg, tok;
+    int32_t a, excl, seg, tok, cross;
     float wsum[kSWarpsPerCta];
 };
 
 // Request b is complete (all of its segments' pairs are stored): decide the
 // drafts, draw the token, write the outputs, rewind the counter.  Block-wide.
 template <int DT>
-__device__ __forceinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSmem& fs)
+__device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSmem& fs)
 {
     using E = SElem<DT>;
     const unsigned full = 0xFFFFFFFFu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t L = a.len[b], S = a.S, V = a.V;
-    const float t = a.inv_temp[b];
+    const float cz = a.inv_temp[b] * kLog2e;  // z = x * cz, weights 2^(z - m)
     const typename E::T* base = static_cast<const typename E::T*>(a.logits) + (int64_t)b * a.req_stride;
     __threadfence();
     // Each row's pair: the segments' pairs in index order, then the butterfly.
@@ -370,7 +436,7 @@ __device__ __forceinline__ void sample_finish(const SampleArgs& a, int32_t b, Fi
         const int32_t c = has ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
         const bool inv = c >= 0 && c < V;
         float ec = 0.0f;
-        if (has && inv) ec = __expf(E::value(base[(int64_t)lane * a.row_stride + c]) * t - fs.m[lane]);
+        if (has && inv) ec = ex2(fmaf(E::value(base[(int64_t)lane * a.row_stride + c]), cz, -fs.m[lane]));
         const float p = has ? ec / fs.s[lane] : 0.0f;
         const float ua = has ? a.uniform[((int64_t)b * kBlock + lane) * 2] : 1.0f;
         const unsigned rej = __ballot_sync(full, has && !(ua < p));
@@ -400,7 +466,7 @@ __device__ __forceinline__ void sample_finish(const SampleArgs& a, int32_t b, Fi
             if (k < S) {
                 for (int i = 0; i < kSWarpsPerCta; ++i) {
                     const float2 q = __ldcg(pp + (int64_t)k * kSWarpsPerCta + i);
-                    if (q.y > 0.0f) w += q.y * __expf(q.x - mra);
+                    if (q.y > 0.0f) w += q.y * ex2(q.x - mra);
                 }
                 if (k == exseg) w = fmaxf(0.0f, w - fs.ex);
             }
@@ -426,53 +492,76 @@ __device__ __forceinline__ void sample_finish(const SampleArgs& a, int32_t b, Fi
         }
     }
     __syncthreads();
-    // Inside the segment: each thread a contiguous run of the segment's
-    // elements; block-wide exclusive scan of the runs' sums; the first thread
-    // whose run crosses the target walks its run.
-    constexpr int32_t kRun = (int32_t)(kSegElems / kSThreads);
+    // Inside the segment, in chunks of kChunk elements: each thread weighs a
+    // contiguous run of kRun elements (its loads issued together), a
+    // block-wide exclusive scan of the runs' sums places the target, and the
+    // thread whose run crosses it walks its weights.
+    constexpr int32_t kRun = 16;
+    constexpr int32_t kChunk = kRun * kSThreads;
     const int32_t sg = fs.seg;
     const typename E::T* row = base + (int64_t)ra * a.row_stride;
-    const int64_t v0 = sg < 0 ? 0 : (int64_t)sg * kSegElems + (int64_t)tid * kRun;
-    const int64_t v1 = sg < 0 ? 0 : min(v0 + kRun, min((int64_t)(sg + 1) * kSegElems, (int64_t)V));
-    float own = 0.0f;
-    int64_t lastv = -1;
-    for (int64_t v = v0; v < v1; ++v) {
-        if (v == excl) continue;
-        const float e = __expf(E::value(row[v]) * t - mra);
-        own += e;
-        if (e > 0.0f) lastv = v;
-    }
-    float incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(full, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) fs.wsum[warp] = incl;
+    const int64_t s0 = sg < 0 ? 0 : (int64_t)sg * kSegElems;
+    const int64_t s1 = sg < 0 ? 0 : min(s0 + kSegElems, (int64_t)V);
+    float tgt = fs.tgt;
+    int64_t lastv = -1;  // this thread's last element of positive weight
     if (tid == 0) fs.tok = CLK_SENT;
-    __syncthreads();
-    float pre = incl - own;
-    for (int w = 0; w < warp; ++w) pre += fs.wsum[w];
-    const float tgt = fs.tgt;
-    const bool crosses = own > 0.0f && pre + own > tgt && !(pre > tgt);
-    if (crosses) {
-        float run = pre;
-        int64_t tok = lastv;
-        for (int64_t v = v0; v < v1; ++v) {
-            if (v == excl) continue;
-            run += __expf(E::value(row[v]) * t - mra);
-            if (run > tgt) {
-                tok = v;
-                break;
-            }
+    for (int64_t c0 = s0; c0 < s1; c0 += kChunk) {
+        const int64_t v0 = c0 + (int64_t)tid * kRun;
+        float wv[kRun];
+        float own = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRun; ++i) {
+            const int64_t v = v0 + i;
+            const bool in = v < s1 && v != excl;
+            const float x = v < s1 ? E::value(row[v]) : 0.0f;
+            wv[i] = in ? ex2(fmaf(x, cz, -mra)) : 0.0f;
+            own += wv[i];
+            if (wv[i] > 0.0f) lastv = v;
         }
-        fs.tok = (int32_t)tok;  // exactly one thread crosses
+        float incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncthreads();  // the previous chunk's sums have been read
+        if (lane == 31) fs.wsum[warp] = incl;
+        if (tid == 0) fs.cross = -1;
+        __syncthreads();
+        float pre = incl - own, tot = 0.0f;
+        for (int w = 0; w < kSWarpsPerCta; ++w) {
+            if (w < warp) pre += fs.wsum[w];
+            tot += fs.wsum[w];
+        }
+        if (tgt < tot) {  // the same decision in every thread
+            // the crossing run: the last one of positive weight that starts
+            // at or before the target (one exists: the first positive run
+            // starts at 0 <= target)
+            if (own > 0.0f && pre <= tgt) atomicMax(&fs.cross, tid);
+            __syncthreads();
+            if (tid == fs.cross) {
+                float run = pre;
+                int64_t tok = lastv;
+#pragma unroll
+                for (int i = 0; i < kRun; ++i) {
+                    run += wv[i];
+                    if (wv[i] > 0.0f && run > tgt) {
+                        tok = v0 + i;
+                        break;
+                    }
+                }
+                fs.tok = (int32_t)tok;
+            }
+            break;
+        }
+        tgt -= tot;
     }
     __syncthreads();
     if (fs.tok == CLK_SENT) {
         // no crossing (rounding, or the target past the segment): the
         // segment's last element of positive weight
         const unsigned has = __ballot_sync(full, lastv >= 0);
+        __syncthreads();
         if (has && lane == 31 - __clz(has)) fs.wsum[warp] = __int_as_float((int32_t)lastv);
         else if (lane == 0 && !has) fs.wsum[warp] = __int_as_float(-1);
         __syncthreads();
@@ -501,7 +590,7 @@ __device__ __forceinline__ void sample_finish(const SampleArgs& a, int32_t b, Fi
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSThreads, 4) k_sample(SampleArgs a)
+__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArgs a)
 {
     extern __shared__ int32_t P[];  // B + 1
     __shared__ int32_t sm_warp[kSWarpsPerCta];
