@@ -154,10 +154,22 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b)
 // rounded as the scalar ones).
 __device__ __forceinline__ unsigned long long pk(float lo, float hi)
 {
-    return ((unsigned long long)__float_as_uint(hi) << 32) | (unsigned long long)__float_as_uint(lo);
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
-__device__ __forceinline__ float pk_lo(unsigned long long v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float pk_hi(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ float pk_lo(unsigned long long v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float pk_hi(unsigned long long v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
 __device__ __forceinline__ unsigned long long fma2(unsigned long long x, unsigned long long y, unsigned long long z)
 {
     unsigned long long r;
@@ -171,29 +183,48 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long x, unsigne
     return r;
 }
 
-// Adds the W values z_i = x_i * c of one vector (c = t log2 e > 0, so the
-// largest x gives the largest z).  The weights 2^(z_i - m) are summed in
-// pairs, then the two halves.
+// Sum of the W weights 2^(x_i c - m) of one vector, in pairs, then the two
+// halves.
+template <int DT>
+__device__ __forceinline__ float vec_weights(const float* f, float c, float m)
+{
+    const unsigned long long c2 = pk(c, c), nm2 = pk(-m, -m);
+    unsigned long long acc = 0ull;  // (+0, +0)
+#pragma unroll
+    for (int i = 0; i < SElem<DT>::W; i += 2) {
+        const unsigned long long z = fma2(pk(f[i], f[i + 1]), c2, nm2);
+        acc = add2(acc, pk(ex2(pk_lo(z)), ex2(pk_hi(z))));
+    }
+    return pk_lo(acc) + pk_hi(acc);
+}
+
+// Weights above this (relative to the running maximum) trigger a rescale;
+// below it the sum cannot overflow (float reaches 2^128).
+constexpr float kRescaleAt = 18446744073709551616.0f;  // 2^64
+
+// Adds the W values z_i = x_i * c of one vector (c = t log2 e > 0).  The
+// running maximum is raised lazily: the weights are taken against the
+// current m, and only a vector whose weights sum past 2^64 (or to inf or
+// NaN: the first vector, where m is still -inf) raises m to its own maximum
+// and is weighed again.  The pair still means s = sum 2^(z - m) exactly as
+// before; m need not be the largest z, only within 64 of it.
 template <int DT>
 __device__ __forceinline__ void ms_add_vec(MS& r, const uint4& v, float c)
 {
     using E = SElem<DT>;
-    const float vm = E::vmax(v) * c;
-    if (vm > r.m) {
-        r.s = r.s == 0.0f ? 0.0f : r.s * ex2(r.m - vm);
-        r.m = vm;
-    }
-    if (r.m == -INFINITY) return;  // every value so far is -inf: weight 0
     float f[E::W];
     E::unpack(v, f);
-    const unsigned long long c2 = pk(c, c), nm2 = pk(-r.m, -r.m);
-    unsigned long long acc = 0ull;  // (+0, +0)
-#pragma unroll
-    for (int i = 0; i < E::W; i += 2) {
-        const unsigned long long z = fma2(pk(f[i], f[i + 1]), c2, nm2);
-        acc = add2(acc, pk(ex2(pk_lo(z)), ex2(pk_hi(z))));
+    float acc = vec_weights<DT>(f, c, r.m);
+    if (!(acc <= kRescaleAt)) {
+        const float vm = E::vmax(v) * c;
+        if (vm > r.m) {
+            r.s = r.s == 0.0f ? 0.0f : r.s * ex2(r.m - vm);
+            r.m = vm;
+        }
+        if (r.m == -INFINITY) return;  // every value so far is -inf: weight 0
+        acc = vec_weights<DT>(f, c, r.m);
     }
-    r.s += pk_lo(acc) + pk_hi(acc);
+    r.s += acc;
 }
 
 // Warp-wide merge in a fixed (butterfly) order; every lane gets the result.
@@ -397,6 +428,7 @@ __device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t
 
 struct FinSmem {
     float m[kBlock], s[kBlock];  // each row's combined pair
+    float xc[kBlock];            // each row's draft logit
     float ex;                    // weight exp(x_c t - m) of the removed draft
     float tgt;                   // the sample's target inside the chosen segment
     int32_t a, excl, seg, tok, cross;
@@ -415,19 +447,38 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
     const float cz = a.inv_temp[b] * kLog2e;  // z = x * cz, weights 2^(z - m)
     const typename E::T* base = static_cast<const typename E::T*>(a.logits) + (int64_t)b * a.req_stride;
     __threadfence();
-    // Each row's pair: the segments' pairs in index order, then the butterfly.
-    for (int32_t r = warp; r < L; r += kSWarpsPerCta) {
-        const float2* pp = part_of(a, b, r, 0);
-        MS acc = ms_empty();
-        for (int32_t i = lane; i < S * kSWarpsPerCta; i += 32) {
-            const float2 q = __ldcg(pp + i);
-            acc = ms_merge(acc, MS{q.x, q.y});
+    // Each row's pair: 16 threads per row (row = tid / 16), each merging the
+    // row's segment pairs sub, sub + 16, ... in order, then a butterfly over
+    // the 16.  Warp 0 also loads every draft's logit in the same round trip.
+    {
+        const int32_t r = tid >> 4, sub = tid & 15;
+        float xc = 0.0f;
+        if (warp == 0 && lane < L - 1) {
+            const int32_t c = a.block[(int64_t)b * kBlock + lane + 1];
+            if (c >= 0 && c < V) xc = E::value(base[(int64_t)lane * a.row_stride + c]);
         }
-        acc = ms_warp(acc);
-        if (lane == 0) {
+        MS acc = ms_empty();
+        if (r < L) {
+            const float2* pp = part_of(a, b, r, 0);
+            const int32_t n = S * kSWarpsPerCta;
+#pragma unroll 8
+            for (int32_t i = sub; i < n; i += 16) {
+                const float2 q = __ldcg(pp + i);
+                acc = ms_merge(acc, MS{q.x, q.y});
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            MS q;
+            q.m = __shfl_xor_sync(full, acc.m, o);
+            q.s = __shfl_xor_sync(full, acc.s, o);
+            acc = (sub & o) ? ms_merge(q, acc) : ms_merge(acc, q);
+        }
+        if (sub == 0 && r < L) {
             fs.m[r] = acc.m;
             fs.s[r] = acc.s;
         }
+        if (warp == 0 && lane < kBlock) fs.xc[lane] = xc;
     }
     __syncthreads();
     // Acceptance of every draft at once (lane r: row r's draft blk[r + 1]).
@@ -436,7 +487,7 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
         const int32_t c = has ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
         const bool inv = c >= 0 && c < V;
         float ec = 0.0f;
-        if (has && inv) ec = ex2(fmaf(E::value(base[(int64_t)lane * a.row_stride + c]), cz, -fs.m[lane]));
+        if (has && inv) ec = ex2(fmaf(fs.xc[lane], cz, -fs.m[lane]));
         const float p = has ? ec / fs.s[lane] : 0.0f;
         const float ua = has ? a.uniform[((int64_t)b * kBlock + lane) * 2] : 1.0f;
         const unsigned rej = __ballot_sync(full, has && !(ua < p));
