@@ -158,17 +158,9 @@ __device__ __forceinline__ unsigned long long pk(float lo, float hi)
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
-__device__ __forceinline__ float pk_lo(unsigned long long v)
+__device__ __forceinline__ void pk_split(unsigned long long v, float& lo, float& hi)
 {
-    float lo, hi;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
-}
-__device__ __forceinline__ float pk_hi(unsigned long long v)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
 }
 __device__ __forceinline__ unsigned long long fma2(unsigned long long x, unsigned long long y, unsigned long long z)
 {
@@ -192,10 +184,13 @@ __device__ __forceinline__ float vec_weights(const float* f, float c, float m)
     unsigned long long acc = 0ull;  // (+0, +0)
 #pragma unroll
     for (int i = 0; i < SElem<DT>::W; i += 2) {
-        const unsigned long long z = fma2(pk(f[i], f[i + 1]), c2, nm2);
-        acc = add2(acc, pk(ex2(pk_lo(z)), ex2(pk_hi(z))));
+        float z0, z1;
+        pk_split(fma2(pk(f[i], f[i + 1]), c2, nm2), z0, z1);
+        acc = add2(acc, pk(ex2(z0), ex2(z1)));
     }
-    return pk_lo(acc) + pk_hi(acc);
+    float a0, a1;
+    pk_split(acc, a0, a1);
+    return a0 + a1;
 }
 
 // Weights above this (relative to the running maximum) trigger a rescale;

@@ -79,6 +79,7 @@ class RunArgs(ctypes.Structure):
     _fields_ = [("params", _P), ("n_req", ctypes.c_int32), ("req_ids", _P), ("prompt", _P), ("prompt_off", _P),
                 ("steps", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("gen_ctx", _P), ("logits_fn", _P), ("head_fn", _P),
+                ("uniform_fn", _P), ("inv_temp", ctypes.c_float), ("pad0", ctypes.c_int32),
                 ("rec_k", _P), ("rec_j", _P), ("rec_L", _P), ("rec_a", _P), ("rec_c", _P), ("rec_blk", _P),
                 ("rec_g", _P), ("hist_out", _P), ("hist_off", _P), ("hist_len", _P), ("counters", _P),
                 ("timed_from", ctypes.c_int32), ("pad", ctypes.c_int32),
@@ -226,14 +227,17 @@ class RunResult:
 
 def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         params: Optional[Params] = None, threads: Optional[int] = None, head=None,
-        timed_from: int = 0) -> RunResult:
+        timed_from: int = 0, inv_temp: float = 0.0) -> RunResult:
     """Run the oracle decode loop of workload `w` for the given requests.
 
     The target logits and head proposals come from the host generator of the
     `workload` package (keyed by the original request ids).  `head`, if
     given, replaces the head proposals: a Python callable (b, t, n) -> 7
     tokens (small tests only: it runs under the GIL).  `timed_from`: the
-    first step counted in method_s / provider_s (per-thread sums)."""
+    first step counted in method_s / provider_s (per-thread sums).
+    `inv_temp` > 0 verifies by sampling (point-mass drafts) at that inverse
+    temperature with the generator's uniforms; the records' `g` then holds
+    each step's emitted tokens instead of the argmax rows."""
     import workload as wl  # the seeded input generator shared by both sides
 
     p = params or Params.default()
@@ -266,6 +270,8 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     args.gen_ctx = gen.ctx_ptr
     args.logits_fn = gen.logits_fn
     args.head_fn = gen.head_fn
+    args.uniform_fn = gen.uniform_fn
+    args.inv_temp = float(inv_temp)
     if head is not None:
         proto = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                  ctypes.POINTER(ctypes.c_int32))

@@ -337,6 +337,8 @@ int32_t or_sample_verify(const void* rows, int32_t dtype, int64_t row_stride, in
 /* Input providers (the synthetic target and draft model). */
 typedef void (*or_logits_fn)(const void* ctx, int32_t b, int64_t P, void* out_row);
 typedef void (*or_head_fn)(const void* ctx, int32_t b, int32_t t, int64_t n, int32_t* out);
+/* The 16 x 2 sampling uniforms of step t of request b ([16][2]). */
+typedef void (*or_uniform_fn)(const void* ctx, int32_t b, int32_t t, float* out);
 
 typedef struct or_run_args {
     const or_params* params;
@@ -351,6 +353,9 @@ typedef struct or_run_args {
     const void* gen_ctx;
     or_logits_fn logits_fn;
     or_head_fn head_fn;
+    or_uniform_fn uniform_fn; /* sampling verification only */
+    float inv_temp;           /* > 0: sampling verification at this 1/temperature; 0: greedy */
+    int32_t pad0;
     /* outputs, indexed [t][i] or [t][i][16] with i the request's position */
     int32_t* rec_k;
     int32_t* rec_j;
@@ -393,7 +398,9 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
     const int64_t cap = a->hist_off[i + 1] - a->hist_off[i];
     const size_t esz = a->dtype == 0 ? 2 : 4;
     int32_t* h = a->hist_out + a->hist_off[i];
-    void* row = malloc((size_t)a->V * esz);
+    const int sampling = a->inv_temp > 0.0f;
+    /* greedy: one row at a time; sampling: the block's rows together */
+    void* row = malloc((size_t)a->V * esz * (sampling ? OR_BLOCK : 1));
     if (!row) return -1;
     if (n0 > cap || n0 < 1) {
         free(row);
@@ -425,13 +432,25 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
         prov += or_now_ns() - u0;
         or_fuse(h[n - 1], c, k, m, L, p, blk);
         for (int32_t r = 0; r < OR_BLOCK; ++r) g[r] = OR_SENT;
-        for (int32_t r = 0; r < L; ++r) {
+        int32_t acc;
+        if (sampling) {
+            /* g: the emitted tokens (accepted drafts, then the drawn token) */
+            float u[2 * OR_BLOCK];
             u0 = or_now_ns();
-            a->logits_fn(a->gen_ctx, b, n + r, row);
+            for (int32_t r = 0; r < L; ++r) a->logits_fn(a->gen_ctx, b, n + r, (char*)row + (size_t)r * a->V * esz);
+            a->uniform_fn(a->gen_ctx, b, t, u);
             prov += or_now_ns() - u0;
-            g[r] = a->dtype == 0 ? or_argmax_bf16((const uint16_t*)row, a->V) : or_argmax_f32((const float*)row, a->V);
+            acc = or_sample_verify(row, a->dtype, a->V, a->V, blk, L, a->inv_temp, u, g);
+        } else {
+            for (int32_t r = 0; r < L; ++r) {
+                u0 = or_now_ns();
+                a->logits_fn(a->gen_ctx, b, n + r, row);
+                prov += or_now_ns() - u0;
+                g[r] = a->dtype == 0 ? or_argmax_bf16((const uint16_t*)row, a->V)
+                                     : or_argmax_f32((const float*)row, a->V);
+            }
+            acc = or_accept(blk, g, L);
         }
-        int32_t acc = or_accept(blk, g, L);
         if (n + acc + 1 > cap) {
             rc = -2;
             break;

@@ -36,3 +36,16 @@ def test_advance_tracks_emitted():
     dev.advance(e)
     dev.advance(e)
     assert dev.pos.cpu().tolist() == [int(n) + 2 * int(x) for n, x in zip(w.n0, [1, 5, 16, 0])]
+
+
+def test_device_uniforms_equal_host_uniforms():
+    w = wl.make_small("mixed", seed=17, B=5, V=512, steps=8)
+    hg, dg = wl.HostGen(w), wl.DevGen(w, device="cuda")
+    out = torch.zeros((w.B, 16, 2), dtype=torch.float32, device="cuda")
+    for t in (0, 1, 7, 123456):
+        dg.uniforms(t, out)
+        d = out.cpu().numpy()
+        for b in range(w.B):
+            h = hg.uniforms(b, t)
+            assert np.array_equal(d[b].view(np.uint32), h.view(np.uint32)), (t, b)
+            assert (h >= 0).all() and (h < 1).all()

@@ -4,6 +4,7 @@ final histories and the counters.  The full-size workloads run in the launch
 configuration the benchmark times (the fused two-kernel step).  GPU."""
 import os
 
+import numpy as np
 import pytest
 
 import context_lookup_speculative_gb300 as clk
@@ -50,6 +51,34 @@ def test_draft_block_variants(kw):
     head/tail splits of the 15 drafts, a longer sticky exit."""
     w = wl.make_small("mixed", seed=74, B=8, V=2048, steps=96)
     _parity(w, params=clk.Params.default(**kw), oparams=oracle.Params.default(**kw))
+
+
+@pytest.mark.parametrize("kind", ["mixed", "periodic", "copy"])
+def test_sampled_loop_at_near_zero_temperature_matches_the_greedy_oracle(kind):
+    """Sampling verification at inverse temperature 1e4 is greedy on these
+    rows (each has a unique maximum): the whole sampled loop on the GPU
+    equals the greedy oracle, records, histories and counters."""
+    w = wl.make_small(kind, seed=75, B=6, V=4096, steps=48)
+    dev = drive.run_device(w, mode="sample", inv_temp=1e4)
+    ref = oracle.run(w, threads=THREADS)
+    # the greedy oracle records argmax rows; the sampled run records the emitted tokens
+    ref.g = np.where(np.arange(16)[None, None, :] <= ref.a[:, :, None], ref.g, -1)
+    msgs = drive.compare(dev, ref)
+    assert not msgs, "\n".join(msgs[:8])
+
+
+@pytest.mark.parametrize("inv_temp", [1.0, 2.5])
+def test_sampled_loop_matches_the_sampled_oracle(inv_temp):
+    """The sampled decode loop (lookup, scheduler, fusion, sampling verify,
+    commit) against the oracle's sampled loop with the same uniforms: every
+    record, history and counter equal (no decision of these seeded runs
+    lies within rounding of its boundary)."""
+    w = wl.make_small("mixed", seed=76, B=6, V=2048, steps=48)
+    dev = drive.run_device(w, mode="sample", inv_temp=inv_temp)
+    ref = oracle.run(w, threads=THREADS, inv_temp=inv_temp)
+    msgs = drive.compare(dev, ref)
+    assert not msgs, "\n".join(msgs[:8])
+    assert (ref.a > 0).any()
 
 
 def test_config0_tiny():

@@ -256,3 +256,33 @@ def test_planted_sampler_mistake_is_caught(name, tmp_path, monkeypatch):
         getattr(lib, fname).restype = getattr(real, fname).restype
     monkeypatch.setattr(oracle, "_lib", lambda: lib)
     assert not _sample_pins_pass(), f"pins did not catch: {name}"
+
+
+def test_sampled_loop_at_near_zero_temperature_is_the_greedy_loop():
+    # every synthetic row has a unique maximum (the ground truth's +8 lift):
+    # at inverse temperature 1e4 the target is a point mass on it, so a draft
+    # is accepted iff it is the argmax and the draw is the argmax
+    for kind in ("mixed", "periodic"):
+        w = wl.make_small(kind, seed=93, B=4, V=1024, steps=40)
+        g = oracle.run(w, threads=4)
+        s = oracle.run(w, threads=4, inv_temp=1e4)
+        for f in ("k", "j", "L", "a", "blk"):
+            assert np.array_equal(getattr(g, f), getattr(s, f)), (kind, f)
+        assert all(np.array_equal(x, y) for x, y in zip(g.histories, s.histories))
+        emitted = np.where(np.arange(16)[None, None, :] <= g.a[:, :, None], g.g, SENT)
+        assert np.array_equal(emitted, s.g)
+
+
+def test_sampled_loop_commits_its_draws():
+    w = wl.make_small("copy", seed=94, B=3, V=512, steps=30)
+    s = oracle.run(w, threads=3, inv_temp=0.8)
+    gen = wl.HostGen(w)
+    for i in range(w.B):
+        n0 = w.prompts[i].size
+        h = s.histories[i]
+        toks = [int(x) for t in range(w.steps) for x in s.g[t, i][:s.a[t, i] + 1]]
+        assert h[n0:].tolist() == toks
+        # replaying step 0 by hand gives the same result
+        rows = gen.logits_rows(i, n0, int(s.L[0, i]))
+        a, out = oracle.sample_verify(rows, s.blk[0, i], int(s.L[0, i]), 0.8, gen.uniforms(i, 0))
+        assert a == s.a[0, i] and out.tolist() == s.g[0, i].tolist()

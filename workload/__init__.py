@@ -375,6 +375,8 @@ def host_lib() -> ctypes.CDLL:
     lib.wl_head.restype = None
     lib.wl_truth.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64]
     lib.wl_truth.restype = ctypes.c_int32
+    lib.wl_uniforms.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+    lib.wl_uniforms.restype = None
     return lib
 
 
@@ -403,6 +405,16 @@ class HostGen:
     def head_fn(self) -> int:
         return ctypes.cast(self.lib.wl_head, ctypes.c_void_p).value
 
+    @property
+    def uniform_fn(self) -> int:
+        return ctypes.cast(self.lib.wl_uniforms, ctypes.c_void_p).value
+
+    def uniforms(self, b: int, t: int) -> np.ndarray:
+        """Step t's sampling uniforms of request b, float32 [16, 2]."""
+        out = np.empty((ROWS, 2), dtype=np.float32)
+        self.lib.wl_uniforms(self.ctx_ptr, b, t, out.ctypes.data)
+        return out
+
     def np_dtype(self):
         return np.uint16 if self.w.dtype == BF16 else np.float32
 
@@ -428,7 +440,8 @@ def dev_lib() -> ctypes.CDLL:
     lib.wl_dev_head.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                 ctypes.c_void_p]
     lib.wl_dev_advance.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
-    for f in (lib.wl_dev_logits, lib.wl_dev_head, lib.wl_dev_advance):
+    lib.wl_dev_uniforms.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    for f in (lib.wl_dev_logits, lib.wl_dev_head, lib.wl_dev_advance, lib.wl_dev_uniforms):
         f.restype = ctypes.c_int
     return lib
 
@@ -496,6 +509,16 @@ class DevGen:
         rc = self.lib.wl_dev_head(ctypes.addressof(self.ctx), pos.data_ptr(), t, out.data_ptr(), self._stream())
         if rc != 0:
             raise RuntimeError(f"wl_dev_head failed ({rc})")
+        return out
+
+    def uniforms(self, t: int, out):
+        """Fill out[B, 16, 2] (contiguous float32) with step t's sampling uniforms."""
+        if tuple(out.shape) != (self.w.B, ROWS, 2) or out.dtype != self.torch.float32 or not out.is_contiguous() \
+                or not out.is_cuda:
+            raise ValueError(f"uniform buffer must be contiguous float32 [{self.w.B}, {ROWS}, 2] on the GPU")
+        rc = self.lib.wl_dev_uniforms(ctypes.addressof(self.ctx), t, out.data_ptr(), self._stream())
+        if rc != 0:
+            raise RuntimeError(f"wl_dev_uniforms failed ({rc})")
         return out
 
     def advance(self, emitted):

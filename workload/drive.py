@@ -44,12 +44,15 @@ def make_lookup(w: wl.Workload, params=None, slots=None, max_hist=None, device="
 
 
 def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: str = "fused",
-               device="cuda", record: bool = True) -> DeviceRun:
+               device="cuda", record: bool = True, inv_temp: float = 0.0) -> DeviceRun:
     """Run `steps` decode steps of workload `w` on the GPU.
 
     mode "fused":   propose_fuse_sched + verify_append (the Step driver)
     mode "semi":    lookup_propose, fuse_sched, verify_append
     mode "unfused": lookup_propose, sched_step, fuse, verify_greedy, lookup_append
+    mode "sample":  lookup_propose, sched_step, fuse, verify_sample (at
+                    `inv_temp`, with the generator's uniforms), lookup_append;
+                    the records' g holds the emitted tokens
     """
     steps = w.steps if steps is None else steps
     params = params or clk.Params.default()
@@ -65,6 +68,12 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     rec = {n: torch.zeros((steps, B), **i32) for n in ("k", "j", "L", "a", "e")}
     rec.update({n: torch.zeros((steps, B, clk.BLOCK), **i32) for n in ("c", "blk", "g")})
     scratch = clk.verify_scratch(B, device=device) if mode == "unfused" else None
+    if mode == "sample":
+        if not inv_temp > 0:
+            raise ValueError("mode 'sample' needs inv_temp > 0")
+        sscratch = clk.verify_sample_scratch(logits.dtype, w.V, B, device=device)
+        uni = torch.zeros((B, clk.BLOCK, 2), dtype=torch.float32, device=device)
+        temps = torch.full((B,), float(inv_temp), dtype=torch.float32, device=device)
     last_tok = torch.from_numpy(np.array([p[-1] for p in w.prompts], dtype=np.int32)).to(device)
     for t in range(steps):
         gen.head(t, head7)
@@ -74,7 +83,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
         elif mode == "semi":
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
             clk.fuse_sched(lk, slots, st.draft, st.k, head, st.accept, st.length, st.length, st.block)
-        elif mode == "unfused":
+        elif mode in ("unfused", "sample"):
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
             clk.sched_step(lk, slots, st.k, st.accept, st.length, st.length)
             clk.fuse(params, last_tok, st.draft, st.k, head, st.length, st.block)
@@ -85,6 +94,12 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
             clk.verify_greedy(logits, st.block, st.length, st.argmax, st.accept, st.emitted, st.out_tok, scratch)
             clk.lookup_append(lk, slots, st.out_tok, st.emitted)
             last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
+        elif mode == "sample":
+            gen.uniforms(t, uni)
+            clk.verify_sample(logits, st.block, st.length, temps, uni, st.accept, st.emitted, st.out_tok, sscratch)
+            clk.lookup_append(lk, slots, st.out_tok, st.emitted)
+            last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
+            st.argmax.copy_(st.out_tok)  # recorded as g
         else:
             st.post(logits)
         gen.advance(st.emitted)

@@ -86,6 +86,14 @@ __global__ void wl_advance_kernel(int64_t* pos, const int32_t* __restrict__ emit
     if (b < B) pos[b] += emitted[b];
 }
 
+__global__ void wl_uniform_kernel(uint64_t seed, int32_t B, int32_t t, float* out)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)B * WL_ROWS * 2) return;
+    uint32_t b = (uint32_t)(i / (WL_ROWS * 2)), r = (uint32_t)((i / 2) % WL_ROWS), k = (uint32_t)(i % 2);
+    out[i] = wl_uniform(seed, b, (uint32_t)t, r, k);
+}
+
 static int wl_check(cudaError_t e) { return e == cudaSuccess ? 0 : -3; }
 
 extern "C" {
@@ -115,6 +123,15 @@ int wl_dev_advance(int64_t* d_pos, const int32_t* d_emitted, int32_t B, cudaStre
 {
     if (B == 0) return 0;
     wl_advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(d_pos, d_emitted, B);
+    return wl_check(cudaGetLastError());
+}
+
+/* The uniforms [B, 16, 2] of step t. */
+int wl_dev_uniforms(const wl_dev_ctx* c, int32_t t, float* d_out, cudaStream_t s)
+{
+    if (c->B == 0) return 0;
+    const int64_t n = (int64_t)c->B * WL_ROWS * 2;
+    wl_uniform_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(c->seed, c->B, t, d_out);
     return wl_check(cudaGetLastError());
 }
 

@@ -76,3 +76,12 @@ void wl_logits_block(const void* ctx, int32_t b, int64_t P0, int32_t rows, void*
     for (int32_t r = 0; r < rows; ++r)
         wl_logits_row(ctx, b, P0 + r, (char*)out + (size_t)r * (size_t)c->V * esz);
 }
+
+/* The 16 x 2 uniforms of step t of request b (row-major [16][2]). */
+void wl_uniforms(const void* ctx, int32_t b, int32_t t, float* out)
+{
+    const wl_ctx* c = (const wl_ctx*)ctx;
+    for (uint32_t r = 0; r < WL_ROWS; ++r)
+        for (uint32_t k = 0; k < 2; ++k) out[2 * r + k] = wl_uniform(c->seed, (uint32_t)b, (uint32_t)t, r, k);
+}
+

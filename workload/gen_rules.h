@@ -38,6 +38,7 @@
 /* Domain-separation words, one per kind of draw. */
 #define WL_DOMAIN_LOGITS 0x6C6F676974730000ull
 #define WL_DOMAIN_HEAD 0x6865616400000000ull
+#define WL_DOMAIN_UNIFORM 0x756E69666F726D00ull
 #define WL_GOLDEN 0x9E3779B97F4A7C15ull
 
 /* Number of head proposals per step and the verify block width. */
@@ -85,6 +86,16 @@ WL_FN int32_t wl_head_token(uint64_t w, uint32_t i, int32_t truth, uint32_t V)
 {
     if ((uint32_t)(w >> 32) < wl_head_threshold(i) && truth >= 0) return truth;
     return (int32_t)(((w & 0xFFFFFFFFull) * (uint64_t)V) >> 32);
+}
+
+/* Uniform number k (0: acceptance, 1: draw) of verify row r at step t of
+ * request b, for sampling verification: the top 24 bits of a hash word times
+ * 2^-24, a float in [0, 1) that both sides compute exactly. */
+WL_FN float wl_uniform(uint64_t seed, uint32_t b, uint32_t t, uint32_t r, uint32_t k)
+{
+    const uint64_t w =
+        wl_mix64(wl_mix64(wl_mix64(wl_mix64(seed ^ WL_DOMAIN_UNIFORM) + b) + t) + (uint64_t)(2u * r + k));
+    return (float)(uint32_t)(w >> 40) * (1.0f / 16777216.0f);
 }
 
 #endif /* WL_GEN_RULES_H */
