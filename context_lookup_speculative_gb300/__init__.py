@@ -108,6 +108,8 @@ _SIGS = [
     ("clk_verify_sample_scratch_bytes", ctypes.c_int, [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     ("clk_verify_sample", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
+    ("clk_verify_sample_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                                _P, _P, ctypes.c_size_t, _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
     ("clk_status_clear", ctypes.c_int, [_P, _P]),
     ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
@@ -362,6 +364,21 @@ def verify_sample(logits, block, length, inv_temp, uniform, accept, emitted, out
                                    scratch.numel(), _stream(stream)))
 
 
+def verify_sample_append(h: Lookup, slots, logits, block, length, inv_temp, uniform, accept, emitted, out_tok,
+                         scratch, stream=None):
+    """Sampling verification fused with the token commit (clk_verify_sample_append)."""
+    dt, rs, qs, V = _logits_args(logits)
+    B = slots.numel()
+    _check("clk_verify_sample_append",
+           lib().clk_verify_sample_append(h.handle, _ptr(slots), logits.data_ptr(), dt, rs, qs, V, B,
+                                          _ptr(block, shape=(B, BLOCK)), _ptr(length, shape=(B,)),
+                                          _ptr(inv_temp, torch.float32, (B,), "inv_temp"),
+                                          _ptr(uniform, torch.float32, (B, BLOCK, 2), "uniform"),
+                                          _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
+                                          _ptr(out_tok, shape=(B, BLOCK)), _ptr(scratch, torch.uint8, name="scratch"),
+                                          scratch.numel(), _stream(stream)))
+
+
 def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None,
                   length_hint=None):
     dt, rs, qs, V = _logits_args(logits)
@@ -382,6 +399,8 @@ class Step:
 
     ``pre(head)``    -> propose + scheduler + fusion: draft, k, j, length, block
     ``post(logits)`` -> verify + commit: argmax, accept, emitted, out_tok
+    ``post_sample(logits, inv_temp, uniform)`` -> the same step verified by
+    sampling (point-mass drafts): accept, emitted, out_tok
     The previous step's accept/length feed the scheduler.  The block lengths
     alternate between two buffers, so that ``post`` can pass the previous
     step's lengths as the verify launch's prediction while ``pre`` writes the
@@ -409,6 +428,7 @@ class Step:
         self._head_shape = (B, lookup.params.head)
         self._rows = lookup.params.long_len
         self._lib = lib()
+        self._sscratch = None
 
     @property
     def length(self) -> torch.Tensor:
@@ -440,3 +460,23 @@ class Step:
                self._lib.clk_verify_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V, self.B,
                                            p["block"], self._lp[self._cur], self._lp[self._cur ^ 1], p["argmax"],
                                            p["accept"], p["emitted"], p["out_tok"], _stream(stream)))
+
+    def post_sample(self, logits, inv_temp, uniform, stream=None):
+        """Verify the block by sampling at inverse temperatures inv_temp
+        (float32 [B]) with the uniforms uniform (float32 [B, 16, 2]), and
+        commit the emitted tokens."""
+        dt, rs, qs, V = _logits_args(logits)
+        if logits.shape[0] != self.B or logits.shape[1] < self._rows:
+            raise ValueError(f"logits must be [{self.B}, >= {self._rows}, V]")
+        if self._sscratch is None or self._sscratch[0] != (logits.dtype, V):
+            self._sscratch = ((logits.dtype, V), verify_sample_scratch(logits.dtype, V, self.B,
+                                                                       device=self.slots.device, stream=stream))
+        p = self._p
+        sc = self._sscratch[1]
+        _check("clk_verify_sample_append",
+               self._lib.clk_verify_sample_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V,
+                                                  self.B, p["block"], self._lp[self._cur],
+                                                  _ptr(inv_temp, torch.float32, (self.B,), "inv_temp"),
+                                                  _ptr(uniform, torch.float32, (self.B, BLOCK, 2), "uniform"),
+                                                  p["accept"], p["emitted"], p["out_tok"], sc.data_ptr(), sc.numel(),
+                                                  _stream(stream)))

@@ -66,6 +66,7 @@ struct SampleArgs {
     int32_t* out_tok;
     uint32_t* done;  // [B] segments finished per request
     float2* part;    // [B][16][S][kSWarpsPerCta] (m, s) per warp
+    const int32_t* slots;  // fused with the commit only: the requests' slots
 };
 
 __device__ __forceinline__ bool len_valid(int32_t l) { return l >= 1 && l <= kBlock; }
@@ -424,16 +425,19 @@ __device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t
 struct FinSmem {
     float m[kBlock], s[kBlock];  // each row's combined pair
     float xc[kBlock];            // each row's draft logit
-    float ex;                    // weight exp(x_c t - m) of the removed draft
-    float tgt;                   // the sample's target inside the chosen segment
+    float ex;                    // weight of the removed draft
+    unsigned long long tgt;      // the draw's target inside the chosen segment (fixed point)
     int32_t a, excl, seg, tok, cross;
-    float wsum[kSWarpsPerCta];
+    unsigned long long wsum[kSWarpsPerCta];
+    int32_t lastw[kSWarpsPerCta];  // each warp's last element of positive weight
+    int32_t out[kBlock];  // the emitted tokens (fused: committed)
+    int32_t flag[2];
 };
 
 // Request b is complete (all of its segments' pairs are stored): decide the
 // drafts, draw the token, write the outputs, rewind the counter.  Block-wide.
-template <int DT>
-__device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSmem& fs)
+template <int DT, bool FUSED>
+__device__ __noinline__ void sample_finish(const SampleArgs& a, const LookupDev& Ldev, int32_t b, FinSmem& fs)
 {
     using E = SElem<DT>;
     const unsigned full = 0xFFFFFFFFu;
@@ -496,34 +500,52 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
     __syncthreads();
     const int32_t ra = fs.a, excl = fs.excl;
     const float mra = fs.m[ra];
-    // The segment holding the sample: running sum of the segments' weights
-    // (relative to the row's maximum, the removed draft taken out of its
-    // segment) against u * (row sum - removed weight).
+    // The segment holding the draw.  The draw's prefix arithmetic is exact:
+    // sums of more than a few weights are scaled to 64-bit fixed point (2^61
+    // for the row's sum) and added as integers, so the long running sums
+    // round nowhere; token widths in a large vocabulary are far below
+    // float32's resolution of a sum of the whole row.  Segment weights (from the stored pairs,
+    // relative to the row's maximum, the removed draft taken out of its
+    // segment) are summed once for the total and again, in order, to find
+    // the segment whose running sum passes u * total.
+    const float sc = 2305843009213693952.0f / fmaxf(fs.s[ra], 1.0f);  // 2^61 / row sum
     if (warp == 0) {
-        const float target = a.uniform[((int64_t)b * kBlock + ra) * 2 + 1] * fmaxf(0.0f, fs.s[ra] - fs.ex);
         const float2* pp = part_of(a, b, ra, 0);
         const int32_t exseg = excl >= 0 ? (int32_t)(excl / kSegElems) : -1;
-        float carry = 0.0f;
+        const unsigned long long qex = __float2ull_rn(fs.ex * sc);
+        auto seg_weight = [&](int32_t k) -> unsigned long long {
+            if (k >= S) return 0ull;
+            float w = 0.0f;
+            for (int i = 0; i < kSWarpsPerCta; ++i) {
+                const float2 q = __ldcg(pp + (int64_t)k * kSWarpsPerCta + i);
+                if (q.y > 0.0f) w += q.y * ex2(q.x - mra);
+            }
+            unsigned long long qw = __float2ull_rn(w * sc);
+            if (k == exseg) qw = qw > qex ? qw - qex : 0ull;
+            return qw;
+        };
+        unsigned long long total = 0ull;
+        for (int32_t k0 = 0; k0 < S; k0 += 32) {
+            unsigned long long w = seg_weight(k0 + lane);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(full, w, o);
+            total += w;
+        }
+        const unsigned long long target =
+            __double2ull_rd((double)a.uniform[((int64_t)b * kBlock + ra) * 2 + 1] * (double)total);
+        unsigned long long carry = 0ull, before = 0ull;
         int32_t found = -1, lastpos = -1;
-        float before = 0.0f;
         for (int32_t k0 = 0; k0 < S && found < 0; k0 += 32) {
             const int32_t k = k0 + lane;
-            float w = 0.0f;
-            if (k < S) {
-                for (int i = 0; i < kSWarpsPerCta; ++i) {
-                    const float2 q = __ldcg(pp + (int64_t)k * kSWarpsPerCta + i);
-                    if (q.y > 0.0f) w += q.y * ex2(q.x - mra);
-                }
-                if (k == exseg) w = fmaxf(0.0f, w - fs.ex);
-            }
-            float incl = w;
+            const unsigned long long w = seg_weight(k);
+            unsigned long long incl = w;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(full, incl, o);
+                const unsigned long long y = __shfl_up_sync(full, incl, o);
                 if (lane >= o) incl += y;
             }
             const unsigned cross = __ballot_sync(full, k < S && carry + incl > target);
-            const unsigned pos = __ballot_sync(full, k < S && w > 0.0f);
+            const unsigned pos = __ballot_sync(full, k < S && w > 0ull);
             if (pos) lastpos = k0 + 31 - __clz(pos);
             if (cross) {
                 const int32_t l = __ffs(cross) - 1;
@@ -534,7 +556,7 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
         }
         if (lane == 0) {
             fs.seg = found >= 0 ? found : lastpos;
-            fs.tgt = found >= 0 ? target - before : INFINITY;  // no crossing: the last positive weight
+            fs.tgt = found >= 0 ? target - before : ~0ull;  // no crossing: the last positive weight
         }
     }
     __syncthreads();
@@ -548,33 +570,34 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
     const typename E::T* row = base + (int64_t)ra * a.row_stride;
     const int64_t s0 = sg < 0 ? 0 : (int64_t)sg * kSegElems;
     const int64_t s1 = sg < 0 ? 0 : min(s0 + kSegElems, (int64_t)V);
-    float tgt = fs.tgt;
+    unsigned long long tgt = fs.tgt;
     int64_t lastv = -1;  // this thread's last element of positive weight
     if (tid == 0) fs.tok = CLK_SENT;
     for (int64_t c0 = s0; c0 < s1; c0 += kChunk) {
         const int64_t v0 = c0 + (int64_t)tid * kRun;
         float wv[kRun];
-        float own = 0.0f;
+        float ownf = 0.0f;  // 16 weights: float is exact enough for one run
 #pragma unroll
         for (int i = 0; i < kRun; ++i) {
             const int64_t v = v0 + i;
             const bool in = v < s1 && v != excl;
             const float x = v < s1 ? E::value(row[v]) : 0.0f;
             wv[i] = in ? ex2(fmaf(x, cz, -mra)) : 0.0f;
-            own += wv[i];
+            ownf += wv[i];
             if (wv[i] > 0.0f) lastv = v;
         }
-        float incl = own;
+        const unsigned long long own = __float2ull_rn(ownf * sc);
+        unsigned long long incl = own;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(full, incl, o);
+            const unsigned long long y = __shfl_up_sync(full, incl, o);
             if (lane >= o) incl += y;
         }
         __syncthreads();  // the previous chunk's sums have been read
         if (lane == 31) fs.wsum[warp] = incl;
         if (tid == 0) fs.cross = -1;
         __syncthreads();
-        float pre = incl - own, tot = 0.0f;
+        unsigned long long pre = incl - own, tot = 0ull;
         for (int w = 0; w < kSWarpsPerCta; ++w) {
             if (w < warp) pre += fs.wsum[w];
             tot += fs.wsum[w];
@@ -583,14 +606,14 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
             // the crossing run: the last one of positive weight that starts
             // at or before the target (one exists: the first positive run
             // starts at 0 <= target)
-            if (own > 0.0f && pre <= tgt) atomicMax(&fs.cross, tid);
+            if (own > 0ull && pre <= tgt) atomicMax(&fs.cross, tid);
             __syncthreads();
             if (tid == fs.cross) {
-                float run = pre;
+                unsigned long long run = pre;
                 int64_t tok = lastv;
 #pragma unroll
                 for (int i = 0; i < kRun; ++i) {
-                    run += wv[i];
+                    run += __float2ull_rn(wv[i] * sc);
                     if (wv[i] > 0.0f && run > tgt) {
                         tok = v0 + i;
                         break;
@@ -608,12 +631,12 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
         // segment's last element of positive weight
         const unsigned has = __ballot_sync(full, lastv >= 0);
         __syncthreads();
-        if (has && lane == 31 - __clz(has)) fs.wsum[warp] = __int_as_float((int32_t)lastv);
-        else if (lane == 0 && !has) fs.wsum[warp] = __int_as_float(-1);
+        if (has && lane == 31 - __clz(has)) fs.lastw[warp] = (int32_t)lastv;
+        else if (lane == 0 && !has) fs.lastw[warp] = -1;
         __syncthreads();
         if (tid == 0) {
             for (int w = kSWarpsPerCta - 1; w >= 0; --w) {
-                const int32_t v = __float_as_int(fs.wsum[w]);
+                const int32_t v = fs.lastw[w];
                 if (v >= 0) {
                     fs.tok = v;
                     break;
@@ -626,6 +649,7 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
         const int32_t r = tid;
         const int32_t out = r < fs.a ? a.block[(int64_t)b * kBlock + r + 1] : (r == fs.a ? fs.tok : CLK_SENT);
         a.out_tok[(int64_t)b * kBlock + r] = out;
+        fs.out[r] = out;
     }
     if (tid == 0) {
         a.accept[b] = fs.a;
@@ -633,25 +657,43 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, int32_t b, FinSm
         a.done[b] = 0u;
     }
     __syncthreads();
+    if (FUSED) {
+        const int32_t slot = a.slots[b];
+        if (slot < 0 || slot >= Ldev.max_slots) {
+            if (tid == 0) latch(Ldev.status, CLK_EINVAL, b);
+        } else {
+            block_commit_tokens(Ldev, slot, fs.out, fs.a + 1, fs.flag);
+        }
+        __syncthreads();
+    }
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArgs a)
+template <int DT, bool VEC, bool FUSED>
+__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArgs a, LookupDev Ldev)
 {
     extern __shared__ int32_t P[];  // B + 1
     __shared__ int32_t sm_warp[kSWarpsPerCta];
     __shared__ int32_t sm_last;
     __shared__ FinSmem fs;
+    if (FUSED) {
+        // Launched as a programmatic dependent of the proposal launch, whose
+        // blocks and lengths it reads: let the next launch be scheduled,
+        // then wait for the proposal to complete.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     const int tid = threadIdx.x;
     const int32_t B = a.B;
     sample_prefix(a, P, sm_warp);
-    // Requests with no rows (invalid length or temperature): empty result.
+    // Requests with no rows (invalid length or temperature): empty result
+    // (fused: an error, nothing committed).
     if (blockIdx.x == 0) {
         for (int32_t b = tid; b < B; b += kSThreads) {
             if (sample_rows(a, b) != 0) continue;
             for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
             a.accept[b] = 0;
             a.emitted[b] = 0;
+            if (FUSED) latch(Ldev.status, CLK_EINVAL, b);
         }
     }
     const int64_t S = a.S;
@@ -672,7 +714,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
             sm_last = atomicAdd(a.done + b, n) + n == need;
         }
         __syncthreads();
-        if (sm_last) sample_finish<DT>(a, b, fs);
+        if (sm_last) sample_finish<DT, FUSED>(a, Ldev, b, fs);
         k = k1;
     }
 }
@@ -688,14 +730,14 @@ int sample_sizes(int32_t dtype, int32_t V, int32_t B, int32_t* S, size_t* bytes)
     return CLK_OK;
 }
 
-template <int DT, bool VEC>
-int launch_sample(const SampleArgs& a, cudaStream_t s)
+template <int DT, bool VEC, bool FUSED>
+int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
 {
     static int cache[64] = {0};  // resident CTAs per SM, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
     const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
-    auto kern = k_sample<DT, VEC>;
+    auto kern = k_sample<DT, VEC, FUSED>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CLK_ECUDA;
@@ -711,8 +753,21 @@ int launch_sample(const SampleArgs& a, cudaStream_t s)
     if (sms <= 0) return CLK_ECUDA;
     const int64_t segs = (int64_t)a.B * kBlock * a.S;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)occ * sms, segs));
-    kern<<<(unsigned)grid, kSThreads, smem, s>>>(a);
-    return launch_status();
+    if (!FUSED) {
+        kern<<<(unsigned)grid, kSThreads, smem, s>>>(a, Ldev);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, a, Ldev));
 }
 
 }  // namespace
@@ -727,16 +782,23 @@ extern "C" int clk_verify_sample_scratch_bytes(int32_t dtype, int32_t V, int32_t
     return sample_sizes(dtype, V, B, &S, bytes);
 }
 
-extern "C" int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
-                                 int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
-                                 const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
-                                 int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
-                                 clk_stream_t s)
+namespace {
+
+// Checks and launches both entry points; h == nullptr: stateless.
+int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype, int64_t row_stride,
+                 int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                 const float* d_inv_temp, const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
+                 int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs)
 {
     int32_t S = 0;
     size_t need = 0;
     int rc = sample_sizes(dtype, V, B, &S, &need);
     if (rc != CLK_OK) return rc;
+    if (h != nullptr) {
+        rc = check_batch(h, B);
+        if (rc != CLK_OK) return rc;
+        if (!ok_i32(d_slots)) return CLK_EINVAL;
+    }
     if (row_stride < V || req_stride < 0 || (B > 1 && req_stride < row_stride)) return CLK_EINVAL;
     const size_t esz = dtype == CLK_DTYPE_BF16 ? 2 : 4;
     if (d_logits == nullptr || !aligned(d_logits, esz)) return CLK_EINVAL;
@@ -761,10 +823,43 @@ extern "C" int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t ro
     a.out_tok = d_out_tok;
     a.done = static_cast<uint32_t*>(d_scratch);
     a.part = reinterpret_cast<float2*>(static_cast<char*>(d_scratch) + align_up((size_t)B * sizeof(uint32_t), 16));
+    a.slots = d_slots;
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
-    cudaStream_t cs = (cudaStream_t)s;
-    if (dtype == CLK_DTYPE_BF16)
-        return vec ? launch_sample<CLK_DTYPE_BF16, true>(a, cs) : launch_sample<CLK_DTYPE_BF16, false>(a, cs);
-    return vec ? launch_sample<CLK_DTYPE_F32, true>(a, cs) : launch_sample<CLK_DTYPE_F32, false>(a, cs);
+    const bool bf = dtype == CLK_DTYPE_BF16;
+    if (h != nullptr) {
+        const LookupDev& L = h->dev;
+        if (bf) return vec ? launch_sample<CLK_DTYPE_BF16, true, true>(a, L, cs)
+                           : launch_sample<CLK_DTYPE_BF16, false, true>(a, L, cs);
+        return vec ? launch_sample<CLK_DTYPE_F32, true, true>(a, L, cs)
+                   : launch_sample<CLK_DTYPE_F32, false, true>(a, L, cs);
+    }
+    const LookupDev none = {};
+    if (bf) return vec ? launch_sample<CLK_DTYPE_BF16, true, false>(a, none, cs)
+                       : launch_sample<CLK_DTYPE_BF16, false, false>(a, none, cs);
+    return vec ? launch_sample<CLK_DTYPE_F32, true, false>(a, none, cs)
+               : launch_sample<CLK_DTYPE_F32, false, false>(a, none, cs);
+}
+
+}  // namespace
+
+extern "C" int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                 int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                 const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                 int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                                 clk_stream_t s)
+{
+    return sample_entry(nullptr, nullptr, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_inv_temp,
+                        d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, (cudaStream_t)s);
+}
+
+extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
+                                        int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                                        const int32_t* d_block, const int32_t* d_len, const float* d_inv_temp,
+                                        const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
+                                        int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, clk_stream_t s)
+{
+    if (h == nullptr) return CLK_EINVAL;
+    return sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_inv_temp,
+                        d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, (cudaStream_t)s);
 }

@@ -355,6 +355,26 @@ CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_s
                               int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
                               clk_stream_t s);
 
+/* clk_verify_sample followed by clk_lookup_append of its d_out_tok /
+ * d_emitted, in one launch: the sampled step of a decode loop.  Each
+ * request's emitted tokens are committed to the history of d_slots[b] as
+ * soon as its draw is made; the k-grams they complete are indexed by the
+ * next proposal call on the slot.  The results equal those of the two
+ * calls.  The launch is a programmatic dependent of the preceding launch on
+ * the stream, and d_block / d_len may come from that launch
+ * (clk_propose_fuse_sched): it waits for it before reading them.  The
+ * logits, inverse temperatures and uniforms must be complete when the call
+ * is made.  A request with an invalid length or temperature gets the empty
+ * result, commits nothing and latches CLK_EINVAL in the handle's status (as
+ * do a bad slot, an out-of-vocabulary token or a full history, which
+ * clk_lookup_append would reject).  Scratch as for clk_verify_sample; calls
+ * sharing it must not overlap on the GPU. */
+CLK_API int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
+                                     int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                                     const int32_t* d_block, const int32_t* d_len, const float* d_inv_temp,
+                                     const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
+                                     int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, clk_stream_t s);
+
 /* ---------------------------------------------------------------------- */
 /* Status, counters, inspection (these synchronise the stream)             */
 /* ---------------------------------------------------------------------- */

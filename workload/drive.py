@@ -53,6 +53,8 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     mode "sample":  lookup_propose, sched_step, fuse, verify_sample (at
                     `inv_temp`, with the generator's uniforms), lookup_append;
                     the records' g holds the emitted tokens
+    mode "sample_fused": propose_fuse_sched + verify_sample_append (the Step
+                    driver's sampled step); g as for "sample"
     """
     steps = w.steps if steps is None else steps
     params = params or clk.Params.default()
@@ -68,7 +70,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     rec = {n: torch.zeros((steps, B), **i32) for n in ("k", "j", "L", "a", "e")}
     rec.update({n: torch.zeros((steps, B, clk.BLOCK), **i32) for n in ("c", "blk", "g")})
     scratch = clk.verify_scratch(B, device=device) if mode == "unfused" else None
-    if mode == "sample":
+    if mode in ("sample", "sample_fused"):
         if not inv_temp > 0:
             raise ValueError("mode 'sample' needs inv_temp > 0")
         sscratch = clk.verify_sample_scratch(logits.dtype, w.V, B, device=device)
@@ -78,7 +80,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     for t in range(steps):
         gen.head(t, head7)
         head = head7[:, :params.head].contiguous()
-        if mode == "fused":
+        if mode in ("fused", "sample_fused"):
             st.pre(head)
         elif mode == "semi":
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
@@ -99,6 +101,10 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
             clk.verify_sample(logits, st.block, st.length, temps, uni, st.accept, st.emitted, st.out_tok, sscratch)
             clk.lookup_append(lk, slots, st.out_tok, st.emitted)
             last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
+            st.argmax.copy_(st.out_tok)  # recorded as g
+        elif mode == "sample_fused":
+            gen.uniforms(t, uni)
+            st.post_sample(logits, temps, uni)
             st.argmax.copy_(st.out_tok)  # recorded as g
         else:
             st.post(logits)
