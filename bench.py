@@ -191,6 +191,21 @@ def run_ours(args, world, rank, local, dist):
             out.copy_(head7[:, :params.head])
 
     logits = gen.alloc_logits()
+    temp = getattr(args, "sampling", None)  # sampled verification at this temperature, else greedy
+    if temp is not None and not temp > 0:
+        raise ValueError("--sampling needs a temperature > 0")
+    temps = torch.full((B,), 1.0 / temp if temp else 1.0, dtype=torch.float32, device=device)
+    uni = torch.zeros((B, 16, 2), dtype=torch.float32, device=device)
+
+    def post(t, lg, u=None):
+        """The step's verify launch: greedy, or sampled with step t's uniforms."""
+        if temp is None:
+            st.post(lg)
+            return
+        if u is None:
+            gen.uniforms(t, uni)
+            u = uni
+        st.post_sample(lg, temps, u)
 
     def reinit():
         clk.lookup_init(lk, slots, d_ptok, d_poff)
@@ -213,7 +228,7 @@ def run_ours(args, world, rank, local, dist):
         gen_head(t, head)
         st.pre(head)
         gen.logits(logits)
-        st.post(logits)
+        post(t, logits)
         gen.advance(st.emitted)
     pos_hist[W + K].copy_(gen.pos)
     torch.cuda.synchronize()
@@ -221,6 +236,7 @@ def run_ours(args, world, rank, local, dist):
     per_step = B * 16 * V * (2 if w.dtype == wl.BF16 else 4)
     chunk = max(1, min(K, int(args.input_gb * 2 ** 30 // per_step)))
     heads = torch.zeros((chunk, B, params.head), dtype=torch.int32, device=device)
+    unis = torch.zeros((chunk, B, 16, 2), dtype=torch.float32, device=device)
     bufs = torch.empty((chunk, B, 16, V), dtype=gen.torch_dtype(), device=device)
     flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=device)  # > 2x the 129 MB L2
     del logits
@@ -232,7 +248,7 @@ def run_ours(args, world, rank, local, dist):
             gen_head(t, head)
             st.pre(head)
             gen.logits(lg)
-            st.post(lg)
+            post(t, lg)
             gen.advance(st.emitted)
         torch.cuda.synchronize()
 
@@ -240,6 +256,8 @@ def run_ours(args, world, rank, local, dist):
         for i in range(n):
             gen_head(t0 + i, heads[i], pos=pos_hist[t0 + i])
             gen.logits(bufs[i], pos=pos_hist[t0 + i])
+            if temp is not None:
+                gen.uniforms(t0 + i, unis[i])
         flush.zero_()  # no step may find its logits in L2
         torch.cuda.synchronize()
 
@@ -255,7 +273,7 @@ def run_ours(args, world, rank, local, dist):
                 st.pre(heads[i])
                 if events is not None:
                     events[3 * i + 1].record()
-                st.post(bufs[i])
+                post(None, bufs[i], unis[i])
                 if events is not None:
                     events[3 * i + 2].record()
                 if lens is not None:
@@ -282,7 +300,7 @@ def run_ours(args, world, rank, local, dist):
             ev[3 * i].record(stream)
             st.pre(heads[i])
             ev[3 * i + 1].record(stream)
-            st.post(bufs[i])
+            post(None, bufs[i], unis[i])
             ev[3 * i + 2].record(stream)
             lens_b[i].copy_(st.length)
         torch.cuda.synchronize()
@@ -344,21 +362,25 @@ def run_ours(args, world, rank, local, dist):
     dc = {k: c_after[k] - c_before[k] for k in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")}
     rows = params.short_len * dc["steps"] + (params.long_len - params.short_len) * dc["long_steps"]
     esz = 2 if w.dtype == wl.BF16 else 4
-    verify_bytes = rows * V * esz                       # logits rows read, all timed steps
+    # sampled verification also re-reads one segment of each request's drawn row
+    draw_bytes = B * min(V, 16384) * esz if temp is not None else 0
+    verify_bytes = rows * V * esz + draw_bytes * K      # logits rows read, all timed steps
     path_bytes = verify_bytes + LOOKUP_BYTES_PER_REQ * B * K
     peak, peak_kind = _peaks()
-    verify_bytes_b = rows_b * V * esz                   # the pass-B steps
+    verify_bytes_b = rows_b * V * esz + draw_bytes * nb  # the pass-B steps
     verify_gbs = verify_bytes_b / (verify_ms * 1e-3) / 1e9
     path_gbs = path_bytes / (total_ms * 1e-3) / 1e9
     ratio = _traffic_ratio()
 
     ablation = run_lookup_ablation(lk, slots, w, device) if args.ablation else None
-    e2e = run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device) if (rank == 0 and not args.no_e2e) else None
+    e2e = (run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device)
+           if (rank == 0 and not args.no_e2e and temp is None) else None)
     cpu = run_cpu_baseline(args, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
     steps_s = world * K / total_s
     out = {
-        "metric": METRIC, "value": round(steps_s, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": METRIC if temp is None else METRIC + f", sampled verification at temperature {temp}",
+        "value": round(steps_s, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(total_s * 1e3 / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}, {W} warm-up + {K} timed of "
@@ -380,10 +402,12 @@ def run_ours(args, world, rank, local, dist):
                               "steps": nb, "note": "each launch timed alone (events between launches)"},
                  "overlapped_us_per_step": round(total_ms * 1e3 / K, 3),
                  "index_build_ms": round(index_build_ms, 3)},
-        "roofline": {"bound": "hbm", "kernel": "k_verify_step (verify_append)", "achieved": round(verify_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": "k_verify_step (verify_append)" if temp is None else
+                     "k_sample (verify_sample_append)", "achieved": round(verify_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(verify_gbs / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": None if ratio is None or args.config != "2" else int(ratio * verify_bytes_b / nb),
+                     "traffic": None if ratio is None or args.config != "2" or temp is not None
+                     else int(ratio * verify_bytes_b / nb),
                      "traffic_note": "ncu dram read+write per launch, as the measured traffic/algorithmic ratio "
                                      "of three captured full-size launches times this run's bytes per launch",
                      "algorithmic_bytes_per_launch": int(verify_bytes_b // nb),
@@ -629,7 +653,8 @@ def run_cpu_baseline(args, w):
 
     steps = min(args.cpu_steps, w.steps)
     threads = os.cpu_count() or 1
-    res = oracle.run(w, steps=steps, threads=threads)
+    temp = getattr(args, "sampling", None)
+    res = oracle.run(w, steps=steps, threads=threads, inv_temp=1.0 / temp if temp else 0.0)
     used = min(threads, w.B)
     per_thread = res.method_s / used
     return {"value": round(steps / per_thread, 3), "unit": UNIT, "cores": used, "kind": "oracle",
@@ -689,6 +714,8 @@ def main(argv=None):
     ap.add_argument("--cpu-steps", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sampling", type=float, default=None, metavar="T",
+                    help="verify by sampling (point-mass drafts) at temperature T instead of greedily")
     ap.add_argument("--sample-verify", action="store_true",
                     help="time the sampling verification (point-mass drafts) on --config's shapes, one JSON line")
     ap.add_argument("--sweep", action="store_true",
