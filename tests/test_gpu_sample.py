@@ -214,3 +214,43 @@ def test_bad_arguments_are_rejected():
         clk.verify_sample(x, blk, L, t, u, acc, em, out, small)
     with pytest.raises(ValueError):
         clk.verify_sample(x, blk, L, t.double(), u, acc, em, out, small)
+
+
+def test_fused_sampled_step_commits_and_rejects_invalid_requests():
+    """verify_sample_append commits each valid request's emitted tokens to
+    its history, and a request with an invalid length or temperature gets
+    the empty result, commits nothing and latches CLK_EINVAL."""
+    from workload import drive
+
+    w = wl.make_small("mixed", seed=81, B=6, V=2048, steps=4)
+    lk, slots = drive.make_lookup(w)
+    st = clk.Step(lk, slots)
+    head = torch.zeros((w.B, 7), dtype=torch.int32, device="cuda")
+    gen = wl.DevGen(w, device="cuda")
+    gen.head(0, head)
+    st.pre(head)
+    lg = gen.alloc_logits()
+    gen.logits(lg)
+    u = torch.zeros((w.B, 16, 2), dtype=torch.float32, device="cuda")
+    gen.uniforms(0, u)
+    length = st.length.clone()
+    length[1] = 0
+    t = torch.full((w.B,), 1.0, device="cuda")
+    t[4] = -1.0
+    before = [lk.history(int(s)).size for s in slots.tolist()]
+    scratch = clk.verify_sample_scratch(lg.dtype, w.V, w.B)
+    clk.verify_sample_append(lk, slots, lg, st.block, length, t, u, st.accept, st.emitted, st.out_tok, scratch)
+    torch.cuda.synchronize()
+    code, detail = lk.status()
+    assert code == clk.EINVAL and detail in (1, 4)
+    em = st.emitted.cpu().numpy()
+    out = st.out_tok.cpu().numpy()
+    after = [lk.history(int(s)) for s in slots.tolist()]
+    for b in range(w.B):
+        if b in (1, 4):
+            assert em[b] == 0 and (out[b] == SENT).all() and after[b].size == before[b]
+        else:
+            assert em[b] >= 1 and after[b].size == before[b] + em[b]
+            assert after[b][before[b]:].tolist() == out[b][:em[b]].tolist()
+    lk.status_clear()
+    assert lk.status()[0] == 0
