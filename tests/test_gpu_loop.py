@@ -100,6 +100,14 @@ def test_sampled_loop_full_size_mixed_batch():
     assert not msgs, "\n".join(msgs[:8])
 
 
+def test_maximum_batch_loop():
+    """The fused two-launch step at B = CLK_MAX_BATCH (8,192) requests with
+    short prompts, 3 steps, against the oracle (the fused verify's shared
+    memory then needs the large-allocation opt-in)."""
+    w = wl.make_small("mixed", seed=77, B=8192, V=64, L=(20, 60), steps=3)
+    _parity(w)
+
+
 def test_config0_tiny():
     _parity(wl.make("0"))
 

@@ -224,3 +224,25 @@ def test_fused_verify_results_do_not_depend_on_the_length_hint(hint):
         committed = want[3][b][:want[2][b]].tolist()
         assert lk.history(b).tolist() == [1] + committed
     assert lk.status()[0] == (clk.EINVAL if (L == 0).any() else 0)
+
+
+def test_maximum_batch():
+    """B = CLK_MAX_BATCH (8,192) requests: the stateless verify against the
+    oracle, and the static-scratch entry's limit (1,024 requests)."""
+    B, V = 8192, 64
+    rng = np.random.default_rng(88)
+    L = rng.integers(1, 17, size=B)
+    x = torch.randn((B, 16, V), generator=torch.Generator(device="cuda").manual_seed(88), device="cuda")
+    _check(x.to(torch.bfloat16).contiguous(), L, rng)
+    # the static entry takes up to 1,024 requests and refuses more, launching nothing
+    xb = x[:1025].to(torch.bfloat16).contiguous()
+    blk = torch.zeros((1025, 16), dtype=torch.int32, device="cuda")
+    ln = torch.full((1025,), 4, dtype=torch.int32, device="cuda")
+    z = lambda *s: torch.zeros(s, dtype=torch.int32, device="cuda")  # noqa: E731
+    g, a, e, out = z(1025, 16), z(1025), z(1025), z(1025, 16)
+    with pytest.raises(clk.ClkError) as err:
+        clk.verify_greedy_static(xb, blk, ln, g, a, e, out)
+    assert err.value.code == clk.ECAPACITY
+    clk.verify_greedy_static(xb[:1024], blk[:1024], ln[:1024], g[:1024], a[:1024], e[:1024], out[:1024])
+    torch.cuda.synchronize()
+    assert (e[:1024] >= 1).all()
