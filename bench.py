@@ -654,14 +654,31 @@ def run_cpu_baseline(args, w):
     steps = min(args.cpu_steps, w.steps)
     threads = os.cpu_count() or 1
     temp = getattr(args, "sampling", None)
-    res = oracle.run(w, steps=steps, threads=threads, inv_temp=1.0 / temp if temp else 0.0)
+    inv_temp = 1.0 / temp if temp else 0.0
+    res = oracle.run(w, steps=steps, threads=threads, inv_temp=inv_temp)
     used = min(threads, w.B)
     per_thread = res.method_s / used
+    # the same steps of every (B/8)-th request on one core, scaled to the whole batch
+    sub = list(range(0, w.B, max(1, w.B // 8)))
+    one = oracle.run(w, req_ids=sub, steps=steps, threads=1, inv_temp=inv_temp)
     return {"value": round(steps / per_thread, 3), "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"{w.B} requests x first {steps} steps of the same workload; full-scan lookup, copy, "
                       f"scheduler, fusion, argmax over every verified row, accept, append; host generation of "
                       f"the logit rows excluded ({res.provider_s / used:.2f} s/thread), wall incl. generation "
-                      f"{res.wall_s:.2f} s", "cpu": _cpu_model()}
+                      f"{res.wall_s:.2f} s", "cpu": _cpu_model(),
+            "us_per_request_step": _oracle_parts(res, w.B * steps),
+            "one_core": {"value": round(steps / (one.method_s * w.B / len(sub)), 3), "unit": UNIT, "cores": 1,
+                         "sample": f"requests {sub[0]}, {sub[1] if len(sub) > 1 else sub[0]}, ... ({len(sub)} of "
+                                   f"{w.B}) x first {steps} steps on one thread, scaled to {w.B} requests",
+                         "us_per_request_step": _oracle_parts(one, len(sub) * steps)}}
+
+
+def _oracle_parts(res, request_steps: int) -> dict:
+    """The oracle's time per request-step by component (thread time, us)."""
+    out = {k: round(getattr(res, k + "_s") * 1e6 / request_steps, 3)
+           for k in ("lookup", "sched_fuse", "verify")}
+    out["total"] = round(res.method_s * 1e6 / request_steps, 3)
+    return out
 
 
 def _cpu_model() -> str:
@@ -697,7 +714,8 @@ def run_reference(args, world, rank):
             "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}", "batch": w.B, "vocab": w.V},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
                              "sample": f"{w.B} requests x {W} warm-up + {K} timed steps, host generation of the "
-                                       f"logit rows excluded", "cpu": _cpu_model()},
+                                       f"logit rows excluded", "cpu": _cpu_model(),
+                             "us_per_request_step": _oracle_parts(res, w.B * K)},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 

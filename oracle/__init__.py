@@ -83,7 +83,8 @@ class RunArgs(ctypes.Structure):
                 ("rec_k", _P), ("rec_j", _P), ("rec_L", _P), ("rec_a", _P), ("rec_c", _P), ("rec_blk", _P),
                 ("rec_g", _P), ("hist_out", _P), ("hist_off", _P), ("hist_len", _P), ("counters", _P),
                 ("timed_from", ctypes.c_int32), ("pad", ctypes.c_int32),
-                ("method_ns", ctypes.c_int64), ("provider_ns", ctypes.c_int64)]
+                ("method_ns", ctypes.c_int64), ("provider_ns", ctypes.c_int64),
+                ("lookup_ns", ctypes.c_int64), ("sched_fuse_ns", ctypes.c_int64), ("verify_ns", ctypes.c_int64)]
 
 
 @lru_cache(maxsize=None)
@@ -234,7 +235,10 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     `workload` package (keyed by the original request ids).  `head`, if
     given, replaces the head proposals: a Python callable (b, t, n) -> 7
     tokens (small tests only: it runs under the GIL).  `timed_from`: the
-    first step counted in method_s / provider_s (per-thread sums).
+    first step counted in method_s / provider_s (per-thread sums); method_s
+    splits into lookup_s (suffix search + copy), sched_fuse_s (scheduler +
+    fusion) and verify_s (argmax or draw + accepted prefix), the small rest
+    being the history append and bookkeeping.
     `inv_temp` > 0 verifies by sampling (point-mass drafts) at that inverse
     temperature with the generator's uniforms; the records' `g` then holds
     each step's emitted tokens instead of the argmax rows."""
@@ -299,4 +303,6 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     histories = [hist[hoff[i]:hoff[i] + hlen[i]].copy() for i in range(n)]
     return RunResult(req_ids=req_ids, steps=steps, threads=threads, histories=histories,
                      counters=[counters[i].as_dict() for i in range(n)],
-                     method_s=args.method_ns * 1e-9, provider_s=args.provider_ns * 1e-9, wall_s=wall, **rec)
+                     method_s=args.method_ns * 1e-9, provider_s=args.provider_ns * 1e-9, wall_s=wall,
+                     lookup_s=args.lookup_ns * 1e-9, sched_fuse_s=args.sched_fuse_ns * 1e-9,
+                     verify_s=args.verify_ns * 1e-9, **rec)

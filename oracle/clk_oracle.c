@@ -374,6 +374,11 @@ typedef struct or_run_args {
     int32_t pad;
     int64_t method_ns;
     int64_t provider_ns;
+    /* the method's time split (timed steps, summed over threads):
+     * lookup + copy (full scan), scheduler + fusion, verification */
+    int64_t lookup_ns;
+    int64_t sched_fuse_ns;
+    int64_t verify_ns;
 } or_run_args;
 
 typedef struct or_shared {
@@ -390,7 +395,7 @@ static int64_t or_now_ns(void)
     return (int64_t)ts.tv_sec * 1000000000LL + ts.tv_nsec;
 }
 
-static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t* provider_ns)
+static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t* provider_ns, int64_t* part_ns)
 {
     const or_params* p = a->params;
     const int32_t b = a->req_ids[i];
@@ -424,13 +429,18 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
         }
         int32_t c[OR_BLOCK], m[OR_BLOCK], blk[OR_BLOCK], g[OR_BLOCK];
         int64_t j;
+        const int64_t p0 = or_now_ns();
         int32_t k = or_lookup(h, n, p->min_k, p->max_k, &j);
         or_copy(h, n, k, j, c);
+        const int64_t p1 = or_now_ns();
         int32_t L = or_sched(&st, k, prev_a, prev_L, p);
         int64_t u0 = or_now_ns();
         a->head_fn(a->gen_ctx, b, t, n, m);
-        prov += or_now_ns() - u0;
+        const int64_t head_ns = or_now_ns() - u0;
+        prov += head_ns;
         or_fuse(h[n - 1], c, k, m, L, p, blk);
+        const int64_t p2 = or_now_ns();
+        const int64_t prov_before_verify = prov;
         for (int32_t r = 0; r < OR_BLOCK; ++r) g[r] = OR_SENT;
         int32_t acc;
         if (sampling) {
@@ -450,6 +460,12 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
                                      : or_argmax_f32((const float*)row, a->V);
             }
             acc = or_accept(blk, g, L);
+        }
+        if (t >= a->timed_from) {
+            const int64_t p3 = or_now_ns();
+            part_ns[0] += p1 - p0;
+            part_ns[1] += (p2 - p1) - head_ns;
+            part_ns[2] += (p3 - p2) - (prov - prov_before_verify);
         }
         if (n + acc + 1 > cap) {
             rc = -2;
@@ -487,12 +503,13 @@ static void* or_worker(void* arg)
 {
     or_shared* sh = (or_shared*)arg;
     int64_t meth = 0, prov = 0;
+    int64_t part[3] = {0, 0, 0};
     for (;;) {
         pthread_mutex_lock(&sh->mu);
         int32_t i = sh->next++;
         pthread_mutex_unlock(&sh->mu);
         if (i >= sh->a->n_req) break;
-        int rc = or_run_request(sh->a, i, &meth, &prov);
+        int rc = or_run_request(sh->a, i, &meth, &prov, part);
         if (rc != 0) {
             pthread_mutex_lock(&sh->mu);
             if (sh->error == 0) sh->error = rc;
@@ -502,6 +519,9 @@ static void* or_worker(void* arg)
     pthread_mutex_lock(&sh->mu);
     sh->a->method_ns += meth;
     sh->a->provider_ns += prov;
+    sh->a->lookup_ns += part[0];
+    sh->a->sched_fuse_ns += part[1];
+    sh->a->verify_ns += part[2];
     pthread_mutex_unlock(&sh->mu);
     return NULL;
 }
@@ -516,6 +536,9 @@ int or_run(or_run_args* a)
     sh.error = 0;
     a->method_ns = 0;
     a->provider_ns = 0;
+    a->lookup_ns = 0;
+    a->sched_fuse_ns = 0;
+    a->verify_ns = 0;
     pthread_mutex_init(&sh.mu, NULL);
     int nt = a->threads < 1 ? 1 : a->threads;
     if (nt > a->n_req) nt = a->n_req < 1 ? 1 : a->n_req;

@@ -108,3 +108,15 @@ def test_generator_statistics():
     w0 = wl.make("0")
     h = w0.prompts[0]
     assert h.size == 2048
+
+
+def test_time_split_covers_the_method_time():
+    """The oracle's per-component times (lookup, scheduler + fusion, verify)
+    are non-negative, fit inside the method time, and leave only the small
+    append and bookkeeping rest uncounted."""
+    w = wl.make_small("mixed", seed=3, B=4, V=4096, L=(200, 400), steps=12)
+    res = oracle.run(w, threads=1, timed_from=2)
+    parts = (res.lookup_s, res.sched_fuse_s, res.verify_s)
+    assert all(x >= 0 for x in parts)
+    assert sum(parts) <= res.method_s + 1e-6
+    assert sum(parts) >= 0.5 * res.method_s
