@@ -48,7 +48,11 @@ namespace {
 constexpr int kSThreads = 256;
 constexpr int kSWarpsPerCta = kSThreads / 32;
 constexpr int kSUnroll = 4;
-constexpr int64_t kSegElems = 16384;  // elements per segment
+#ifndef CLK_SAMPLE_SEG
+#define CLK_SAMPLE_SEG 16384
+#endif
+constexpr int64_t kSegElems = CLK_SAMPLE_SEG;  // elements per segment
+static_assert(kSegElems % (8 * kSUnroll * kSThreads) == 0, "a segment is whole groups of vectors");
 
 struct SampleArgs {
     const void* logits;
@@ -223,18 +227,20 @@ __device__ __forceinline__ void ms_add_vec(MS& r, const uint4& v, float c)
     r.s += acc;
 }
 
-// Warp-wide merge in a fixed (butterfly) order; every lane gets the result.
+// Warp-wide merge: the largest m of the lanes, each lane's sum taken
+// against it, and the sums added in a fixed (butterfly) order.  Both
+// partners of every exchange add the same two numbers, so every lane gets
+// the same result.  A lane with s = 0 (no weight yet) adds nothing; its m is
+// -inf, so it does not raise the maximum either.
 __device__ __forceinline__ MS ms_warp(MS r)
 {
+    float m = r.m;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        MS q;
-        q.m = __shfl_xor_sync(0xFFFFFFFFu, r.m, o);
-        q.s = __shfl_xor_sync(0xFFFFFFFFu, r.s, o);
-        // the lower lane's pair first, so both lanes compute the same value
-        r = (threadIdx.x & o) ? ms_merge(q, r) : ms_merge(r, q);
-    }
-    return r;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float s = r.s == 0.0f ? 0.0f : r.s * ex2(r.m - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    return MS{m, s};
 }
 
 // Adds one value z = x * c.
