@@ -109,7 +109,7 @@ _SIGS = [
     ("clk_verify_sample", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
     ("clk_verify_sample_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
-                                                _P, _P, ctypes.c_size_t, _P]),
+                                                _P, _P, _P, ctypes.c_size_t, _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
     ("clk_status_clear", ctypes.c_int, [_P, _P]),
     ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
@@ -365,13 +365,15 @@ def verify_sample(logits, block, length, inv_temp, uniform, accept, emitted, out
 
 
 def verify_sample_append(h: Lookup, slots, logits, block, length, inv_temp, uniform, accept, emitted, out_tok,
-                         scratch, stream=None):
-    """Sampling verification fused with the token commit (clk_verify_sample_append)."""
+                         scratch, stream=None, length_hint=None):
+    """Sampling verification fused with the token commit (clk_verify_sample_append);
+    ``length_hint`` (int32 [B] or None) predicts the block lengths."""
     dt, rs, qs, V = _logits_args(logits)
     B = slots.numel()
     _check("clk_verify_sample_append",
            lib().clk_verify_sample_append(h.handle, _ptr(slots), logits.data_ptr(), dt, rs, qs, V, B,
                                           _ptr(block, shape=(B, BLOCK)), _ptr(length, shape=(B,)),
+                                          _ptr(length_hint, shape=(B,), name="length_hint"),
                                           _ptr(inv_temp, torch.float32, (B,), "inv_temp"),
                                           _ptr(uniform, torch.float32, (B, BLOCK, 2), "uniform"),
                                           _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
@@ -464,7 +466,8 @@ class Step:
     def post_sample(self, logits, inv_temp, uniform, stream=None):
         """Verify the block by sampling at inverse temperatures inv_temp
         (float32 [B]) with the uniforms uniform (float32 [B, 16, 2]), and
-        commit the emitted tokens."""
+        commit the emitted tokens.  Like ``post`` it passes the previous
+        step's lengths as the prediction of the new ones."""
         dt, rs, qs, V = _logits_args(logits)
         if logits.shape[0] != self.B or logits.shape[1] < self._rows:
             raise ValueError(f"logits must be [{self.B}, >= {self._rows}, V]")
@@ -475,7 +478,7 @@ class Step:
         sc = self._sscratch[1]
         _check("clk_verify_sample_append",
                self._lib.clk_verify_sample_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V,
-                                                  self.B, p["block"], self._lp[self._cur],
+                                                  self.B, p["block"], self._lp[self._cur], self._lp[self._cur ^ 1],
                                                   _ptr(inv_temp, torch.float32, (self.B,), "inv_temp"),
                                                   _ptr(uniform, torch.float32, (self.B, BLOCK, 2), "uniform"),
                                                   p["accept"], p["emitted"], p["out_tok"], sc.data_ptr(), sc.numel(),

@@ -51,6 +51,7 @@ constexpr int kSUnroll = 4;
 #ifndef CLK_SAMPLE_SEG
 #define CLK_SAMPLE_SEG 16384
 #endif
+
 constexpr int64_t kSegElems = CLK_SAMPLE_SEG;  // elements per segment
 static_assert(kSegElems % (8 * kSUnroll * kSThreads) == 0, "a segment is whole groups of vectors");
 
@@ -63,6 +64,7 @@ struct SampleArgs {
     int32_t S;            // segments per row
     const int32_t* block;
     const int32_t* len;
+    const int32_t* len_hint;  // fused: predicted block lengths (may be null)
     const float* inv_temp;  // [B]
     const float* uniform;   // [B][16][2]
     int32_t* accept;
@@ -254,15 +256,15 @@ __device__ __forceinline__ void ms_add1(MS& r, float x, float c)
     if (r.m != -INFINITY) r.s += ex2(fmaf(x, c, -r.m));
 }
 
-// P[b] = rows of requests b' < b; P[B] = total.  Block-wide.
-__device__ __forceinline__ void sample_prefix(const SampleArgs& a, int32_t* P, int32_t* sm_warp)
+// P[b] = rows(b') summed over requests b' < b; P[B] = total.  Block-wide.
+template <typename Rows>
+__device__ __forceinline__ void rows_prefix(int32_t B, Rows rows, int32_t* P, int32_t* sm_warp)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int32_t B = a.B;
     const int32_t per = (B + kSThreads - 1) / kSThreads;
     const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) local += sample_rows(a, b);
+    for (int32_t b = b0; b < b1; ++b) local += rows(b);
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -284,10 +286,16 @@ __device__ __forceinline__ void sample_prefix(const SampleArgs& a, int32_t* P, i
     int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
         P[b] = run;
-        run += sample_rows(a, b);
+        run += rows(b);
     }
     if (tid == kSThreads - 1) P[B] = sm_warp[kSWarpsPerCta - 1];
     __syncthreads();
+}
+
+// P[b] = rows of requests b' < b; P[B] = total.  Block-wide.
+__device__ __forceinline__ void sample_prefix(const SampleArgs& a, int32_t* P, int32_t* sm_warp)
+{
+    rows_prefix(a.B, [&a](int32_t b) { return sample_rows(a, b); }, P, sm_warp);
 }
 
 // Largest b with P[b] <= ri.
@@ -309,14 +317,14 @@ __device__ __forceinline__ float2* part_of(const SampleArgs& a, int32_t b, int32
 // Segment k (flat) of request b: the row's first byte and the segment's
 // range in units (vectors on the vector path, elements otherwise).
 template <int DT, bool VEC>
-__device__ __forceinline__ void seg_range(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k,
+__device__ __forceinline__ void seg_range(const SampleArgs& a, const int32_t* P, int32_t b, int32_t roff, int64_t k,
                                           const char*& row, int32_t& u0, int32_t& u1, int32_t& r, int32_t& sg)
 {
     using E = SElem<DT>;
     constexpr int W = VEC ? E::W : 1;
     const int64_t ri = k / a.S;
     sg = (int32_t)(k - ri * a.S);
-    r = (int32_t)(ri - P[b]);
+    r = roff + (int32_t)(ri - P[b]);
     row = static_cast<const char*>(a.logits) +
           ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(typename E::T);
     const int64_t e0 = (int64_t)sg * kSegElems, e1 = min(e0 + kSegElems, (int64_t)a.V);
@@ -324,13 +332,15 @@ __device__ __forceinline__ void seg_range(const SampleArgs& a, const int32_t* P,
     u1 = (int32_t)(e1 / W);
 }
 
-// Streams segments [k0, k1) of request b and stores one (m, s) pair per
+// Streams segments [k0, k1) of request b (flat segment k is segment k % S of
+// the request's row roff + k / S - P[b]) and stores one (m, s) pair per
 // segment and warp.  Vector path: two groups of kSUnroll 16-byte loads per
 // thread alternate, and the next segment's first group is issued before the
 // current segment's last group is reduced.  The segment and row advance
 // incrementally (segments of a request are consecutive: row-major).
 template <int DT>
-__device__ __forceinline__ void stream_vec(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k0, int64_t k1)
+__device__ __forceinline__ void stream_vec(const SampleArgs& a, const int32_t* P, int32_t b, int32_t roff, int64_t k0,
+                                           int64_t k1)
 {
     using E = SElem<DT>;
     constexpr int32_t SV = (int32_t)(kSegElems / E::W);  // vectors per full segment
@@ -342,7 +352,7 @@ __device__ __forceinline__ void stream_vec(const SampleArgs& a, const int32_t* P
     const uint4* req = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
                                                      (int64_t)b * a.req_stride * (int64_t)sizeof(typename E::T));
     const int64_t ri0 = k0 / a.S;
-    int32_t r = (int32_t)(ri0 - P[b]);
+    int32_t r = roff + (int32_t)(ri0 - P[b]);
     int32_t sg = (int32_t)(k0 - ri0 * a.S);
     int32_t left = (int32_t)(k1 - k0);  // segments still to finish, the current one included
     // current group: row `row`, vectors [g, g + G) of segment sg (which ends at e)
@@ -410,8 +420,8 @@ __device__ __forceinline__ void stream_vec(const SampleArgs& a, const int32_t* P
 
 // Scalar path (rows not 16-byte aligned): one segment at a time.
 template <int DT>
-__device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k0,
-                                              int64_t k1)
+__device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t* P, int32_t b, int32_t roff,
+                                              int64_t k0, int64_t k1)
 {
     using E = SElem<DT>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -419,7 +429,7 @@ __device__ __forceinline__ void stream_scalar(const SampleArgs& a, const int32_t
     for (int64_t k = k0; k < k1; ++k) {
         const char* rowp;
         int32_t u0, u1, r, sg;
-        seg_range<DT, false>(a, P, b, k, rowp, u0, u1, r, sg);
+        seg_range<DT, false>(a, P, b, roff, k, rowp, u0, u1, r, sg);
         const typename E::T* row = reinterpret_cast<const typename E::T*>(rowp);
         MS run = ms_empty();
         for (int32_t i = u0 + tid; i < u1; i += kSThreads) ms_add1(run, E::value(row[i]), c);
@@ -674,32 +684,23 @@ __device__ __noinline__ void sample_finish(const SampleArgs& a, const LookupDev&
     }
 }
 
-template <int DT, bool VEC, bool FUSED>
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArgs a, LookupDev Ldev)
 {
     extern __shared__ int32_t P[];  // B + 1
     __shared__ int32_t sm_warp[kSWarpsPerCta];
     __shared__ int32_t sm_last;
     __shared__ FinSmem fs;
-    if (FUSED) {
-        // Launched as a programmatic dependent of the proposal launch, whose
-        // blocks and lengths it reads: let the next launch be scheduled,
-        // then wait for the proposal to complete.
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-    }
     const int tid = threadIdx.x;
     const int32_t B = a.B;
     sample_prefix(a, P, sm_warp);
-    // Requests with no rows (invalid length or temperature): empty result
-    // (fused: an error, nothing committed).
+    // Requests with no rows (invalid length or temperature): empty result.
     if (blockIdx.x == 0) {
         for (int32_t b = tid; b < B; b += kSThreads) {
             if (sample_rows(a, b) != 0) continue;
             for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
             a.accept[b] = 0;
             a.emitted[b] = 0;
-            if (FUSED) latch(Ldev.status, CLK_EINVAL, b);
         }
     }
     const int64_t S = a.S;
@@ -710,8 +711,8 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
     while (k < hi) {
         const int32_t b = sample_owner(P, B, k / S);
         const int64_t k1 = min(hi, (int64_t)P[b + 1] * S);
-        if (VEC) stream_vec<DT>(a, P, b, k, k1);
-        else stream_scalar<DT>(a, P, b, k, k1);
+        if (VEC) stream_vec<DT>(a, P, b, 0, k, k1);
+        else stream_scalar<DT>(a, P, b, 0, k, k1);
         __syncthreads();  // every warp's pairs are stored
         if (tid == 0) {
             __threadfence();
@@ -720,8 +721,168 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
             sm_last = atomicAdd(a.done + b, n) + n == need;
         }
         __syncthreads();
-        if (sm_last) sample_finish<DT, FUSED>(a, Ldev, b, fs);
+        if (sm_last) sample_finish<DT, false>(a, Ldev, b, fs);
         k = k1;
+    }
+}
+
+// The sampler fused with the commit (clk_verify_sample_append), launched as
+// a programmatic dependent of the proposal launch that produces the blocks
+// and lengths.  As in the fused greedy verification, it first streams the
+// segments of every request's predicted rows, max(1 + head, hint) (the
+// short block when the hint is missing or not a valid length), while the
+// proposal launch may still run; the counts of those segments are kept and
+// decided after the wait, when the lengths are known.  Each CTA streams its
+// even share of the predicted segments in two halves with the wait between
+// them; after the wait it also streams its share of the rows the prediction
+// missed.  A request's total is max(predicted, L_b) rows of segments; the
+// count that reaches it finishes the request (pairs of rows past L_b are
+// never used).  A request with a valid temperature but an invalid length
+// streams its predicted rows for nothing: the count that completes it only
+// sets the counter back to zero.  The inverse temperatures are read before
+// the wait, so they must not come from the proposal launch.
+constexpr int kSMaxDefer = 32;
+constexpr int64_t kSSplitMin = 4;  // segments: shares below this are not split
+
+// The block's next action, chosen by thread 0.
+enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
+
+struct SampleStepSmem {
+    int64_t k, kend;          // the current phase's next segment and end (flat)
+    int64_t kstop, hi1;       // where the first phase stopped; the end of this CTA's predicted share
+    int64_t c0, c1;           // the piece to stream: segments [c0, c1) of request cb,
+    int32_t cb, croff;        // rows counted from croff
+    int32_t phase, act;
+    int32_t db[kSMaxDefer];   // kept counts: request,
+    uint32_t dc[kSMaxDefer];  // and the count its addition returned
+    int32_t nd, ci;           // kept counts, and how many of them are decided
+};
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(SampleArgs a, LookupDev Ldev)
+{
+    extern __shared__ int32_t sm_p[];  // P1[B + 1] (predicted rows), then P2[B + 1] (missed rows)
+    __shared__ int32_t sm_warp[kSWarpsPerCta];
+    __shared__ FinSmem fs;
+    __shared__ SampleStepSmem ss;
+    // Let the next launch (the next proposal) be scheduled; it waits for
+    // this grid to complete before it reads anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    const int32_t B = a.B;
+    int32_t* P1 = sm_p;
+    int32_t* P2 = sm_p + (B + 1);
+    const int32_t base = min(kBlock, 1 + Ldev.p.head);
+    rows_prefix(B, [&a, base](int32_t b) {
+        if (!temp_valid(a.inv_temp[b])) return 0;
+        const int32_t h = a.len_hint != nullptr ? a.len_hint[b] : 0;
+        return len_valid(h) ? max(h, base) : base;
+    }, P1, sm_warp);
+    if (tid == 0) {
+        const int64_t n = (int64_t)P1[B] * a.S;
+        const int64_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
+        ss.k = lo;
+        ss.kend = (hi - lo >= kSSplitMin) ? lo + (hi - lo) / 2 : hi;
+        ss.hi1 = hi;
+        ss.phase = 0;
+        ss.nd = 0;
+        ss.ci = 0;
+    }
+    // Phase 0: the first half of this CTA's predicted segments, counts kept
+    // (stopping early if the list of kept counts is full); the wait; phase
+    // 1: this CTA's share of the missed rows; phase 2: the rest of its
+    // predicted segments.  After the wait every kept count is decided: the
+    // one that equals its request's total (max(predicted, L_b) rows of
+    // segments) finishes the request, or, for an invalid length, only
+    // rewinds its counter.
+    for (;;) {
+        if (tid == 0) {
+            int32_t act = kActDone;
+            for (;;) {
+                if (ss.phase > 0 && ss.ci < ss.nd) {
+                    act = kActCheck;
+                    break;
+                }
+                if (ss.phase > 0) ss.ci = ss.nd = 0;
+                if (ss.k < ss.kend && !(ss.phase == 0 && ss.nd == kSMaxDefer)) {
+                    const int32_t* P = ss.phase == 1 ? P2 : P1;
+                    const int32_t b = sample_owner(P, B, ss.k / a.S);
+                    ss.cb = b;
+                    ss.c0 = ss.k;
+                    ss.c1 = min(ss.kend, (int64_t)P[b + 1] * a.S);
+                    ss.croff = ss.phase == 1 ? P1[b + 1] - P1[b] : 0;
+                    act = kActStream;
+                    break;
+                }
+                if (ss.phase == 0) {
+                    ss.kstop = ss.k;
+                    act = kActWait;
+                    break;
+                }
+                if (ss.phase == 1) {
+                    ss.phase = 2;
+                    ss.k = ss.kstop;
+                    ss.kend = ss.hi1;
+                    continue;
+                }
+                break;
+            }
+            ss.act = act;
+        }
+        __syncthreads();
+        const int32_t act = ss.act;
+        if (act == kActDone) break;
+        if (act == kActStream) {
+            const int32_t b = ss.cb;
+            const int32_t* P = ss.phase == 1 ? P2 : P1;
+            if (VEC) stream_vec<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
+            else stream_scalar<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
+            __syncthreads();  // every warp's pairs are stored
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t c = (uint32_t)(ss.c1 - ss.c0);
+                ss.db[ss.nd] = b;
+                ss.dc[ss.nd] = atomicAdd(a.done + b, c) + c;
+                ss.nd += 1;
+                ss.k = ss.c1;
+            }
+        } else if (act == kActCheck) {
+            const int32_t b = ss.db[ss.ci];
+            const int32_t Lb = __ldcg(a.len + b);
+            const int32_t pr = P1[b + 1] - P1[b];
+            const uint32_t total = (uint32_t)((pr > 0 && len_valid(Lb)) ? max(pr, Lb) : pr) * (uint32_t)a.S;
+            if (ss.dc[ss.ci] == total) {
+                if (len_valid(Lb)) sample_finish<DT, true>(a, Ldev, b, fs);
+                else if (tid == 0) a.done[b] = 0u;
+            }
+            __syncthreads();
+            if (tid == 0) ss.ci += 1;
+        } else {  // kActWait
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            rows_prefix(B, [&a, P1](int32_t b) {
+                const int32_t pr = P1[b + 1] - P1[b];
+                const int32_t Lb = __ldcg(a.len + b);
+                return (pr > 0 && len_valid(Lb)) ? max(0, Lb - pr) : 0;
+            }, P2, sm_warp);
+            // Requests with no rows (invalid length or temperature): the
+            // empty result, nothing committed, an error.
+            if (blockIdx.x == 0) {
+                for (int32_t b = tid; b < B; b += kSThreads) {
+                    if (sample_rows(a, b) != 0) continue;
+                    for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
+                    a.accept[b] = 0;
+                    a.emitted[b] = 0;
+                    latch(Ldev.status, CLK_EINVAL, b);
+                }
+            }
+            if (tid == 0) {
+                const int64_t n = (int64_t)P2[B] * a.S;
+                ss.k = n * blockIdx.x / gridDim.x;
+                ss.kend = n * (blockIdx.x + 1) / gridDim.x;
+                ss.phase = 1;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -742,8 +903,8 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     static int cache[64] = {0};  // resident CTAs per SM, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
-    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
-    auto kern = k_sample<DT, VEC, FUSED>;
+    const size_t smem = (size_t)(FUSED ? 2 : 1) * (a.B + 1) * sizeof(int32_t);
+    auto kern = FUSED ? k_sample_step<DT, VEC> : k_sample<DT, VEC>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CLK_ECUDA;
@@ -793,7 +954,7 @@ namespace {
 // Checks and launches both entry points; h == nullptr: stateless.
 int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype, int64_t row_stride,
                  int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
-                 const float* d_inv_temp, const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
+                 const int32_t* d_len_hint, const float* d_inv_temp, const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
                  int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs)
 {
     int32_t S = 0;
@@ -812,6 +973,7 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
         d_inv_temp == nullptr || !aligned(d_inv_temp, 4) || d_uniform == nullptr || !aligned(d_uniform, 4))
         return CLK_EINVAL;
     if (d_scratch == nullptr || !aligned(d_scratch, 16) || scratch_bytes < need) return CLK_EINVAL;
+    if (d_len_hint != nullptr && !aligned(d_len_hint, 4)) return CLK_EINVAL;
     if (B == 0) return CLK_OK;
     SampleArgs a;
     a.logits = d_logits;
@@ -822,6 +984,7 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     a.S = S;
     a.block = d_block;
     a.len = d_len;
+    a.len_hint = d_len_hint;
     a.inv_temp = d_inv_temp;
     a.uniform = d_uniform;
     a.accept = d_accept;
@@ -855,17 +1018,20 @@ extern "C" int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t ro
                                  int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
                                  clk_stream_t s)
 {
-    return sample_entry(nullptr, nullptr, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_inv_temp,
-                        d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, (cudaStream_t)s);
+    return sample_entry(nullptr, nullptr, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, nullptr,
+                        d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
+                        (cudaStream_t)s);
 }
 
 extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                                         int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
-                                        const int32_t* d_block, const int32_t* d_len, const float* d_inv_temp,
-                                        const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
-                                        int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, clk_stream_t s)
+                                        const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
+                                        const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                        int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch,
+                                        size_t scratch_bytes, clk_stream_t s)
 {
     if (h == nullptr) return CLK_EINVAL;
-    return sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_inv_temp,
-                        d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, (cudaStream_t)s);
+    return sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_len_hint,
+                        d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
+                        (cudaStream_t)s);
 }

@@ -362,18 +362,26 @@ CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_s
  * next proposal call on the slot.  The results equal those of the two
  * calls.  The launch is a programmatic dependent of the preceding launch on
  * the stream, and d_block / d_len may come from that launch
- * (clk_propose_fuse_sched): it waits for it before reading them.  The
- * logits, inverse temperatures and uniforms must be complete when the call
- * is made.  A request with an invalid length or temperature gets the empty
- * result, commits nothing and latches CLK_EINVAL in the handle's status (as
- * do a bad slot, an out-of-vocabulary token or a full history, which
- * clk_lookup_append would reject).  Scratch as for clk_verify_sample; calls
- * sharing it must not overlap on the GPU. */
+ * (clk_propose_fuse_sched).  As in clk_verify_append, it first reads the
+ * rows of a predicted length of every request with a valid temperature:
+ * max(1 + head, d_len_hint[b]) when the hint is a valid length, else
+ * 1 + head; after waiting for that launch it reads the rows the prediction
+ * missed.  d_len_hint (nullable, e.g. the previous step's lengths in a
+ * buffer the preceding launch does not write) is only a prediction: any
+ * value gives the same results.  So the logits (every predicted row; 16
+ * rows per request serve any hint), the inverse temperatures and the
+ * uniforms must be complete when the call is made.  A request with an
+ * invalid length or temperature gets the empty result, commits nothing and
+ * latches CLK_EINVAL in the handle's status (as do a bad slot, an
+ * out-of-vocabulary token or a full history, which clk_lookup_append would
+ * reject).  Scratch as for clk_verify_sample; calls sharing it must not
+ * overlap on the GPU. */
 CLK_API int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                                      int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
-                                     const int32_t* d_block, const int32_t* d_len, const float* d_inv_temp,
-                                     const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
-                                     int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, clk_stream_t s);
+                                     const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
+                                     const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                     int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                                     clk_stream_t s);
 
 /* ---------------------------------------------------------------------- */
 /* Status, counters, inspection (these synchronise the stream)             */

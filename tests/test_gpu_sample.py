@@ -216,6 +216,48 @@ def test_bad_arguments_are_rejected():
         clk.verify_sample(x, blk, L, t.double(), u, acc, em, out, small)
 
 
+@pytest.mark.parametrize("hint", ["none", "short", "long", "exact", "garbage"])
+def test_fused_sampler_results_do_not_depend_on_the_length_hint(hint):
+    """clk_verify_sample_append streams the rows of a predicted length before
+    the preceding launch has finished; the prediction changes only what is
+    read early.  Every segment's pairs and the finisher's fixed-order
+    combination are the same whichever CTA reads a row, so the outputs equal
+    the stateless sampler's bit for bit (which is checked against the oracle
+    here too), and each valid request commits exactly its emitted tokens."""
+    B, V = 40, 4096
+    x, blk, L, t, u = _case(B, V, torch.bfloat16, seed=90)
+    L[::7] = 0  # invalid lengths and temperatures take the empty result
+    t[3] = 0.0
+    want_acc, want_out = _check(x, blk, L, t, u)
+    rng = np.random.default_rng(90)
+    hints = {"none": None, "short": np.full(B, 8), "long": np.full(B, 16), "exact": L.cpu().numpy(),
+             "garbage": rng.integers(-5, 40, size=B)}
+    h = hints[hint]
+    lk = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+    s = torch.arange(B, dtype=torch.int32, device="cuda")
+    clk.lookup_init(lk, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                    torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+    acc = torch.full((B,), 77, dtype=torch.int32, device="cuda")
+    em, out = torch.full_like(acc, 77), torch.full((B, 16), 77, dtype=torch.int32, device="cuda")
+    scratch = clk.verify_sample_scratch(x.dtype, V, B)
+    hint_t = None if h is None else torch.from_numpy(np.asarray(h, np.int32)).cuda()
+    clk.verify_sample_append(lk, s, x, blk, L, t, u, acc, em, out, scratch, length_hint=hint_t)
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), want_acc)
+    assert np.array_equal(out.cpu().numpy(), want_out)
+    emn, outn = em.cpu().numpy(), out.cpu().numpy()
+    for b in range(B):
+        assert lk.history(b).tolist() == [1] + outn[b][:emn[b]].tolist(), b
+    assert lk.status()[0] == clk.EINVAL
+    # the counters were rewound: the same call again gives the same answer
+    lk2 = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+    clk.lookup_init(lk2, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                    torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+    clk.verify_sample_append(lk2, s, x, blk, L, t, u, acc, em, out, scratch, length_hint=hint_t)
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), want_acc) and np.array_equal(out.cpu().numpy(), want_out)
+
+
 def test_fused_sampled_step_commits_and_rejects_invalid_requests():
     """verify_sample_append commits each valid request's emitted tokens to
     its history, and a request with an invalid length or temperature gets
