@@ -161,8 +161,9 @@ def _ptr(t: Optional[torch.Tensor], dtype=torch.int32, shape=None, name="tensor"
 
 
 def _logits_args(logits: torch.Tensor):
-    if not logits.is_cuda or logits.dim() != 3:
-        raise ValueError("logits must be a CUDA tensor [B, rows, V]")
+    # a CUDA tensor, or a pinned host tensor that the kernels read in place
+    if not (logits.is_cuda or logits.is_pinned()) or logits.dim() != 3:
+        raise ValueError("logits must be a CUDA tensor or a pinned host tensor [B, rows, V]")
     if logits.dtype == torch.bfloat16:
         dt = BF16
     elif logits.dtype == torch.float32:

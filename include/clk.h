@@ -33,6 +33,12 @@
  *   owned by the caller (e.g. PyTorch tensors) and passed as a plain device
  *   pointer ("d_" prefix) or host pointer ("h_" prefix).  Integer arrays are
  *   int32, C-contiguous, 4-byte aligned, with the shapes given below.
+ * - Logits: d_logits of the verify entry points may also point into
+ *   page-locked host memory (cudaHostAlloc / cudaMallocHost, or
+ *   cudaHostRegister'ed), which unified addressing lets kernels load from
+ *   with the same pointer.  The kernels then read the rows they verify in
+ *   place over the host link, and only those rows: no staging copy of the
+ *   whole [B, rows, V] array.  Results are identical to device logits.
  * - Requests are addressed by slot (0 <= slot < max_slots).  A batch is a
  *   device array d_slots[B] of distinct slots; per-request arrays of the
  *   call are indexed by batch position b, not by slot.

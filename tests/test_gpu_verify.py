@@ -246,3 +246,49 @@ def test_maximum_batch():
     clk.verify_greedy_static(xb[:1024], blk[:1024], ln[:1024], g[:1024], a[:1024], e[:1024], out[:1024])
     torch.cuda.synchronize()
     assert (e[:1024] >= 1).all()
+
+
+@pytest.mark.parametrize("V", [5000, 5003])  # the 16-byte vector path and the scalar path
+def test_pinned_host_logits_are_read_in_place(V):
+    """Logits in pinned host memory: the stateless and fused greedy verifies
+    and the sampler load them in place (unified addressing) and give exactly
+    the results of the same logits in device memory, the oracle's for the
+    greedy ones."""
+    rng = np.random.default_rng(12)
+    B = 24
+    x = torch.from_numpy(rng.integers(-30, 30, size=(B, 16, V)).astype(np.float32)).to(torch.bfloat16)
+    xd, xh = x.cuda(), x.pin_memory()
+    L = rng.integers(1, 17, size=B).astype(np.int32)
+    block = _blocks_from(_np_view(x), L, rng, p_agree=0.85)
+    want = _oracle_rows(_np_view(x), block, L)
+    bd, Ld = torch.from_numpy(block).cuda(), torch.from_numpy(L).cuda()
+    z = lambda *sh: torch.full(sh, 77, dtype=torch.int32, device="cuda")  # noqa: E731
+    for src in (xd, xh):
+        g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+        clk.verify_greedy(src, bd, Ld, g, a, e, out, clk.verify_scratch(B))
+        torch.cuda.synchronize()
+        for name, gg, ww in zip(("argmax", "accept", "emitted", "out_tok"), (g, a, e, out), want):
+            assert np.array_equal(gg.cpu().numpy(), ww), (name, src.is_cuda)
+    s = torch.arange(B, dtype=torch.int32, device="cuda")
+    hist = []
+    for src in (xd, xh):
+        lk = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+        clk.lookup_init(lk, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                        torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+        g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+        clk.verify_append(lk, s, src, bd, Ld, g, a, e, out, length_hint=torch.full_like(Ld, 8))
+        torch.cuda.synchronize()
+        for name, gg, ww in zip(("argmax", "accept", "emitted", "out_tok"), (g, a, e, out), want):
+            assert np.array_equal(gg.cpu().numpy(), ww), (name, "fused", src.is_cuda)
+        hist.append([lk.history(b).tolist() for b in range(B)])
+    assert hist[0] == hist[1]
+    t = torch.full((B,), 1.5, device="cuda")
+    u = torch.rand((B, 16, 2), generator=torch.Generator(device="cuda").manual_seed(12), device="cuda")
+    res = []
+    for src in (xd, xh):
+        a, e, out = z(B), z(B), z(B, 16)
+        clk.verify_sample(src, bd, Ld, t, u, a, e, out, clk.verify_sample_scratch(x.dtype, V, B))
+        torch.cuda.synchronize()
+        res.append((a.cpu().numpy(), e.cpu().numpy(), out.cpu().numpy()))
+    for p, q in zip(*res):
+        assert np.array_equal(p, q)
