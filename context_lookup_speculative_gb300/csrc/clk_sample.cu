@@ -51,7 +51,6 @@ constexpr int kSUnroll = 4;
 #ifndef CLK_SAMPLE_SEG
 #define CLK_SAMPLE_SEG 16384
 #endif
-
 constexpr int64_t kSegElems = CLK_SAMPLE_SEG;  // elements per segment
 static_assert(kSegElems % (8 * kSUnroll * kSThreads) == 0, "a segment is whole groups of vectors");
 
@@ -733,16 +732,14 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
 // short block when the hint is missing or not a valid length), while the
 // proposal launch may still run; the counts of those segments are kept and
 // decided after the wait, when the lengths are known.  Each CTA streams its
-// even share of the predicted segments in two halves with the wait between
-// them; after the wait it also streams its share of the rows the prediction
-// missed.  A request's total is max(predicted, L_b) rows of segments; the
+// even share of the predicted segments, waits, and then streams its share of
+// the rows the prediction missed.  A request's total is max(predicted, L_b) rows of segments; the
 // count that reaches it finishes the request (pairs of rows past L_b are
 // never used).  A request with a valid temperature but an invalid length
 // streams its predicted rows for nothing: the count that completes it only
 // sets the counter back to zero.  The inverse temperatures are read before
 // the wait, so they must not come from the proposal launch.
 constexpr int kSMaxDefer = 32;
-constexpr int64_t kSSplitMin = 4;  // segments: shares below this are not split
 
 // The block's next action, chosen by thread 0.
 enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
@@ -782,19 +779,21 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
         const int64_t n = (int64_t)P1[B] * a.S;
         const int64_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
         ss.k = lo;
-        ss.kend = (hi - lo >= kSSplitMin) ? lo + (hi - lo) / 2 : hi;
+        ss.kend = hi;
         ss.hi1 = hi;
         ss.phase = 0;
         ss.nd = 0;
         ss.ci = 0;
     }
-    // Phase 0: the first half of this CTA's predicted segments, counts kept
-    // (stopping early if the list of kept counts is full); the wait; phase
-    // 1: this CTA's share of the missed rows; phase 2: the rest of its
-    // predicted segments.  After the wait every kept count is decided: the
-    // one that equals its request's total (max(predicted, L_b) rows of
-    // segments) finishes the request, or, for an invalid length, only
-    // rewinds its counter.
+    // Phase 0: this CTA's predicted segments, counts kept (stopping early if
+    // the list of kept counts is full); the wait; phase 1: its share of the
+    // missed rows; phase 2: whatever phase 0 left.  After the wait every
+    // kept count is decided: the one that equals its request's total
+    // (max(predicted, L_b) rows of segments) finishes the request, or, for
+    // an invalid length, only rewinds its counter.  The wait comes after the
+    // whole predicted share: a request completes only once all of its
+    // segments are read, so its finisher runs at the end whatever the order,
+    // and a wait in the middle would pause every CTA at about the same time.
     for (;;) {
         if (tid == 0) {
             int32_t act = kActDone;
