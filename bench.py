@@ -589,6 +589,39 @@ def run_lookup_ablation(lk, slots, w, device, reps: int = 20):
     return res
 
 
+ABLATION_SWEEP_B = (1, 64)
+ABLATION_SWEEP_L = (1024, 4096, 16384, 65536, 262144)
+
+
+def run_ablation_sweep(args, world, rank, local):
+    """Where the incremental index overtakes the full history scan: for each
+    batch size and history length, a lookup holding that many synthetic
+    prompt tokens per request (the mixed recipe; its index built at
+    ingestion), the proposal by the index and by the GPU full scan timed
+    from the same state, and whether their answers are identical."""
+    import torch
+
+    import workload as wl
+    from workload import drive
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    rows = []
+    for B in ABLATION_SWEEP_B:
+        for L in ABLATION_SWEEP_L:
+            w = wl.make_small("mixed", seed=700 + B, B=B, V=32000, L=(L, L), steps=1)
+            lk, slots = drive.make_lookup(w, device=device)
+            r = run_lookup_ablation(lk, slots, w, device)
+            rows.append({"batch": B, "history": L, "index_us": r["gpu_index_us"], "scan_us": r["gpu_scan_us"],
+                         "answers_identical": r["answers_identical"]})
+            del lk
+            torch.cuda.empty_cache()
+    if not all(r["answers_identical"] for r in rows):
+        raise RuntimeError("ablation sweep: the index and the full scan disagree")
+    return {"metric": "proposal latency: incremental index vs full history scan", "unit": "us per batch step",
+            "data": "synthetic", "rows": rows}
+
+
 def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
     """Same metric through the public API with host buffers.  Each step copies
     its head proposals from pinned host memory, runs the two launches on the
@@ -769,6 +802,8 @@ def main(argv=None):
                     help="time the sampling verification (point-mass drafts) on --config's shapes, one JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="block-size and sticky variants of the measured step on --config, one JSON line")
+    ap.add_argument("--ablation-sweep", action="store_true",
+                    help="the index lookup against the full history scan over batch sizes and history lengths")
     ap.add_argument("--ablation", action="store_true",
                     help="also time the proposal by index vs by full history scan (GPU and CPU oracle)")
     args = ap.parse_args(argv)
@@ -787,6 +822,8 @@ def main(argv=None):
             out = run_sample_verify(args, world, rank, local, dist)
         elif args.sweep:
             out = run_sweep(args, world, rank, local, dist)
+        elif args.ablation_sweep:
+            out = run_ablation_sweep(args, world, rank, local)
         else:
             out = run_ours(args, world, rank, local, dist)
         if rank == 0:
