@@ -566,11 +566,13 @@ def run_lookup_ablation(lk, slots, w, device, reps: int = 20):
 
     B = w.B
     z = lambda *sh: torch.zeros(sh, dtype=torch.int32, device=device)  # noqa: E731
-    outs = {m: (z(B, 16), z(B), z(B)) for m in ("index", "scan")}
+    outs = {m: (z(B, 16), z(B), z(B)) for m in ("index", "scan", "scan_one_cta")}
     clk.lookup_propose(lk, slots, *outs["index"])  # indexes the last step's tokens first
     torch.cuda.synchronize()
     res = {}
-    for mode, fn in (("index", clk.lookup_propose), ("scan", clk.lookup_propose_scan)):
+    # the grid-wide scan, and the pages' form: one CTA per request
+    scan1 = lambda *a: clk.lookup_propose_scan(*a, ctas_per_request=1)  # noqa: E731
+    for mode, fn in (("index", clk.lookup_propose), ("scan", clk.lookup_propose_scan), ("scan_one_cta", scan1)):
         fn(lk, slots, *outs[mode])
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -582,7 +584,8 @@ def run_lookup_ablation(lk, slots, w, device, reps: int = 20):
         res[f"gpu_{mode}_us"] = round(a.elapsed_time(b) * 1e3 / reps, 3)
     lens = [lk.slot_info(int(s))["n"] for s in slots.tolist()]
     res.update({
-        "answers_identical": all(torch.equal(x, y) for x, y in zip(outs["index"], outs["scan"])),
+        "answers_identical": all(torch.equal(x, y) and torch.equal(x, y1)
+                                 for x, y, y1 in zip(outs["index"], outs["scan"], outs["scan_one_cta"])),
         "history_tokens_mean": int(np.mean(lens)),
         "batch": B,
     })
@@ -613,7 +616,7 @@ def run_ablation_sweep(args, world, rank, local):
             lk, slots = drive.make_lookup(w, device=device)
             r = run_lookup_ablation(lk, slots, w, device)
             rows.append({"batch": B, "history": L, "index_us": r["gpu_index_us"], "scan_us": r["gpu_scan_us"],
-                         "answers_identical": r["answers_identical"]})
+                         "scan_one_cta_us": r["gpu_scan_one_cta_us"], "answers_identical": r["answers_identical"]})
             del lk
             torch.cuda.empty_cache()
     if not all(r["answers_identical"] for r in rows):

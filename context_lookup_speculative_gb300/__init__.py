@@ -93,7 +93,7 @@ _SIGS = [
     ("clk_lookup_init", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_append", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_propose", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
-    ("clk_lookup_propose_scan", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
+    ("clk_lookup_propose_scan", ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P, _P]),
     ("clk_sched_step", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     ("clk_fuse", ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
     ("clk_fuse_sched", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -264,11 +264,14 @@ def lookup_propose(h: Lookup, slots, draft, k, j, stream=None):
                                                           _stream(stream)))
 
 
-def lookup_propose_scan(h: Lookup, slots, draft, k, j, stream=None):
+def lookup_propose_scan(h: Lookup, slots, draft, k, j, stream=None, ctas_per_request: int = 0):
+    """The proposal by a full history scan (clk_lookup_propose_scan);
+    ctas_per_request=1 is the pages' one-program-per-request form."""
     B = slots.numel()
     _check("clk_lookup_propose_scan",
-           lib().clk_lookup_propose_scan(h.handle, _ptr(slots, name="slots"), B, _ptr(draft, shape=(B, BLOCK)),
-                                         _ptr(k, shape=(B,)), _ptr(j, shape=(B,)), _stream(stream)))
+           lib().clk_lookup_propose_scan(h.handle, _ptr(slots, name="slots"), B, int(ctas_per_request),
+                                         _ptr(draft, shape=(B, BLOCK)), _ptr(k, shape=(B,)), _ptr(j, shape=(B,)),
+                                         _stream(stream)))
 
 
 def sched_step(h: Lookup, slots, k, prev_accept, prev_len, length, stream=None):

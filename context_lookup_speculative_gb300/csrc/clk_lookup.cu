@@ -238,7 +238,7 @@ __global__ void k_fuse_sched(LookupDev L, const int32_t* __restrict__ slots, int
 // ---------------------------------------------------------------------------
 constexpr int kScanPerCta = 4096;
 
-__global__ void k_scan_match(LookupDev L, const int32_t* __restrict__ slots, int32_t chunks)
+__global__ void k_scan_match(LookupDev L, const int32_t* __restrict__ slots, int32_t chunks, int32_t per_cta)
 {
     __shared__ int32_t sm_suf[kMaxK];
     __shared__ unsigned long long sm_red[kThreads / 32];
@@ -247,7 +247,9 @@ __global__ void k_scan_match(LookupDev L, const int32_t* __restrict__ slots, int
     const int32_t slot = slots[b];
     if (slot < 0 || slot >= L.max_slots) return;
     const int32_t n = L.state[slot].n;
-    const int32_t lo = c * kScanPerCta, hi = min(n - 1, lo + kScanPerCta);  // end positions [lo, hi)
+    const int64_t lo64 = (int64_t)c * per_cta;
+    if (lo64 >= n - 1) return;
+    const int32_t lo = (int32_t)lo64, hi = (int32_t)min((int64_t)n - 1, lo64 + per_cta);  // end positions [lo, hi)
     if (n < 2 || lo >= hi) return;
     const clk_params& p = L.p;
     const int32_t* h = hist_of(L, slot);
@@ -616,16 +618,23 @@ extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int
                                     d_block, (cudaStream_t)s);
 }
 
-extern "C" int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft,
-                                       int32_t* d_k, int32_t* d_j, clk_stream_t s)
+extern "C" int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t ctas_per_request,
+                                       int32_t* d_draft, int32_t* d_k, int32_t* d_j, clk_stream_t s)
 {
     int rc = check_batch(h, B);
     if (rc != CLK_OK) return rc;
+    if (ctas_per_request < 0) return CLK_EINVAL;
     if (B == 0) return CLK_OK;
     if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
-    const int64_t chunks = (h->dev.cap + kScanPerCta - 1) / kScanPerCta;
-    if ((int64_t)B * chunks > 0x7FFFFFFF) return CLK_EINVAL;
-    k_scan_match<<<(unsigned)(B * chunks), kThreads, 0, (cudaStream_t)s>>>(h->dev, d_slots, (int32_t)chunks);
+    // Each request's end positions [0, cap) are cut into `chunks` ranges of
+    // per_cta positions, one CTA each.
+    const int64_t cap = h->dev.cap;
+    int64_t chunks = ctas_per_request > 0 ? ctas_per_request : (cap + kScanPerCta - 1) / kScanPerCta;
+    if (chunks > cap) chunks = cap;
+    const int64_t per_cta = (cap + chunks - 1) / chunks;
+    if ((int64_t)B * chunks > 0x7FFFFFFF || per_cta > 0x7FFFFFFF) return CLK_EINVAL;
+    k_scan_match<<<(unsigned)(B * chunks), kThreads, 0, (cudaStream_t)s>>>(h->dev, d_slots, (int32_t)chunks,
+                                                                          (int32_t)per_cta);
     if ((rc = launch_status()) != CLK_OK) return rc;
     k_scan_finish<<<(B + 3) / 4, 128, 0, (cudaStream_t)s>>>(h->dev, d_slots, B, d_draft, d_k, d_j);
     return launch_status();

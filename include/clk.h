@@ -197,9 +197,13 @@ CLK_API int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t B,
  * ("三步走", Step 1: one scan per request; most candidates fail on their first
  * tokens, the survivors are extended up to max_k), without the index.  Cost
  * O(n) per request per call; kept as the ablation of the incremental index.
- * Outputs and errors as clk_lookup_propose; the index is not touched. */
-CLK_API int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft,
-                                    int32_t* d_k, int32_t* d_j, clk_stream_t s);
+ * ctas_per_request: 1 scans each request's history in one CTA, the pages'
+ * form (one program per request); n > 1 splits it over n CTAs; 0 takes one
+ * CTA per 4,096 positions of the workspace's history capacity.  Any value
+ * gives the same answers.  Outputs and errors as clk_lookup_propose
+ * (CLK_EINVAL for a negative ctas_per_request); the index is not touched. */
+CLK_API int clk_lookup_propose_scan(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t ctas_per_request,
+                                    int32_t* d_draft, int32_t* d_k, int32_t* d_j, clk_stream_t s);
 
 /* Step 3 of "三步走" (the long-block scheduler), one step per request.  The
  * flag is k >= tail_k (the lookup can fill the tail); nearly full means the

@@ -214,12 +214,12 @@ def test_commits_without_lookup_in_between(commits):
     assert lk.status() == (0, 0)
 
 
-def _propose_scan(lk, s):
+def _propose_scan(lk, s, ctas_per_request=0):
     B = s.numel()
     d = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
     k = torch.zeros(B, dtype=torch.int32, device="cuda")
     j = torch.zeros(B, dtype=torch.int32, device="cuda")
-    clk.lookup_propose_scan(lk, s, d, k, j)
+    clk.lookup_propose_scan(lk, s, d, k, j, ctas_per_request=ctas_per_request)
     torch.cuda.synchronize()
     return d.cpu().numpy(), k.cpu().numpy(), j.cpu().numpy()
 
@@ -260,4 +260,10 @@ def test_full_scan_lookup_matches_oracle_and_index(kind):
     again = _propose_scan(lk, s)
     for a, b in zip(got, again):
         assert np.array_equal(a, b)
+    # one CTA per request (the pages' form), and other splits: the same answers
+    for per in (1, 3, 7):
+        for a, b in zip(got, _propose_scan(lk, s, ctas_per_request=per)):
+            assert np.array_equal(a, b), per
     assert lk.status() == (0, 0)
+    with pytest.raises(clk.ClkError):
+        _propose_scan(lk, s, ctas_per_request=-1)
