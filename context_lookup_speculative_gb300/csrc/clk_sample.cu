@@ -18,15 +18,17 @@
 // 2, a running maximum m of z = x * t * log2(e) and the sum s = sum 2^(z - m)
 // over its strided vectors of a segment (one fused multiply-add and one
 // hardware exp2 per element: the PTX ex2.approx.ftz.f32 instruction, whose
-// relative error the PTX ISA bounds by 2^-22); each warp combines its 32 threads' pairs with shuffles in a fixed
-// order and stores one (m, s) pair per segment and warp in the scratch, so no
-// barrier is needed per segment.  When a CTA leaves a request it adds the
+// relative error the PTX ISA bounds by 2^-22); each warp combines its 32
+// threads' pairs with shuffles in a fixed order and stores one (m, s) pair
+// per segment and warp in the scratch, so no barrier is needed per segment.  When a CTA leaves a request it adds the
 // number of that request's segments it finished to the request's counter;
 // the CTA that completes the count finishes the request: it combines the
 // pairs of each row in a fixed order, decides all acceptances at once, finds
 // the segment that holds the sample from the pairs and the token inside it by
 // reading that one segment again.  Every reduction has a fixed order, so the
-// results do not depend on the grid or on timing.
+// results do not depend on the grid or on timing.  k_sample serves the
+// stateless entry point; k_sample_step, fused with the token commit, starts
+// streaming predicted rows before the proposal launch it depends on ends.
 #include <algorithm>
 
 #include <cuda_bf16.h>
