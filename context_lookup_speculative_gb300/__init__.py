@@ -115,6 +115,7 @@ _SIGS = [
     ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
     ("clk_read_slot_info", ctypes.c_int, [_P, _I32, _P, _P]),
     ("clk_lookup_read_history", ctypes.c_int, [_P, _I32, _P, _I64, ctypes.POINTER(_I64), _P]),
+    ("clk_lookup_restore_state", ctypes.c_int, [_P, _I32, _P, _P, _P]),
     ("clk_lookup_destroy", None, [_P]),
 ]
 
@@ -236,6 +237,33 @@ class Lookup:
                lib().clk_lookup_read_history(self.handle, slot, out.ctypes.data, n.value, ctypes.byref(n),
                                              _stream(stream)))
         return out
+
+    # -- checkpoint / resume ----------------------------------------------
+    def snapshot(self, slot: int, stream=None) -> dict:
+        """Everything needed to resume request `slot` elsewhere: its history,
+        scheduler state and counters (host copies; synchronising)."""
+        return {"history": self.history(slot, stream), "info": self.slot_info(slot, stream),
+                "counters": self.counters(slot, stream)}
+
+    def restore(self, slot: int, snap: dict, stream=None):
+        """Resume a snapshot in `slot` of this lookup (same parameters): the
+        history is ingested again (which rebuilds its index), then the
+        scheduler state and counters are written back (synchronising)."""
+        import numpy as np
+        dev = self.workspace.device
+        hist = np.ascontiguousarray(snap["history"], dtype=np.int32)
+        s = torch.tensor([slot], dtype=torch.int32, device=dev)
+        off = torch.tensor([0, hist.size], dtype=torch.int64, device=dev)
+        lookup_init(self, s, torch.from_numpy(hist).to(dev), off, stream=stream)
+        info = SlotInfo(**{n: int(snap["info"][n]) for n, _ in SlotInfo._fields_})
+        c = Counters(**{n: int(snap["counters"][n]) for n in
+                        ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")})
+        for i in range(2):
+            for j in range(16):
+                c.accept_hist[i][j] = int(snap["counters"]["accept_hist"][i][j])
+        _check("clk_lookup_restore_state",
+               lib().clk_lookup_restore_state(self.handle, slot, ctypes.byref(info), ctypes.byref(c),
+                                              _stream(stream)))
 
 
 # ---------------------------------------------------------------------------
@@ -445,6 +473,17 @@ class Step:
         for t in self._len:
             t.zero_()
         self.accept.zero_()
+
+    def resume(self, accept, length):
+        """Continue from a checkpoint: the previous step's accepted counts and
+        block lengths (int32 [B], as ``accept`` and ``length`` held them when
+        the lookup was snapshotted), the inputs of the next scheduler step."""
+        for t, name in ((accept, "accept"), (length, "length")):
+            if tuple(t.shape) != (self.B,):
+                raise ValueError(f"{name} must have shape ({self.B},)")
+        for t in self._len:
+            t.copy_(length)
+        self.accept.copy_(accept)
 
     def pre(self, head, stream=None):
         if tuple(head.shape) != self._head_shape or head.dtype != torch.int32 or not head.is_cuda \

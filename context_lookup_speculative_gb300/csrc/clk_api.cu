@@ -231,6 +231,37 @@ extern "C" int clk_read_slot_info(clk_lookup* h, int32_t slot, clk_slot_info* ou
     return CLK_OK;
 }
 
+extern "C" int clk_lookup_restore_state(clk_lookup* h, int32_t slot, const clk_slot_info* info,
+                                        const clk_counters* counters, clk_stream_t s)
+{
+    if (!handle_ok(h) || info == nullptr || counters == nullptr || slot < 0 || slot >= h->dev.max_slots)
+        return CLK_EINVAL;
+    if ((info->mode != kShort && info->mode != kLong) || info->streak < 0 || info->miss < 0 ||
+        (info->has_prev != 0 && info->has_prev != 1) || info->cur_len < 0 || info->cur_len > kBlock)
+        return CLK_EINVAL;
+    SlotState st;
+    int rc = read_state(h, slot, &st, s);
+    if (rc != CLK_OK) return rc;
+    if (st.n != info->n) return CLK_EINVAL;
+    st.mode = info->mode;
+    st.streak = info->streak;
+    st.miss = info->miss;
+    st.has_prev = info->has_prev;
+    st.cur_len = info->cur_len;
+    st.steps = counters->steps;
+    st.hits = counters->hits;
+    st.long_steps = counters->long_steps;
+    st.drafted = counters->drafted;
+    st.accepted = counters->accepted;
+    st.emitted = counters->emitted;
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 16; ++j) st.accept_hist[i][j] = counters->accept_hist[i][j];
+    cudaStream_t cs = (cudaStream_t)s;
+    if (cudaMemcpyAsync(h->dev.state + slot, &st, sizeof st, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return CLK_ECUDA;
+    return cuda_status(cudaStreamSynchronize(cs));  // the host copy of st dies with this call
+}
+
 extern "C" int clk_lookup_read_history(clk_lookup* h, int32_t slot, int32_t* h_out, int64_t cap, int64_t* n_out,
                                        clk_stream_t s)
 {

@@ -22,8 +22,8 @@
  *   returns CLK_ECUDA.  No C++ exception crosses this boundary.
  * - Asynchrony: every call that takes a clk_stream_t (a cudaStream_t) only
  *   enqueues work on that stream; none synchronises, except clk_status,
- *   clk_read_counters, clk_read_slot_info and clk_lookup_read_history, which
- *   say so.
+ *   clk_read_counters, clk_read_slot_info, clk_lookup_read_history and
+ *   clk_lookup_restore_state, which say so.
  * - Device errors: problems that can only be seen on the device (a history
  *   capacity overflow, a token outside [0, vocab), a bad slot index, a bad
  *   block length) are latched into a status word inside the lookup
@@ -414,6 +414,21 @@ CLK_API int clk_read_slot_info(clk_lookup* h, int32_t slot, clk_slot_info* out, 
  * into host memory h_out; *n_out receives the history length. */
 CLK_API int clk_lookup_read_history(clk_lookup* h, int32_t slot, int32_t* h_out, int64_t cap, int64_t* n_out,
                                     clk_stream_t s);
+
+/* Checkpoint / resume of one request.  A snapshot is three reads:
+ * clk_lookup_read_history, clk_read_slot_info and clk_read_counters (the
+ * slot's own).  To resume it, in the same or another workspace with the same
+ * parameters: clk_lookup_init(slot, history) rebuilds the history and its
+ * index, then this call writes back the scheduler state (mode, streak, miss,
+ * has_prev, cur_len) and the counters.  info->n must equal the slot's
+ * history length; mode must be 0 or 1, streak and miss >= 0, has_prev 0 or
+ * 1, cur_len 0 or a block length 1..16; else CLK_EINVAL and nothing is
+ * written.  n_indexed and the index itself stay as clk_lookup_init left
+ * them.  The caller keeps the previous step's accepted count and block
+ * length (the inputs of the next scheduler step) with the snapshot.
+ * Synchronises `s`. */
+CLK_API int clk_lookup_restore_state(clk_lookup* h, int32_t slot, const clk_slot_info* info,
+                                     const clk_counters* counters, clk_stream_t s);
 
 /* Frees the host handle (not the workspace). */
 CLK_API void clk_lookup_destroy(clk_lookup* h);

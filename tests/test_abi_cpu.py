@@ -121,6 +121,16 @@ def test_handle_over_fake_workspace_validates_batches(clk):
         assert L.clk_lookup_append(h, 0x1000, -1, 0x1000, 0x1000, None) == clk.EINVAL
         assert L.clk_lookup_propose(h, 0x1000, 0, 0x1000, 0x1000, 0x1000, None) == 0  # empty batch: no-op
         assert L.clk_read_counters(h, 9, ctypes.byref(clk.Counters()), None) == clk.EINVAL
+        # a resume refuses a bad slot or scheduler state before touching the device
+        ok = clk.SlotInfo(n=5, mode=1, streak=0, miss=2, has_prev=1, cur_len=16, n_indexed=5)
+        c = clk.Counters()
+        assert L.clk_lookup_restore_state(h, 9, ctypes.byref(ok), ctypes.byref(c), None) == clk.EINVAL
+        assert L.clk_lookup_restore_state(h, 0, None, ctypes.byref(c), None) == clk.EINVAL
+        assert L.clk_lookup_restore_state(h, 0, ctypes.byref(ok), None, None) == clk.EINVAL
+        for field, bad in (("mode", 2), ("streak", -1), ("miss", -1), ("has_prev", 2), ("cur_len", 17)):
+            info = clk.SlotInfo(n=5, mode=1, streak=0, miss=2, has_prev=1, cur_len=16, n_indexed=5)
+            setattr(info, field, bad)
+            assert L.clk_lookup_restore_state(h, 0, ctypes.byref(info), ctypes.byref(c), None) == clk.EINVAL, field
     finally:
         L.clk_lookup_destroy(h)
 
