@@ -241,8 +241,8 @@ __device__ __forceinline__ int32_t fuse_slot(const clk_params& p, int32_t i, int
 // Commit of `count` tokens (in shared memory) to one slot: validation, the
 // history write, the new length and the step counters.  The k-grams that the
 // tokens complete are left for the index (nidx stays).  All threads of the
-// block call it with the same arguments; returns true if the tokens were
-// written (uniform across the block).
+// block call it with the same arguments; sm_flag is 3 ints of shared
+// memory; returns true if the tokens were written (uniform across the block).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t slot, const int32_t* sm_tok,
                                                     int32_t count, int32_t* sm_flag)
@@ -252,6 +252,7 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
     if (tid == 0) {
         int ok = 1;
         const int32_t n = st->n;
+        const int32_t len = st->cur_len;  // loaded with n: one round trip
         if (count < 0 || count > kBlock) {
             latch(L.status, CLK_EINVAL, slot);
             ok = 0;
@@ -268,6 +269,7 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
         }
         sm_flag[0] = ok;
         sm_flag[1] = n;
+        sm_flag[2] = len;
     }
     __syncthreads();
     const bool ok = sm_flag[0] != 0;
@@ -277,11 +279,16 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
         if (tid < count) h[n_old + tid] = sm_tok[tid];
         if (tid == 0) {
             st->n = n_old + count;
-            const int32_t len = st->cur_len;
+            const int32_t len = sm_flag[2];
             if (len != 0 && count > 0) {
-                st->accepted += count - 1;
-                st->emitted += count;
-                if (count - 1 < 16) st->accept_hist[(L.p.tail > 0 && len == long_len(L.p)) ? 1 : 0][count - 1] += 1;
+                // No other CTA touches this slot in the launch: the additions
+                // need no return value, so nothing waits for them.
+                atomicAdd(reinterpret_cast<unsigned long long*>(&st->accepted), (unsigned long long)(count - 1));
+                atomicAdd(reinterpret_cast<unsigned long long*>(&st->emitted), (unsigned long long)count);
+                if (count - 1 < 16) {
+                    const int cls = (L.p.tail > 0 && len == long_len(L.p)) ? 1 : 0;
+                    atomicAdd(reinterpret_cast<unsigned long long*>(&st->accept_hist[cls][count - 1]), 1ull);
+                }
             }
             st->cur_len = 0;
         }

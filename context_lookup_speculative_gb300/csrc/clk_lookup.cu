@@ -120,7 +120,7 @@ __global__ void k_append(LookupDev L, const int32_t* __restrict__ slots, const i
                          const int32_t* __restrict__ count)
 {
     __shared__ int32_t sm_tok[kBlock];
-    __shared__ int32_t sm_flag[2];
+    __shared__ int32_t sm_flag[3];
     __shared__ int32_t sm_nidx;
     const int32_t b = blockIdx.x;
     const int32_t slot = slots[b];

@@ -448,7 +448,7 @@ struct FinSmem {
     unsigned long long wsum[kSWarpsPerCta];
     int32_t lastw[kSWarpsPerCta];  // each warp's last element of positive weight
     int32_t out[kBlock];  // the emitted tokens (fused: committed)
-    int32_t flag[2];
+    int32_t flag[3];
 };
 
 // Request b is complete (all of its segments' pairs are stored): decide the

@@ -298,8 +298,9 @@ struct VerifySmem {
     int32_t warp[kVWarps];
     int32_t last;
     int32_t count;
+    int32_t slot;  // fused: the finished request's slot
     int32_t tok[kBlock];
-    int32_t flag[2];
+    int32_t flag[3];
 };
 
 // One row piece: this CTA's maximum over vectors [s0, s1) of row r of
@@ -336,6 +337,8 @@ __device__ __forceinline__ void finalize(const VerifyArgs& a, const LookupDev& L
         }
         if (lane < kBlock) kp[lane] = 0ull;
         const int32_t nxt = (lane + 1 < kBlock) ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
+        // fused: the slot, loaded in the same round trip as the keys
+        const int32_t slot = (FUSED && lane == 31) ? a.slots[b] : -1;
         const unsigned match = __ballot_sync(0xFFFFFFFFu, valid && lane < Lb - 1 && nxt == g);
         const int32_t acc = __ffs(~match) - 1;
         const int32_t out = (valid && lane <= acc) ? g : CLK_SENT;
@@ -350,10 +353,11 @@ __device__ __forceinline__ void finalize(const VerifyArgs& a, const LookupDev& L
             a.done[b] = 0ull;
             sm.count = valid ? acc + 1 : -1;
         }
+        if (FUSED && lane == 31) sm.slot = slot;
     }
     __syncthreads();
     if (FUSED) {
-        const int32_t slot = a.slots[b];
+        const int32_t slot = sm.slot;
         if (sm.count < 0 || slot < 0 || slot >= L.max_slots) {
             if (tid == 0) latch(L.status, CLK_EINVAL, b);
         } else {
