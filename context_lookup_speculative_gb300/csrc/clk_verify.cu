@@ -485,7 +485,9 @@ struct StepSmem {
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
 {
-    extern __shared__ int32_t sm_prefix[];  // P1[B + 1] (predicted rows), then P2[B + 1] (missed rows)
+    // P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then Lc[B + 1]
+    // (after the wait: each request's length, read once)
+    extern __shared__ int32_t sm_prefix[];
     __shared__ VerifySmem sm;
     __shared__ StepSmem ss;
     // Let the next launch (the next proposal) be scheduled; it waits for
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     const int32_t B = a.B;
     int32_t* P1 = sm_prefix;
     int32_t* P2 = sm_prefix + (B + 1);
+    int32_t* Lc = sm_prefix + 2 * (B + 1);
     const int32_t base = min(kBlock, 1 + L.p.head);
     const int64_t vpr = VEC ? (int64_t)a.V / Elem<DT>::W : (int64_t)a.V;
     if (tid == 0) {
@@ -514,14 +517,15 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     auto flush = [&]() {
         if (!ss.waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            block_prefix(B, [&a, P1](int32_t b) {
+            block_prefix(B, [&a, P1, Lc](int32_t b) {
                 const int32_t Lb = __ldcg(a.len + b);
+                Lc[b] = Lb;
                 return len_ok(Lb) ? max(0, Lb - (P1[b + 1] - P1[b])) : 0;
             }, P2, sm.warp);
             if (tid == 0) ss.waited = 1;
         }
         const int32_t nd = ss.nd;
-        if (tid < nd) ss.dl[tid] = __ldcg(a.len + ss.db[tid]);
+        if (tid < nd) ss.dl[tid] = Lc[ss.db[tid]];
         __syncthreads();
         for (int32_t i = 0; i < nd; ++i) {
             if (ss.dc[i] == total(ss.db[i], ss.dl[i])) finalize<true>(a, L, ss.db[i], ss.dl[i], sm);
@@ -543,8 +547,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
             const int64_t s1 = min(to, (ri + 1) * vpr) - ri * vpr;
             piece_max<DT, VEC>(a, b, (int32_t)(ri - P1[b]), s0, s1, sm);
             if (ss.waited) {
-                piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, __ldcg(a.len + b)),
-                                  __ldcg(a.len + b), sm);
+                piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, Lc[b]), Lc[b], sm);
             } else {
                 if (tid == 0) {
                     __threadfence();
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
             const int64_t s0 = lo2 - ri * vpr;
             const int64_t s1 = min(hi2, (ri + 1) * vpr) - ri * vpr;
             piece_max<DT, VEC>(a, b, pr + (int32_t)(ri - P2[b]), s0, s1, sm);
-            const int32_t Lb = __ldcg(a.len + b);
+            const int32_t Lb = Lc[b];
             piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, Lb), Lb, sm);
             ri += 1;
             lo2 = ri * vpr;
@@ -640,7 +643,7 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
 {
     constexpr int W = VEC ? Elem<DT>::W : 1;
     const int64_t vpr = (int64_t)a.V / W;
-    const size_t smem = (size_t)(FUSED ? 2 : 1) * (a.B + 1) * sizeof(int32_t);
+    const size_t smem = (size_t)(FUSED ? 3 : 1) * (a.B + 1) * sizeof(int32_t);
     int64_t grid = 0;
     if (!FUSED) {
         auto kern = k_verify<DT, VEC>;
