@@ -373,8 +373,8 @@ def run_ours(args, world, rank, local, dist):
     ratio = _traffic_ratio()
 
     ablation = run_lookup_ablation(lk, slots, w, device) if args.ablation else None
-    e2e = (run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device)
-           if (rank == 0 and not args.no_e2e and temp is None) else None)
+    e2e = (run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp)
+           if (rank == 0 and not args.no_e2e) else None)
     cpu = run_cpu_baseline(args, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
     steps_s = world * K / total_s
@@ -625,14 +625,15 @@ def run_ablation_sweep(args, world, rank, local):
             "data": "synthetic", "rows": rows}
 
 
-def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
+def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp=None):
     """Same metric through the public API with host buffers.  Each step copies
-    its head proposals from pinned host memory, runs the two launches on the
-    step's logits in pinned host memory, which the verify kernel reads in
-    place over the host link (only the rows it verifies), and reads back the
-    emitted tokens and counts.  The same steps with the whole [B, 16, V]
-    logits copied to the device first are reported as `staged`; the two runs
-    must emit the same tokens."""
+    its head proposals (and, sampled at temperature `temp`, its uniforms) from
+    pinned host memory, runs the two launches on the step's logits in pinned
+    host memory, which the verify kernel reads in place over the host link
+    (only the rows it verifies), and reads back the emitted tokens and
+    counts.  The same steps with the whole [B, 16, V] logits copied to the
+    device first are reported as `staged`; the two runs must emit the same
+    tokens."""
     import numpy as np
     import torch
 
@@ -649,14 +650,26 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
     # host copies of the n steps' inputs after the warm-up (pinned)
     h_heads = torch.empty((n, B, wl.HEAD), dtype=torch.int32, pin_memory=True)
     h_logits = torch.empty((n, B, 16, V), dtype=gen.torch_dtype(), pin_memory=True)
+    h_unis = torch.empty((n, B, 16, 2), dtype=torch.float32, pin_memory=True)
+    uni = torch.zeros((B, 16, 2), dtype=torch.float32, device=device)
     for i in range(n):
         gen.head(W + i, head, pos=pos_hist[W + i])
         gen.logits(dl, pos=pos_hist[W + i])
         h_heads[i].copy_(head)
         h_logits[i].copy_(dl)
+        gen.uniforms(W + i, uni)
+        h_unis[i].copy_(uni)
     torch.cuda.synchronize()
     esz = dl.element_size()
     base = min(16, 1 + params.head)
+    temps = torch.full((B,), 1.0 / temp if temp else 1.0, dtype=torch.float32, device=device)
+
+    def post(st, lg):
+        """The step's verify launch: greedy, or sampled with the uniforms in `uni`."""
+        if temp is None:
+            st.post(lg)
+        else:
+            st.post_sample(lg, temps, uni)
 
     def run(staged: bool):
         lk, slots = drive.make_lookup(w, params, device=device)
@@ -666,7 +679,9 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
             g.head(t, head)
             st.pre(head)
             g.logits(dl)
-            st.post(dl)
+            if temp is not None:
+                g.uniforms(t, uni)
+            post(st, dl)
             g.advance(st.emitted)
         h_out = torch.empty((n, B, 16), dtype=torch.int32, pin_memory=True)
         h_em = torch.empty((n, B), dtype=torch.int32, pin_memory=True)
@@ -678,14 +693,16 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
         start.record(stream)
         for i in range(n):
             head.copy_(h_heads[i], non_blocking=True)
+            if temp is not None:
+                uni.copy_(h_unis[i], non_blocking=True)
             lens[i, 0].copy_(st.length)  # the previous step's lengths: the verify's prediction
             st.pre(head)
             lens[i, 1].copy_(st.length)
             if staged:
                 dl.copy_(h_logits[i], non_blocking=True)
-                st.post(dl)
+                post(st, dl)
             else:
-                st.post(h_logits[i])
+                post(st, h_logits[i])
             h_out[i].copy_(st.out_tok, non_blocking=True)
             h_em[i].copy_(st.emitted, non_blocking=True)
         end.record(stream)
@@ -701,13 +718,14 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device):
     ms_s, wall_s, _, out_s, em_s = run(staged=True)
     if not (np.array_equal(out, out_s) and np.array_equal(em, em_s)):
         raise RuntimeError("e2e: host-resident and staged logits gave different tokens")
-    head_b = B * wl.HEAD * 4
+    head_b = B * wl.HEAD * 4 + (B * 16 * 2 * 4 if temp is not None else 0)  # heads (and uniforms)
     bo = B * 16 * 4 + B * 4
     return {"value": round(n / (ms * 1e-3), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(head_b + rows * V * esz), "d2h_bytes_per_step": bo,
             "steps": n, "wall_s": round(wall, 4),
-            "note": "head proposals copied from pinned host memory; the verify kernel reads the step's logits in "
-                    "place from pinned host memory over the host link, only the rows it verifies",
+            "note": "head proposals (sampled: and uniforms) copied from pinned host memory; the verify kernel "
+                    "reads the step's logits in place from pinned host memory over the host link, only the rows "
+                    "it verifies",
             "staged": {"value": round(n / (ms_s * 1e-3), 2), "unit": UNIT,
                        "h2d_bytes_per_step": head_b + B * 16 * V * esz, "wall_s": round(wall_s, 4),
                        "note": "the whole [B,16,V] logits copied to the device every step; same tokens"}}
