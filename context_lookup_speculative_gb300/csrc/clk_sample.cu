@@ -760,7 +760,9 @@ struct SampleStepSmem {
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(SampleArgs a, LookupDev Ldev)
 {
-    extern __shared__ int32_t sm_p[];  // P1[B + 1] (predicted rows), then P2[B + 1] (missed rows)
+    // P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then Lc[B + 1]
+    // (after the wait: each request's length, read once)
+    extern __shared__ int32_t sm_p[];
     __shared__ int32_t sm_warp[kSWarpsPerCta];
     __shared__ FinSmem fs;
     __shared__ SampleStepSmem ss;
@@ -771,6 +773,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
     const int32_t B = a.B;
     int32_t* P1 = sm_p;
     int32_t* P2 = sm_p + (B + 1);
+    int32_t* Lc = sm_p + 2 * (B + 1);
     const int32_t base = min(kBlock, 1 + Ldev.p.head);
     rows_prefix(B, [&a, base](int32_t b) {
         if (!temp_valid(a.inv_temp[b])) return 0;
@@ -849,7 +852,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
             }
         } else if (act == kActCheck) {
             const int32_t b = ss.db[ss.ci];
-            const int32_t Lb = __ldcg(a.len + b);
+            const int32_t Lb = Lc[b];
             const int32_t pr = P1[b + 1] - P1[b];
             const uint32_t total = (uint32_t)((pr > 0 && len_valid(Lb)) ? max(pr, Lb) : pr) * (uint32_t)a.S;
             if (ss.dc[ss.ci] == total) {
@@ -860,9 +863,10 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
             if (tid == 0) ss.ci += 1;
         } else {  // kActWait
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            rows_prefix(B, [&a, P1](int32_t b) {
+            rows_prefix(B, [&a, P1, Lc](int32_t b) {
                 const int32_t pr = P1[b + 1] - P1[b];
                 const int32_t Lb = __ldcg(a.len + b);
+                Lc[b] = Lb;
                 return (pr > 0 && len_valid(Lb)) ? max(0, Lb - pr) : 0;
             }, P2, sm_warp);
             // Requests with no rows (invalid length or temperature): the
@@ -904,7 +908,7 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     static int cache[64] = {0};  // resident CTAs per SM, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
-    const size_t smem = (size_t)(FUSED ? 2 : 1) * (a.B + 1) * sizeof(int32_t);
+    const size_t smem = (size_t)(FUSED ? 3 : 1) * (a.B + 1) * sizeof(int32_t);
     auto kern = FUSED ? k_sample_step<DT, VEC> : k_sample<DT, VEC>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
