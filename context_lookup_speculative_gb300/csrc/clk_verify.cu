@@ -48,6 +48,7 @@ struct VerifyArgs {
     unsigned long long* keys;  // [B * 16]
     unsigned long long* done;  // [B]
     const int32_t* slots;      // fused only
+    int32_t late;              // fused: trailing CTAs that start behind the proposal launch (0: none)
 };
 
 // Order-preserving 32-bit key of a float: larger value, larger key; +0 == -0.
@@ -466,6 +467,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 // A CTA with a short share (small batches) streams all of it first.
 constexpr int kVMaxDefer = 32;
 constexpr int64_t kVSplitMin = 16 * kVThreads;  // vectors: shares below this are not split
+constexpr int64_t kLateBytes = 60ll << 20;      // HBM bytes in the ~10 us a proposal launch runs
 
 // Rows read before the wait for request b.
 __device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b, int32_t base)
@@ -564,9 +566,25 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
         }
     };
 
+    // The predicted rows' flat range, split over the grid.  In the fused
+    // step the proposal launch's CTAs still hold registers when this launch
+    // starts, so its last `late` CTAs (dispatched last) start only when they
+    // leave, about kLateBytes of HBM time in.  Those CTAs get f8/8 of a
+    // share, less the shorter this launch; the split still covers the range
+    // exactly, so only the timing depends on it.
     const int64_t total1 = (int64_t)P1[B] * vpr;
-    const int64_t lo = total1 * blockIdx.x / gridDim.x;
-    const int64_t hi = total1 * (blockIdx.x + 1) / gridDim.x;
+    const int64_t G = gridDim.x;
+    const int64_t D = min((int64_t)a.late, G / 4);
+    const int64_t bytes1 = total1 * (int64_t)(VEC ? 16 : sizeof(typename Elem<DT>::T));
+    int64_t f8 = bytes1 > 0 ? 8 - (8 * kLateBytes + bytes1 / 2) / bytes1 : 8;
+    f8 = f8 < 1 ? 1 : (f8 > 8 ? 8 : f8);
+    const int64_t Wtot = (G - D) * 8 + D * f8;
+    auto start = [&](int64_t c) {  // total1 * W(c) / Wtot without overflow
+        const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
+        return (total1 / Wtot) * w + (total1 % Wtot) * w / Wtot;
+    };
+    const int64_t lo = start(blockIdx.x);
+    const int64_t hi = start(blockIdx.x + 1);
     const int64_t mid = (hi - lo >= kVSplitMin) ? lo + (hi - lo) / 2 : hi;
     phase1(lo, mid);
     flush();
@@ -745,6 +763,7 @@ extern "C" int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t ro
     a.keys = static_cast<unsigned long long*>(d_scratch);
     a.done = a.keys + (size_t)B * kBlock;
     a.slots = nullptr;
+    a.late = 0;
     LookupDev none = {};
     return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
 }
@@ -778,6 +797,11 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.keys = h->dev.vkeys;
     a.done = h->dev.vdone;
     a.slots = d_slots;
+    // The proposal launch this one overlaps runs one CTA of 14 warps per
+    // request (at most 64 registers a thread): each such CTA leaves room for
+    // 2 of the 4 CTAs of this launch on its SM.
+    const int sms = num_sms();
+    a.late = 2 * (B < sms ? B : (sms > 0 ? sms : 0));
     return verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
 }
 
@@ -849,6 +873,7 @@ extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int
     a.keys = static_cast<unsigned long long*>(scratch);
     a.done = a.keys + (size_t)B * kBlock;
     a.slots = nullptr;
+    a.late = 0;
     LookupDev none = {};
     return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
 }
