@@ -74,6 +74,7 @@ struct SampleArgs {
     uint32_t* done;  // [B] segments finished per request
     float2* part;    // [B][16][S][kSWarpsPerCta] (m, s) per warp
     const int32_t* slots;  // fused with the commit only: the requests' slots
+    int32_t late;          // fused: trailing CTAs that start behind the proposal launch (0: none)
 };
 
 __device__ __forceinline__ bool len_valid(int32_t l) { return l >= 1 && l <= kBlock; }
@@ -742,6 +743,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
 // sets the counter back to zero.  The inverse temperatures are read before
 // the wait, so they must not come from the proposal launch.
 constexpr int kSMaxDefer = 32;
+constexpr int64_t kSLateBytes = 60ll << 20;  // HBM bytes in the ~10 us a proposal launch runs
 
 // The block's next action, chosen by thread 0.
 enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
@@ -781,8 +783,22 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
         return len_valid(h) ? max(h, base) : base;
     }, P1, sm_warp);
     if (tid == 0) {
+        // This CTA's share of the predicted segments.  As in the fused greedy
+        // verification, the last `late` CTAs start only when the proposal
+        // launch's CTAs leave their SMs, about kSLateBytes of HBM time in;
+        // they get f8/8 of a share, less the shorter this launch.
         const int64_t n = (int64_t)P1[B] * a.S;
-        const int64_t lo = n * blockIdx.x / gridDim.x, hi = n * (blockIdx.x + 1) / gridDim.x;
+        const int64_t G = gridDim.x;
+        const int64_t D = min((int64_t)a.late, G / 4);
+        const int64_t bytes = (int64_t)P1[B] * a.V * (int64_t)sizeof(typename SElem<DT>::T);
+        int64_t f8 = bytes > 0 ? 8 - (8 * kSLateBytes + bytes / 2) / bytes : 8;
+        f8 = f8 < 1 ? 1 : (f8 > 8 ? 8 : f8);
+        const int64_t Wtot = (G - D) * 8 + D * f8;
+        auto start = [&](int64_t c) {  // n * W(c) / Wtot without overflow
+            const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
+            return (n / Wtot) * w + (n % Wtot) * w / Wtot;
+        };
+        const int64_t lo = start(blockIdx.x), hi = start(blockIdx.x + 1);
         ss.k = lo;
         ss.kend = hi;
         ss.hi1 = hi;
@@ -998,6 +1014,11 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     a.done = static_cast<uint32_t*>(d_scratch);
     a.part = reinterpret_cast<float2*>(static_cast<char*>(d_scratch) + align_up((size_t)B * sizeof(uint32_t), 16));
     a.slots = d_slots;
+    // Fused: the proposal launch this one overlaps runs one CTA of 14 warps
+    // per request, which leaves room for 2 of the 4 CTAs of this launch on
+    // its SM.
+    const int sms = num_sms();
+    a.late = h != nullptr ? 2 * (B < sms ? B : (sms > 0 ? sms : 0)) : 0;
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
     const bool bf = dtype == CLK_DTYPE_BF16;
