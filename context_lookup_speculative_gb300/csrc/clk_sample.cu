@@ -792,7 +792,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
         const int64_t D = min((int64_t)a.late, G / 4);
         const int64_t bytes = (int64_t)P1[B] * a.V * (int64_t)sizeof(typename SElem<DT>::T);
         int64_t f8 = bytes > 0 ? 8 - (8 * kSLateBytes + bytes / 2) / bytes : 8;
-        f8 = f8 < 1 ? 1 : (f8 > 8 ? 8 : f8);
+        f8 = f8 < 0 ? 0 : (f8 > 8 ? 8 : f8);
         const int64_t Wtot = (G - D) * 8 + D * f8;
         auto start = [&](int64_t c) {  // n * W(c) / Wtot without overflow
             const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;

@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     const int64_t D = min((int64_t)a.late, G / 4);
     const int64_t bytes1 = total1 * (int64_t)(VEC ? 16 : sizeof(typename Elem<DT>::T));
     int64_t f8 = bytes1 > 0 ? 8 - (8 * kLateBytes + bytes1 / 2) / bytes1 : 8;
-    f8 = f8 < 1 ? 1 : (f8 > 8 ? 8 : f8);
+    f8 = f8 < 0 ? 0 : (f8 > 8 ? 8 : f8);
     const int64_t Wtot = (G - D) * 8 + D * f8;
     auto start = [&](int64_t c) {  // total1 * W(c) / Wtot without overflow
         const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
