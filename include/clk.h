@@ -69,7 +69,7 @@ enum {
     CLK_EINVAL = -1,    /* bad argument */
     CLK_ECAPACITY = -2, /* history or index capacity exceeded */
     CLK_ECUDA = -3,     /* CUDA runtime error */
-    CLK_ENOTIMPL = -4,  /* not supported by this build */
+    CLK_ENOTIMPL = -4,  /* not supported by the compiled library */
     CLK_ESTATE = -5     /* call out of order (e.g. handle not set up) */
 };
 
