@@ -19,7 +19,15 @@ struct Layout {
     int64_t hstride;
     uint64_t tsize;
     int32_t nlev;
+    uint32_t posmask, fpmask;
 };
+
+// Fingerprint bits kept in an index entry.  A build may lower the limit to
+// make equal fingerprints of different k-grams frequent (a test of the
+// branches that tell them apart); answers never depend on it.
+#ifndef CLK_TEST_FP_BITS
+#define CLK_TEST_FP_BITS 32
+#endif
 
 uint64_t next_pow2(uint64_t x)
 {
@@ -37,22 +45,29 @@ int layout_of(const clk_params* p, int32_t max_slots, int64_t max_hist, Layout* 
     L.nlev = p->max_k - p->min_k + 1;
     L.hstride = (int64_t)align_up((size_t)max_hist, 64);
     L.tsize = next_pow2((uint64_t)(2 * max_hist) > 64 ? (uint64_t)(2 * max_hist) : 64);
+    // An entry holds q + 1 <= max_hist - 1 in its low bits and a fingerprint
+    // in the rest (at least one bit: max_hist <= 2^30).
+    int pos_bits = 1;
+    while (pos_bits < 31 && ((int64_t)1 << pos_bits) <= max_hist) ++pos_bits;
+    L.posmask = (uint32_t)((1ull << pos_bits) - 1);
+    const int fp_bits = (32 - pos_bits) < CLK_TEST_FP_BITS ? (32 - pos_bits) : CLK_TEST_FP_BITS;
+    L.fpmask = (uint32_t)(((1ull << fp_bits) - 1) << pos_bits);
     const size_t ns = (size_t)max_slots;
     size_t off = 0;
     L.status = off;
     off = align_up(off + 64 * sizeof(int32_t), kAlign);
     L.state = off;
     off = align_up(off + ns * sizeof(SlotState), kAlign);
-    L.vkeys = off;
-    off = align_up(off + ns * kBlock * sizeof(unsigned long long), kAlign);
+    L.vkeys = off;  // two halves, see clk_lookup::vparity
+    off = align_up(off + 2 * ns * kBlock * sizeof(unsigned long long), kAlign);
     L.vdone = off;
-    off = align_up(off + ns * sizeof(unsigned long long), kAlign);
+    off = align_up(off + 2 * ns * sizeof(unsigned long long), kAlign);
     L.skeys = off;
     off = align_up(off + ns * sizeof(unsigned long long), kAlign);
     L.hist = off;
     off = align_up(off + ns * (size_t)L.hstride * sizeof(int32_t), kAlign);
     L.tab = off;
-    off = align_up(off + ns * (size_t)L.nlev * (size_t)L.tsize * sizeof(unsigned long long), kAlign);
+    off = align_up(off + ns * (size_t)L.nlev * (size_t)L.tsize * sizeof(uint32_t), kAlign);
     L.total = off;
     *out = L;
     return CLK_OK;
@@ -129,10 +144,12 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     D.vdone = reinterpret_cast<unsigned long long*>(base + L.vdone);
     D.skeys = reinterpret_cast<unsigned long long*>(base + L.skeys);
     D.hist = reinterpret_cast<int32_t*>(base + L.hist);
-    D.tab = reinterpret_cast<unsigned long long*>(base + L.tab);
+    D.tab = reinterpret_cast<uint32_t*>(base + L.tab);
     D.hstride = L.hstride;
     D.cap = max_hist;
     D.tsize = L.tsize;
+    D.posmask = L.posmask;
+    D.fpmask = L.fpmask;
     D.nlev = L.nlev;
     D.max_slots = max_slots;
     D.vocab = vocab;
@@ -141,6 +158,8 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     hh->ws = d_workspace;
     hh->bytes = L.total;
     hh->device = 0;
+    hh->vparity = 0;
+    hh->last_fused = kFusedNone;
     cudaGetDevice(&hh->device);
     *h = hh;
     return CLK_OK;

@@ -2,25 +2,31 @@
 //
 // Workspace layout (one caller-owned device buffer, see clk_lookup_workspace_bytes):
 //   status  int32[64]                   latched device error (word 0) and its slot (word 1)
-//   state   SlotState[max_slots]        scheduler state, history length, counters
-//   vkeys   u64[max_slots * 16]         fused verify: per-row packed (value, index) maxima
-//   vdone   u64[max_slots]              fused verify: vectors verified per request
+//   state   SlotState[max_slots]        scheduler state, history length, the last 64 tokens, counters
+//   vkeys   u64[2][max_slots * 16]      fused verify: per-row packed (value, index) maxima
+//   vdone   u64[2][max_slots]           fused verify: vectors verified per request
+//                                       (two halves: consecutive fused verifies alternate)
 //   skeys   u64[max_slots]              full-scan lookup: best (length, position) per request
 //   hist    int32[max_slots][hstride]   token histories
-//   tab     u64[max_slots][nlev][tsize] k-gram index, one table per match length
+//   tab     u32[max_slots][nlev][tsize] k-gram index, one table per match length
 //
 // The k-gram index.  For every match length k in [min_k, max_k] a slot owns an
 // open-addressing table (linear probing, load <= 1/2) that maps a k-gram to
-// the END position q of its most recent occurrence.  An entry is
-// (fingerprint << 32) | (q + 1); 0 is empty.  A k-gram ending at q is
-// inserted once position q + 1 exists, so a table never returns the current
-// suffix itself and every hit q gives a candidate j = q + 1 <= n - 1 with
-// j >= k.  The longest suffix match of the pages' Step 1 is then the largest
-// k whose table holds the suffix's k-gram, and its most recent occurrence is
-// that table's entry: no chain walk and no history rescan, whatever the
-// history length or its periodicity.  Entries are only ever inserted (the
+// the END position q of its most recent occurrence.  An entry is one 32-bit
+// word: the low pos_bits bits hold q + 1 (pos_bits = the bit width of the
+// history capacity) and the high bits a fingerprint of the k-gram's hash; 0
+// is empty.  A k-gram ending at q is inserted once position q + 1 exists, so
+// a table never returns the current suffix itself and every hit q gives a
+// candidate j = q + 1 <= n - 1 with j >= k.  The longest suffix match of the
+// pages' Step 1 is then the largest k whose table holds the suffix's k-gram,
+// and its most recent occurrence is that table's entry: no chain walk and no
+// history rescan, whatever the history length or its periodicity.  A
+// fingerprint only filters: every stored occurrence is compared token by
+// token before it is used or updated, so equal fingerprints of different
+// k-grams never change an answer.  Entries are only ever inserted (the
 // history only grows), so concurrent inserts use a CAS to claim an empty
-// slot and an atomicMax on the same key to keep the largest q.
+// slot and an atomicMax on the same word (same fingerprint, larger q) to
+// keep the most recent occurrence.
 //
 // Deferred inserts.  A slot records nidx, the history length up to which its
 // tables are complete: they hold every k-gram ending at q <= nidx - 2.  The
@@ -30,6 +36,10 @@
 // directly against the suffix (they are the most recent candidates) and the
 // tables for everything older.  The answer is the same as with a complete
 // index, and the insert latency leaves the verify kernel.
+//
+// The last kRing tokens of every history are also kept in the slot's record
+// (ring[p mod kRing] = h[p]), next to n and the scheduler state, so that the
+// proposal reads the state and the suffix window in one round trip.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -41,6 +51,7 @@ namespace clk {
 
 constexpr int kBlock = CLK_BLOCK;
 constexpr int kMaxK = CLK_MAX_K;
+constexpr int kRing = 64;  // tokens of the history tail kept in the slot record
 constexpr int kShort = 0;
 constexpr int kLong = 1;
 
@@ -53,6 +64,7 @@ struct __align__(16) SlotState {
     int32_t cur_len;
     int32_t nidx;  // tables hold every k-gram ending at q <= nidx - 2
     int32_t pad1;
+    int32_t ring[kRing];  // ring[p % kRing] = h[p] for the last kRing positions p < n
     long long steps, hits, long_steps, drafted, accepted, emitted;
     long long accept_hist[2][16];
 };
@@ -64,10 +76,12 @@ struct LookupDev {
     unsigned long long* vdone;
     unsigned long long* skeys;  // full-scan lookup: packed (length, end + 1) per batch position
     int32_t* hist;
-    unsigned long long* tab;
+    uint32_t* tab;
     int64_t hstride;  // int32 elements per history
     int64_t cap;      // max_hist
     uint64_t tsize;   // entries per table (power of two)
+    uint32_t posmask; // low bits of an entry: end position + 1
+    uint32_t fpmask;  // high bits of an entry: fingerprint
     int32_t nlev;     // max_k - min_k + 1
     int32_t max_slots;
     int32_t vocab;
@@ -85,7 +99,7 @@ __device__ __forceinline__ int32_t* hist_of(const LookupDev& L, int32_t slot)
     return L.hist + (int64_t)slot * L.hstride;
 }
 
-__device__ __forceinline__ unsigned long long* table_of(const LookupDev& L, int32_t slot, int32_t level)
+__device__ __forceinline__ uint32_t* table_of(const LookupDev& L, int32_t slot, int32_t level)
 {
     return L.tab + ((uint64_t)slot * (uint64_t)L.nlev + (uint64_t)level) * L.tsize;
 }
@@ -134,26 +148,81 @@ __device__ __forceinline__ bool kgram_at(const int32_t* h, int32_t p, const int3
     return same;
 }
 
-// Insert k-gram w (ending at q, hash H) into one table; keeps the largest q.
-// Returns false only if the table is full (cannot happen at load <= 1/2).
-__device__ __forceinline__ bool index_insert(unsigned long long* tab, uint64_t mask, uint64_t H,
-                                             const int32_t* h, int32_t q, const int32_t* w,
-                                             int32_t k)
+// The entry of the k-gram with hash H ending at q.
+__device__ __forceinline__ uint32_t kg_entry(const LookupDev& L, uint64_t H, int32_t q)
 {
-    const uint32_t fp = (uint32_t)(H >> 32);
-    const unsigned long long entry = ((unsigned long long)fp << 32) | (uint32_t)(q + 1);
-    uint64_t s = H & mask;
-    for (uint64_t probe = 0; probe <= mask; ++probe, s = (s + 1) & mask) {
-        unsigned long long cur = __ldcg(tab + s);
-        if (cur == 0ull) {
-            unsigned long long old = atomicCAS(tab + s, 0ull, entry);
-            if (old == 0ull) return true;
+    return ((uint32_t)(H >> 32) & L.fpmask) | (uint32_t)(q + 1);
+}
+
+// Insert k-gram w (ending at q, hash H) into one table; keeps the largest q.
+// `same(p)` tells whether the k-gram ending at p equals w.  Linear probing
+// from H mod tsize.  Returns false only if the table is full (cannot happen
+// at load <= 1/2).
+template <typename Same>
+__device__ __forceinline__ bool index_insert(const LookupDev& L, uint32_t* tab, uint64_t H, int32_t q, Same same)
+{
+    const uint32_t mask = (uint32_t)(L.tsize - 1);
+    const uint32_t entry = kg_entry(L, H, q);
+    const uint32_t fp = entry & L.fpmask;
+    uint32_t s = (uint32_t)H & mask;
+    for (uint32_t probe = 0; probe <= mask; ++probe, s = (s + 1) & mask) {
+        uint32_t cur = __ldcg(tab + s);
+        if (cur == 0u) {
+            const uint32_t old = atomicCAS(tab + s, 0u, entry);
+            if (old == 0u) return true;
             cur = old;
         }
-        if ((uint32_t)(cur >> 32) == fp && kgram_at(h, (int32_t)(uint32_t)cur - 1, w, k)) {
+        if ((cur & L.fpmask) == fp && same((int32_t)(cur & L.posmask) - 1)) {
             atomicMax(tab + s, entry);
             return true;
         }
+    }
+    return false;
+}
+
+// index_insert for the latency-bound proposal launch: the probe sequence is
+// read 8 entries per round trip (8 independent 4-byte loads), then the
+// entries are examined in order.  Same result as index_insert.
+template <typename Same>
+__device__ __forceinline__ bool index_insert8(const LookupDev& L, uint32_t* tab, uint64_t H, int32_t q, Same same)
+{
+    const uint32_t mask = (uint32_t)(L.tsize - 1);
+    const uint32_t entry = kg_entry(L, H, q);
+    const uint32_t fp = entry & L.fpmask;
+    uint32_t s = (uint32_t)H & mask;
+    uint32_t probed = 0;
+    while (probed <= mask) {
+        uint32_t e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = __ldcg(tab + ((s + (uint32_t)i) & mask));
+        // the first entry that is empty or carries the fingerprint
+        int i0 = 8;
+#pragma unroll
+        for (int i = 7; i >= 0; --i)
+            if (e[i] == 0u || (e[i] & L.fpmask) == fp) i0 = i;
+        if (i0 == 8) {
+            s = (s + 8u) & mask;
+            probed += 8;
+            continue;
+        }
+        uint32_t cur = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i == i0) cur = e[i];
+        const uint32_t at = (s + (uint32_t)i0) & mask;
+        if (cur == 0u) {
+            const uint32_t old = atomicCAS(tab + at, 0u, entry);
+            if (old == 0u) return true;
+            cur = old;
+        }
+        if ((cur & L.fpmask) == fp && same((int32_t)(cur & L.posmask) - 1)) {
+            atomicMax(tab + at, entry);
+            return true;
+        }
+        // a different k-gram (same fingerprint, or a slot taken meanwhile):
+        // continue after it
+        s = (at + 1u) & mask;
+        probed += (uint32_t)i0 + 1u;
     }
     return false;
 }
@@ -192,10 +261,15 @@ __device__ __forceinline__ int32_t sched_apply(const clk_params& p, SlotState* s
     st->miss = miss;
     st->has_prev = 1;
     st->cur_len = len;
-    st->steps += 1;
-    st->hits += (k >= p.min_k) ? 1 : 0;
-    st->long_steps += (p.tail > 0 && len == long_len(p)) ? 1 : 0;  // no tail: no long block
-    st->drafted += p.head + ((len == long_len(p) && k >= p.tail_k) ? p.tail : 0);
+    // Only this thread touches the slot's counters in the launch: additions
+    // whose result nothing waits for (no load of the old values).
+    auto add = [](long long* c, long long v) {
+        if (v != 0) atomicAdd(reinterpret_cast<unsigned long long*>(c), (unsigned long long)v);
+    };
+    add(&st->steps, 1);
+    add(&st->hits, (k >= p.min_k) ? 1 : 0);
+    add(&st->long_steps, (p.tail > 0 && len == long_len(p)) ? 1 : 0);  // no tail: no long block
+    add(&st->drafted, p.head + ((len == long_len(p) && k >= p.tail_k) ? p.tail : 0));
     return len;
 }
 
@@ -276,7 +350,10 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
     if (ok) {
         const int32_t n_old = sm_flag[1];
         int32_t* h = hist_of(L, slot);
-        if (tid < count) h[n_old + tid] = sm_tok[tid];
+        if (tid < count) {
+            h[n_old + tid] = sm_tok[tid];
+            st->ring[(n_old + tid) & (kRing - 1)] = sm_tok[tid];
+        }
         if (tid == 0) {
             st->n = n_old + count;
             const int32_t len = sm_flag[2];
@@ -306,7 +383,6 @@ __device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, in
     if (q_hi < q_lo) return;
     const clk_params& p = L.p;
     const int32_t* h = hist_of(L, slot);
-    const uint64_t mask = L.tsize - 1;
     const int64_t tasks = (int64_t)(q_hi - q_lo + 1) * L.nlev;
     for (int64_t task = rank; task < tasks; task += nthr) {
         const int32_t q = q_lo + (int32_t)(task / L.nlev);
@@ -322,7 +398,8 @@ __device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, in
                 acc = kg_step(acc, w[l]);
             }
         }
-        if (!index_insert(table_of(L, slot, lvl), mask, kg_final(acc, k), h, q, w, k))
+        auto same = [&](int32_t pos) { return kgram_at(h, pos, w, k); };
+        if (!index_insert(L, table_of(L, slot, lvl), kg_final(acc, k), q, same))
             latch(L.status, CLK_ECAPACITY, slot);
     }
 }

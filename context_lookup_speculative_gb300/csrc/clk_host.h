@@ -12,11 +12,18 @@ struct clk_lookup {
     void* ws;
     size_t bytes;
     int device;
+    // The fused greedy verify alternates between two scratch halves (vparity)
+    // so that it may start streaming while the previous one finishes; the
+    // proposal lets its dependent start at once only after such a verify
+    // (last_fused = kFusedGreedy), whose scratch use it then cannot disturb.
+    int vparity;
+    int last_fused;
 };
 
 namespace clk {
 
 constexpr size_t kAlign = 256;
+constexpr int kFusedNone = 0, kFusedGreedy = 1, kFusedSampled = 2;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

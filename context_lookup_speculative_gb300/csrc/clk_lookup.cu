@@ -60,12 +60,14 @@ __global__ void k_copy_prompt(LookupDev L, const int32_t* __restrict__ slots, co
     const int32_t slot = init_slot(L, slots, off, b, &n);
     if (slot < 0 || n < 1 || n > L.cap) return;
     int32_t* h = hist_of(L, slot);
+    int32_t* ring = L.state[slot].ring;
     const int32_t* src = prompt + off[b];
     bool bad = false;
     for (int64_t q = c * kThreads * 4 + threadIdx.x; q < min(n, (c + 1) * kThreads * 4); q += kThreads) {
         const int32_t t = src[q];
         bad |= !token_ok(L, t);
         h[q] = t;
+        if (q >= n - kRing) ring[q  & (kRing - 1)] = t;
     }
     if (bad) latch(L.status, CLK_EINVAL, slot);
 }
@@ -77,9 +79,9 @@ __global__ void k_clear_tables(LookupDev L, const int32_t* __restrict__ slots, i
     const uint64_t c = blockIdx.x % chunks;
     const int32_t slot = slots[b];
     if (slot < 0 || slot >= L.max_slots) return;
-    const uint64_t total = (uint64_t)L.nlev * L.tsize;  // entries, even
+    const uint64_t total = (uint64_t)L.nlev * L.tsize;  // entries, a multiple of 4
     uint4* base = reinterpret_cast<uint4*>(table_of(L, slot, 0));
-    const uint64_t lo = c * per_chunk, hi = min(total / 2, (c + 1) * per_chunk);
+    const uint64_t lo = c * per_chunk, hi = min(total / 4, (c + 1) * per_chunk);
     for (uint64_t i = lo + threadIdx.x; i < hi; i += kThreads) base[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
@@ -100,7 +102,6 @@ __global__ void k_build_index(LookupDev L, const int32_t* __restrict__ slots, co
     int32_t w[kMaxK];
 #pragma unroll
     for (int l = 0; l < kMaxK; ++l) w[l] = (l < p.max_k && q - l >= 0) ? h[q - l] : CLK_SENT;
-    const uint64_t mask = L.tsize - 1;
     uint64_t acc = kHashSeed;
 #pragma unroll
     for (int l = 0; l < kMaxK; ++l) {
@@ -108,7 +109,8 @@ __global__ void k_build_index(LookupDev L, const int32_t* __restrict__ slots, co
         if (k > p.max_k || q < k - 1) break;
         acc = kg_step(acc, w[l]);
         if (k >= p.min_k) {
-            if (!index_insert(table_of(L, slot, k - p.min_k), mask, kg_final(acc, k), h, (int32_t)q, w, k))
+            auto same = [&](int32_t pos) { return kgram_at(h, pos, w, k); };
+            if (!index_insert(L, table_of(L, slot, k - p.min_k), kg_final(acc, k), (int32_t)q, same))
                 latch(L.status, CLK_ECAPACITY, slot);
         }
     }
@@ -307,136 +309,152 @@ __global__ void k_scan_finish(LookupDev L, const int32_t* __restrict__ slots, in
     }
 }
 
-constexpr int kMaxPending = 32;                  // pending end positions checked directly
-constexpr int kWin = kMaxPending + kMaxK + 1;    // window of history tokens in shared memory
-constexpr int kInsertWarps = 5;                  // warps that index the pending positions
+constexpr int kMaxPending = 32;  // pending end positions checked directly
+constexpr int kInsertWarps = 5;  // warps that index the pending positions
+constexpr int kStepWarps = kMaxK + kInsertWarps;
+static_assert(kMaxPending + kMaxK <= kRing, "the ring must cover the pending window");
+
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // Step 1 (and with FUSE, Steps 3 and 2) for one request per CTA.
+//   Every warp loads the slot, then the slot's record: n, nidx, the
+//   scheduler state and the last kRing tokens (one round trip, no barrier).
 //   warps 0..nlev-1: one match length k = min_k + warp each.  The pending end
-//     positions (not yet in the tables) are checked against the suffix from a
-//     shared-memory window, most recent first; if none matches, the table of
-//     length k is probed, and one warp-wide load both verifies the stored
-//     occurrence token by token and fetches the 16 tokens that follow it.
-//   the last kInsertWarps warps: index the pending positions meanwhile.
+//     positions (not yet in the tables) are checked against the suffix from
+//     the ring, most recent first; if none matches, 32 consecutive entries of
+//     the table of length k are read at once from the k-gram's probe start,
+//     and each one whose fingerprint matches (before the first empty entry)
+//     is checked token by token by one warp-wide load, which also fetches the
+//     16 tokens that follow the occurrence.
+//   the last kInsertWarps warps: index the pending positions meanwhile; they
+//     synchronise only among themselves, so the proposal never waits for them.
 //   warp 0 then takes the longest level that matched (ballot), builds the
 //   LZ77 draft, and with FUSE runs the scheduler and the fusion rule.
 template <bool FUSE>
-__global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ head,
-                              const int32_t* prev_a, const int32_t* prev_len, int32_t* __restrict__ draft,
-                              int32_t* __restrict__ k_out, int32_t* __restrict__ j_out, int32_t* len_out,
-                              int32_t* __restrict__ block)
+__global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
+    LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ head, const int32_t* prev_a,
+    const int32_t* prev_len, int32_t* __restrict__ draft, int32_t* __restrict__ k_out, int32_t* __restrict__ j_out,
+    int32_t* len_out, int32_t* __restrict__ block, int32_t early)
 {
-    __shared__ int32_t sm_tok[kWin];
+    __shared__ __align__(16) int32_t sm_win[kStepWarps][kRing];  // each warp's copy of the ring (16-byte stores)
     __shared__ int32_t sm_q[kMaxK];
     __shared__ int32_t sm_follow[kMaxK][kBlock];
-    __shared__ int32_t sm_info[4];
     const unsigned full = 0xFFFFFFFFu;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t b = blockIdx.x;
     const clk_params& p = L.p;
+    const int nlev = L.nlev;
 
     // Launched as a programmatic dependent of the previous step's verify
-    // launch: wait for it (it commits the tokens this launch reads), then let
-    // this step's verify launch start streaming its first rows.
+    // launch, which commits the tokens this launch reads: wait for it.  This
+    // step's verify launch may start streaming its first rows before (early:
+    // the previous launch was a fused greedy verify, which uses the other
+    // half of the scratch and let this launch start only after its own wait)
+    // or only after that wait.
+    if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Inputs that do not depend on the history, loaded first.
+    // Round trip 1: the slot (every warp); warp 0 also loads the inputs that
+    // do not depend on it.
+    const int32_t slot = slots[b];
     int32_t m_lane = CLK_SENT, pa = 0, pl = 0;
-    SchedFields sf = {0, 0, 0, 0};
     if (FUSE && warp == 0) {
         if (lane < p.head) m_lane = head[(int64_t)b * p.head + lane];
-        if (lane == 0) {
-            pa = prev_a[b];
-            pl = prev_len[b];
-        }
+        pa = prev_a[b];
+        pl = prev_len[b];
     }
+    const bool valid = slot >= 0 && slot < L.max_slots;
+    // Round trip 2: the slot's record up to the end of the ring (18 x 16 B).
+    int4 rec = make_int4(0, 0, 0, 0);
+    if (valid && lane < 2 + kRing / 4) rec = __ldcg(reinterpret_cast<const int4*>(L.state + slot) + lane);
+    // Keep the compiler from sinking round trip 1's loads to their first use
+    // after the lookup: their values are needed by then anyway.
+    if (FUSE) asm volatile("" ::"r"(m_lane), "r"(pa), "r"(pl));
+    const int32_t n = __shfl_sync(full, rec.x, 0);
+    int32_t nidx = min(__shfl_sync(full, rec.z, 1), n);
+    int32_t* win = sm_win[warp];
+    if (lane >= 2 && lane < 2 + kRing / 4) reinterpret_cast<int4*>(win)[lane - 2] = rec;
+    __syncwarp();
+    // 1: a request with a history; 2: a valid slot with an empty history (no
+    // proposal; the scheduler still steps); 0: a bad slot.
+    const int32_t ok = valid ? (n >= 1 ? 1 : 2) : 0;
     if (tid == 0) {
-        const int32_t slot = slots[b];
-        int32_t ok = 1, n = 0, nidx = 0;
-        if (slot < 0 || slot >= L.max_slots) {
-            latch(L.status, CLK_EINVAL, b);
-            ok = 0;
-        } else {
-            const SlotState* st = L.state + slot;
-            n = st->n;
-            nidx = st->nidx;
-            sf = sched_load(st);
-            if (n < 1) {
-                latch(L.status, CLK_ESTATE, slot);
-                ok = 2;  // a valid but empty slot: no proposal, the scheduler still steps
-            }
-        }
-        sm_info[0] = slot;
-        sm_info[1] = n;
-        sm_info[2] = min(nidx, n);
-        sm_info[3] = ok;
+        if (!valid) latch(L.status, CLK_EINVAL, b);
+        else if (ok == 2) latch(L.status, CLK_ESTATE, slot);
     }
-    if (tid < kMaxK) sm_q[tid] = -1;
-    __syncthreads();
-    const int32_t slot = sm_info[0], n = sm_info[1], ok = sm_info[3];
-    int32_t nidx = sm_info[2];
     const int32_t* h = ok == 1 ? hist_of(L, slot) : nullptr;
     if (ok == 1 && n - nidx > kMaxPending) {
         // Many commits without a lookup in between: index them all first.
         index_range(L, slot, max(nidx - 1, 0), n - 2, tid, blockDim.x);
-        nidx = n;
         __syncthreads();
+        if (tid == 0) L.state[slot].nidx = n;
+        nidx = n;
     }
-    const int32_t pend_lo = max(nidx - 1, 0);         // first end position not in the tables
-    const int32_t wlo = max(0, pend_lo - (p.max_k - 1));  // window = history [wlo, n)
-    if (ok == 1 && tid < n - wlo) sm_tok[tid] = h[wlo + tid];
-    __syncthreads();
+    const int32_t pend_lo = max(nidx - 1, 0);  // first end position not in the tables
+    const int32_t wlo = max(0, n - kRing);     // the ring holds positions [wlo, n)
+    // Token at position x < n: from the ring when it holds x, else from the history.
+    auto tok_at = [&](int32_t x) { return x >= wlo ? win[x  & (kRing - 1)] : __ldcg(h + x); };
 
-    if (ok == 1) {
-        if (warp < L.nlev) {
-            const int32_t k = p.min_k + warp;
-            int32_t q = -1, fol = CLK_SENT;
-            if (n >= k + 1) {
-                const int32_t cand = n - 2 - lane;
-                bool m = cand >= max(pend_lo, k - 1);
-                for (int l = 0; m && l < k; ++l) m = sm_tok[cand - l - wlo] == sm_tok[n - 1 - l - wlo];
-                const unsigned hits = __ballot_sync(full, m);
-                if (hits) {
-                    q = n - 2 - (__ffs(hits) - 1);
-                } else {
-                    uint64_t acc = kHashSeed;
-                    for (int l = 0; l < k; ++l) acc = kg_step(acc, sm_tok[n - 1 - l - wlo]);
-                    const uint64_t H = kg_final(acc, k);
-                    const uint32_t fp = (uint32_t)(H >> 32);
-                    const uint64_t mask = L.tsize - 1;
-                    const unsigned long long* tab = table_of(L, slot, warp);
-                    const int32_t sl = lane < k ? sm_tok[n - 1 - lane - wlo] : 0;
-                    uint64_t sidx = H & mask;
-                    for (uint64_t probe = 0; probe <= mask; ++probe, sidx = (sidx + 1) & mask) {
-                        unsigned long long e = 0ull;
-                        if (lane == 0) e = tab[sidx];
-                        e = __shfl_sync(full, e, 0);
-                        if (e == 0ull) break;
-                        if ((uint32_t)(e >> 32) != fp) continue;
-                        const int32_t pp = (int32_t)(uint32_t)e - 1;
+    if (warp < nlev) {
+        const int32_t k = p.min_k + warp;
+        int32_t q = -1, fol = CLK_SENT;
+        if (ok == 1 && n >= k + 1) {
+            const int32_t cand = n - 2 - lane;
+            bool m = cand >= max(pend_lo, k - 1);
+            for (int l = 0; m && l < k; ++l) m = win[(cand - l)  & (kRing - 1)] == win[(n - 1 - l)  & (kRing - 1)];
+            const unsigned hits = __ballot_sync(full, m);
+            if (hits) {
+                q = n - 2 - (__ffs(hits) - 1);
+            } else {
+                uint64_t acc = kHashSeed;
+                for (int l = 0; l < k; ++l) acc = kg_step(acc, win[(n - 1 - l)  & (kRing - 1)]);
+                const uint64_t H = kg_final(acc, k);
+                const uint32_t fp = kg_entry(L, H, 0) & L.fpmask;
+                const uint32_t mask = (uint32_t)(L.tsize - 1);
+                const uint32_t* tab = table_of(L, slot, warp);
+                const int32_t sl = lane < k ? win[(n - 1 - lane)  & (kRing - 1)] : 0;
+                const uint32_t s0 = (uint32_t)H & mask;
+                bool done = false;
+                for (uint32_t probed = 0; !done && probed <= mask; probed += 32) {
+                    const uint32_t e = __ldcg(tab + ((s0 + probed + (uint32_t)lane) & mask));
+                    const unsigned empty = __ballot_sync(full, e == 0u);
+                    const int lim = empty ? __ffs(empty) - 1 : 32;
+                    unsigned cands = __ballot_sync(full, lane < lim && (e & L.fpmask) == fp);
+                    done = empty != 0u;
+                    while (cands) {
+                        const int c = __ffs(cands) - 1;
+                        cands &= cands - 1;
+                        const int32_t pp = (int32_t)(__shfl_sync(full, e, c) & L.posmask) - 1;
                         bool same = true;
-                        if (lane < k) same = pp - lane >= 0 && h[pp - lane] == sl;
+                        if (lane < k) same = pp < n && pp - lane >= 0 && tok_at(pp - lane) == sl;
                         int32_t f = CLK_SENT;
-                        if (lane >= 16 && pp + 1 + (lane - 16) < n) f = h[pp + 1 + (lane - 16)];
+                        if (lane >= 16 && pp + 1 + (lane - 16) < n) f = tok_at(pp + 1 + (lane - 16));
                         if (__all_sync(full, same)) {
                             q = pp;
                             fol = f;
+                            done = true;
                             break;
                         }
                     }
                 }
             }
-            if (lane == 0) sm_q[warp] = q;
-            if (lane >= 16) sm_follow[warp][lane - 16] = fol;
-        } else if (n - 2 >= pend_lo) {
-            // Index the pending end positions, tokens from the window.
-            const int32_t rank = tid - L.nlev * 32, nthr = (int32_t)blockDim.x - L.nlev * 32;
-            const uint64_t mask = L.tsize - 1;
-            const int32_t tasks = (n - 1 - pend_lo) * L.nlev;
+        }
+        if (lane == 0) sm_q[warp] = q;
+        if (lane >= 16) sm_follow[warp][lane - 16] = fol;
+        __syncwarp();
+        named_barrier(1, nlev * 32);
+    } else {
+        if (ok == 1 && n - 2 >= pend_lo) {
+            // Index the pending end positions, tokens from the ring.
+            const int32_t rank = tid - nlev * 32, nthr = (int32_t)blockDim.x - nlev * 32;
+            const int32_t tasks = (n - 1 - pend_lo) * nlev;
             for (int32_t task = rank; task < tasks; task += nthr) {
-                const int32_t q = pend_lo + task / L.nlev;
-                const int32_t lvl = task % L.nlev;
+                const int32_t q = pend_lo + task / nlev;
+                const int32_t lvl = task % nlev;
                 const int32_t k = p.min_k + lvl;
                 if (q < k - 1) continue;
                 int32_t w[kMaxK];
@@ -444,21 +462,36 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
 #pragma unroll
                 for (int l = 0; l < kMaxK; ++l) {
                     if (l < k) {
-                        w[l] = sm_tok[q - l - wlo];
+                        w[l] = win[(q - l)  & (kRing - 1)];
                         acc = kg_step(acc, w[l]);
                     }
                 }
-                if (!index_insert(table_of(L, slot, lvl), mask, kg_final(acc, k), h, q, w, k))
+                // One branch per check: the stored occurrence's k tokens from
+                // the ring when it holds them all, else k loads issued together.
+                auto same = [&](int32_t pos) {
+                    if (pos - (k - 1) < 0 || pos >= n) return false;
+                    if (pos - (k - 1) >= wlo) {
+                        bool eq = true;
+#pragma unroll
+                        for (int l = 0; l < kMaxK; ++l)
+                            if (l < k) eq &= win[(pos - l) & (kRing - 1)] == w[l];
+                        return eq;
+                    }
+                    return kgram_at(h, pos, w, k);
+                };
+                if (!index_insert8(L, table_of(L, slot, lvl), kg_final(acc, k), q, same))
                     latch(L.status, CLK_ECAPACITY, slot);
             }
+            __syncwarp();
+            named_barrier(2, (int)blockDim.x - nlev * 32);
+            if (rank == 0) L.state[slot].nidx = n;
         }
+        return;
     }
-    __syncthreads();
     if (warp != 0) return;
-    if (ok == 1 && lane == 0) L.state[slot].nidx = n;
     int32_t kbest = 0, j = -1, c = CLK_SENT;
     if (ok == 1) {
-        const int32_t lv = lane < L.nlev ? sm_q[lane] : -1;
+        const int32_t lv = lane < nlev ? sm_q[lane] : -1;
         const unsigned hit = __ballot_sync(full, lv >= 0);
         if (hit) {
             const int best = 31 - __clz((int)hit);
@@ -467,7 +500,7 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
             j = q + 1;
             if (lane < kBlock) {
                 const int32_t idx = lane % (n - j);  // LZ77 copy at distance n - j
-                c = q >= pend_lo ? sm_tok[j + idx - wlo] : sm_follow[best][idx];
+                c = q >= pend_lo ? win[(j + idx)  & (kRing - 1)] : sm_follow[best][idx];
             }
         }
     }
@@ -477,13 +510,16 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
         j_out[b] = j;
     }
     if (FUSE) {
+        // scheduler state from the record: (n, mode, streak, miss) in lane 0,
+        // (has_prev, ...) in lane 1
+        const int32_t has_prev = __shfl_sync(full, rec.x, 1);
         int32_t l = short_len(p);
         if (lane == 0) {
-            if (ok != 0) l = sched_apply(p, L.state + slot, sf, kbest, pa, pl);
+            if (ok != 0) l = sched_apply(p, L.state + slot, SchedFields{rec.y, rec.z, rec.w, has_prev}, kbest, pa, pl);
             len_out[b] = l;
         }
         l = __shfl_sync(full, l, 0);
-        const int32_t last = ok == 1 ? sm_tok[n - 1 - wlo] : CLK_SENT;
+        const int32_t last = ok == 1 ? win[(n - 1)  & (kRing - 1)] : CLK_SENT;
         warp_fuse(p, last, c, kbest, m_lane, l, block + (int64_t)b * kBlock);
     }
 }
@@ -491,13 +527,15 @@ __global__ void k_lookup_step(LookupDev L, const int32_t* __restrict__ slots, co
 // One CTA per request, launched as a programmatic dependent of the previous
 // launch in the stream (see k_lookup_step).
 template <bool FUSE>
-int launch_lookup_step(const LookupDev& L, const int32_t* slots, int32_t B, const int32_t* head,
+int launch_lookup_step(const clk_lookup* h, const int32_t* slots, int32_t B, const int32_t* head,
                        const int32_t* prev_a, const int32_t* prev_len, int32_t* draft, int32_t* k, int32_t* j,
                        int32_t* len, int32_t* block, cudaStream_t s)
 {
+    const LookupDev& L = h->dev;
+    const int32_t early = h->last_fused == kFusedGreedy ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
-    cfg.blockDim = dim3(32u * (unsigned)(L.nlev + kInsertWarps));
+    cfg.blockDim = dim3(32u * (unsigned)(L.nlev + kInsertWarps));  // <= 32 * kStepWarps
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -506,7 +544,7 @@ int launch_lookup_step(const LookupDev& L, const int32_t* slots, int32_t B, cons
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cuda_status(cudaLaunchKernelEx(&cfg, k_lookup_step<FUSE>, L, slots, head, prev_a, prev_len, draft, k, j,
-                                          len, block));
+                                          len, block, early));
 }
 
 }  // namespace clk
@@ -529,7 +567,7 @@ extern "C" int clk_lookup_init(clk_lookup* h, const int32_t* d_slots, int32_t B,
     k_copy_prompt<<<(unsigned)(B * copy_chunks), kThreads, 0, st>>>(L, d_slots, d_prompt, d_prompt_off,
                                                                      (int32_t)copy_chunks);
     if ((rc = launch_status()) != CLK_OK) return rc;
-    const uint64_t vec_total = (uint64_t)L.nlev * L.tsize / 2;  // uint4 stores per slot
+    const uint64_t vec_total = (uint64_t)L.nlev * L.tsize / 4;  // uint4 stores per slot
     const uint64_t per_chunk = kThreads * 16;
     const int64_t clear_chunks = (int64_t)((vec_total + per_chunk - 1) / per_chunk);
     k_clear_tables<<<(unsigned)(B * clear_chunks), kThreads, 0, st>>>(L, d_slots, (int32_t)clear_chunks, per_chunk);
@@ -558,7 +596,7 @@ extern "C" int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t
     if (rc != CLK_OK) return rc;
     if (B == 0) return CLK_OK;
     if (!ok_i32(d_slots) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j)) return CLK_EINVAL;
-    return launch_lookup_step<false>(h->dev, d_slots, B, nullptr, nullptr, nullptr, d_draft, d_k, d_j, nullptr,
+    return launch_lookup_step<false>(h, d_slots, B, nullptr, nullptr, nullptr, d_draft, d_k, d_j, nullptr,
                                      nullptr, (cudaStream_t)s);
 }
 
@@ -614,7 +652,7 @@ extern "C" int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int
         !ok_i32(d_prev_len) || !ok_i32(d_draft) || !ok_i32(d_k) || !ok_i32(d_j) || !ok_i32(d_len) ||
         !ok_i32(d_block))
         return CLK_EINVAL;
-    return launch_lookup_step<true>(h->dev, d_slots, B, d_head, d_prev_accept, d_prev_len, d_draft, d_k, d_j, d_len,
+    return launch_lookup_step<true>(h, d_slots, B, d_head, d_prev_accept, d_prev_len, d_draft, d_k, d_j, d_len,
                                     d_block, (cudaStream_t)s);
 }
 

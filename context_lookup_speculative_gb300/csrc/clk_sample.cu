@@ -1057,6 +1057,9 @@ extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, c
                                         size_t scratch_bytes, clk_stream_t s)
 {
     if (h == nullptr) return CLK_EINVAL;
+    // Its scratch is the caller's, one buffer for every step: the next
+    // proposal must not let the next verify start before this one completes.
+    h->last_fused = kFusedSampled;
     return sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_len_hint,
                         d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
                         (cudaStream_t)s);

@@ -287,6 +287,48 @@ __device__ __forceinline__ void block_prefix(int32_t B, Rows rows, int32_t* P, i
     __syncthreads();
 }
 
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// block_prefix computed by warps 1 .. kVWarps-1 only (named barrier 1), so
+// that warp 0 can do other work meanwhile.  Called by those warps only.
+template <typename Rows>
+__device__ __forceinline__ void rest_prefix(int32_t B, Rows rows, int32_t* P, int32_t* sm_warp)
+{
+    constexpr int kW = kVWarps - 1, kT = kW * 32;
+    const int t = threadIdx.x - 32, lane = t & 31, w = t >> 5;
+    const int32_t per = (B + kT - 1) / kT;
+    const int32_t b0 = min(B, t * per), b1 = min(B, b0 + per);
+    int32_t local = 0;
+    for (int32_t b = b0; b < b1; ++b) local += rows(b);
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm_warp[w] = incl;
+    named_barrier(1, kT);
+    if (w == 0) {
+        int32_t v = lane < kW ? sm_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane < kW) sm_warp[lane] = v;  // inclusive warp totals
+    }
+    named_barrier(1, kT);
+    int32_t run = (incl - local) + (w > 0 ? sm_warp[w - 1] : 0);
+    for (int32_t b = b0; b < b1; ++b) {
+        P[b] = run;
+        run += rows(b);
+    }
+    if (t == kT - 1) P[B] = sm_warp[kW - 1];
+}
+
 // P[b] = rows_after(L_b', base) summed over requests b' < b; P[B] = total.
 __device__ __forceinline__ void block_row_prefix(const int32_t* __restrict__ len, int32_t B, int32_t base, int32_t* P,
                                                  int32_t* sm_warp)
@@ -298,10 +340,7 @@ struct VerifySmem {
     unsigned long long red[kVWarps];
     int32_t warp[kVWarps];
     int32_t last;
-    int32_t count;
-    int32_t slot;  // fused: the finished request's slot
-    int32_t tok[kBlock];
-    int32_t flag[3];
+    int32_t slot;  // fused: the slot of the request a count may finish
 };
 
 // One row piece: this CTA's maximum over vectors [s0, s1) of row r of
@@ -319,50 +358,115 @@ __device__ __forceinline__ void piece_max(const VerifyArgs& a, int32_t b, int32_
 }
 
 // Request b is complete: argmax tokens, accepted count, emitted tokens; the
-// row keys and the counter go back to zero; fused, the tokens are committed.
-// Lb outside 1..16 gives the empty result.  Block-wide.
+// row keys and the counter go back to zero; fused, the tokens are committed
+// to slot `slot` (its history, the ring of its last tokens, its length and
+// counters).  Lb outside 1..16 gives the empty result.  Run by warp 0; the
+// row keys, the drafts and the slot's length and last block length arrive
+// in one round trip, and the commit is stores only.
+// Counter addition with release (this CTA's key merges before it) and acquire
+// (the merges of every CTA whose addition came before, for the finisher).
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
+// Loads issued as written (volatile): a finisher's loads are issued before
+// the barriers that follow them and consumed after.
+__device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ int32_t ld_cg_i32(const int32_t* p)
+{
+    int32_t v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// What a finisher reads, one value per lane of warp 0: lane r < 16 the key
+// of row r and the draft blk[r + 1]; lane 16 the slot's history length and
+// lane 17 its last block length (fused).
+struct FinLoads {
+    unsigned long long kv;
+    int32_t nxt;
+    int32_t sv;
+};
+
+template <bool FUSED>
+__device__ __forceinline__ FinLoads finalize_loads(const VerifyArgs& a, const LookupDev& L, int32_t b, int32_t slot)
+{
+    const int lane = threadIdx.x & 31;
+    FinLoads f;
+    f.kv = lane < kBlock ? ld_cg_u64(a.keys + (int64_t)b * kBlock + lane) : 0ull;
+    f.nxt = (lane + 1 < kBlock) ? ld_cg_i32(a.block + (int64_t)b * kBlock + lane + 1) : CLK_SENT;
+    f.sv = 0;
+    const bool sok = FUSED && slot >= 0 && slot < L.max_slots;
+    if (sok && lane == 16) f.sv = ld_cg_i32(&L.state[slot].n);
+    if (sok && lane == 17) f.sv = ld_cg_i32(&L.state[slot].cur_len);
+    return f;
+}
+
 template <bool FUSED>
 __device__ __forceinline__ void finalize(const VerifyArgs& a, const LookupDev& L, int32_t b, int32_t Lb,
-                                         VerifySmem& sm)
+                                         int32_t slot, bool have = false, FinLoads pre = FinLoads{0ull, CLK_SENT, 0})
 {
-    const int tid = threadIdx.x;
-    __threadfence();
+    if (threadIdx.x >= 32) return;
+    const unsigned full = 0xFFFFFFFFu;
+    const int lane = threadIdx.x;
+    const FinLoads f = have ? pre : finalize_loads<FUSED>(a, L, b, slot);
     const bool valid = len_ok(Lb);
-    if (tid < 32) {
-        const int lane = tid;
-        unsigned long long* kp = a.keys + (int64_t)b * kBlock;
-        int32_t g = CLK_SENT;
-        if (valid && lane < Lb) {
-            const unsigned long long kv = atomicAdd(kp + lane, 0ull);
-            g = (int32_t)(0xFFFFFFFFu - (uint32_t)kv);
-        }
-        if (lane < kBlock) kp[lane] = 0ull;
-        const int32_t nxt = (lane + 1 < kBlock) ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
-        // fused: the slot, loaded in the same round trip as the keys
-        const int32_t slot = (FUSED && lane == 31) ? a.slots[b] : -1;
-        const unsigned match = __ballot_sync(0xFFFFFFFFu, valid && lane < Lb - 1 && nxt == g);
-        const int32_t acc = __ffs(~match) - 1;
-        const int32_t out = (valid && lane <= acc) ? g : CLK_SENT;
-        if (lane < kBlock) {
-            a.argmax[(int64_t)b * kBlock + lane] = g;
-            a.out_tok[(int64_t)b * kBlock + lane] = out;
-            sm.tok[lane] = out;
-        }
-        if (lane == 0) {
-            a.accept[b] = valid ? acc : 0;
-            a.emitted[b] = valid ? acc + 1 : 0;
-            a.done[b] = 0ull;
-            sm.count = valid ? acc + 1 : -1;
-        }
-        if (FUSED && lane == 31) sm.slot = slot;
+    unsigned long long* kp = a.keys + (int64_t)b * kBlock;
+    const unsigned long long kv = f.kv;
+    const int32_t nxt = f.nxt;
+    const bool sok = FUSED && slot >= 0 && slot < L.max_slots;
+    const int32_t sv = f.sv;
+    const int32_t g = (valid && lane < Lb) ? (int32_t)(0xFFFFFFFFu - (uint32_t)kv) : CLK_SENT;
+    const unsigned match = __ballot_sync(full, valid && lane < Lb - 1 && nxt == g);
+    const int32_t acc = __ffs(~match) - 1;
+    const int32_t out = (valid && lane <= acc) ? g : CLK_SENT;
+    if (lane < kBlock) {
+        a.argmax[(int64_t)b * kBlock + lane] = g;
+        a.out_tok[(int64_t)b * kBlock + lane] = out;
+        kp[lane] = 0ull;
     }
-    __syncthreads();
-    if (FUSED) {
-        const int32_t slot = sm.slot;
-        if (sm.count < 0 || slot < 0 || slot >= L.max_slots) {
-            if (tid == 0) latch(L.status, CLK_EINVAL, b);
-        } else {
-            block_commit_tokens(L, slot, sm.tok, sm.count, sm.flag);
+    if (lane == 0) {
+        a.accept[b] = valid ? acc : 0;
+        a.emitted[b] = valid ? acc + 1 : 0;
+        a.done[b] = 0ull;
+    }
+    if (!FUSED) return;
+    const int32_t n = __shfl_sync(full, sv, 16);
+    const int32_t cur_len = __shfl_sync(full, sv, 17);
+    if (!valid || !sok) {
+        if (lane == 0) latch(L.status, CLK_EINVAL, b);
+        return;
+    }
+    // The commit of clk_lookup_append: count = acc + 1 <= 16 tokens.
+    const int32_t count = acc + 1;
+    const unsigned bad_tok = __ballot_sync(full, lane < count && !token_ok(L, out));
+    if ((int64_t)n + count > L.cap || bad_tok) {
+        if (lane == 0) latch(L.status, bad_tok && (int64_t)n + count <= L.cap ? CLK_EINVAL : CLK_ECAPACITY, slot);
+        return;
+    }
+    SlotState* st = L.state + slot;
+    if (lane < count) {
+        hist_of(L, slot)[n + lane] = out;
+        st->ring[(n + lane) & (kRing - 1)] = out;
+    }
+    if (lane == 0) {
+        st->n = n + count;
+        st->cur_len = 0;
+        if (cur_len != 0) {
+            // No other CTA touches this slot in the launch: additions whose
+            // result nothing waits for.
+            atomicAdd(reinterpret_cast<unsigned long long*>(&st->accepted), (unsigned long long)(count - 1));
+            atomicAdd(reinterpret_cast<unsigned long long*>(&st->emitted), (unsigned long long)count);
+            const int cls = (L.p.tail > 0 && cur_len == long_len(L.p)) ? 1 : 0;
+            atomicAdd(reinterpret_cast<unsigned long long*>(&st->accept_hist[cls][count - 1]), 1ull);
         }
     }
 }
@@ -374,11 +478,13 @@ __device__ __forceinline__ void piece_count(const VerifyArgs& a, const LookupDev
                                             unsigned long long need, int32_t Lb, VerifySmem& sm)
 {
     if (threadIdx.x == 0) {
-        __threadfence();
-        sm.last = (atomicAdd(a.done + b, add) + add == need) ? 1 : 0;
+        const unsigned long long c = atom_add_acq_rel(a.done + b, add) + add;
+        const int32_t slot = FUSED ? a.slots[b] : -1;  // loaded in the same round trip
+        sm.last = c == need ? 1 : 0;
+        sm.slot = slot;
     }
     __syncthreads();
-    if (sm.last) finalize<FUSED>(a, L, b, Lb, sm);
+    if (sm.last) finalize<FUSED>(a, L, b, Lb, sm.slot);
     __syncthreads();
 }
 
@@ -479,9 +585,11 @@ __device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b
 struct StepSmem {
     int32_t db[kVMaxDefer];             // deferred checks: request,
     unsigned long long dc[kVMaxDefer];  // the count its addition returned,
-    int32_t dl[kVMaxDefer];             // and (after the wait) its length
+    int32_t ds[kVMaxDefer];             // and its slot
     int32_t nd;
     int32_t waited;
+    int32_t acc_b;               // the request whose vectors this CTA has
+    unsigned long long acc_add;  // merged but not yet counted, and how many
 };
 
 template <int DT, bool VEC>
@@ -492,9 +600,6 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     extern __shared__ int32_t sm_prefix[];
     __shared__ VerifySmem sm;
     __shared__ StepSmem ss;
-    // Let the next launch (the next proposal) be scheduled; it waits for
-    // this grid to complete before it reads anything this grid writes.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int32_t B = a.B;
     int32_t* P1 = sm_prefix;
@@ -505,6 +610,8 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     if (tid == 0) {
         ss.nd = 0;
         ss.waited = 0;
+        ss.acc_b = -1;
+        ss.acc_add = 0ull;
     }
     block_prefix(B, [&a, base](int32_t b) { return predicted_rows(a, b, base); }, P1, sm.warp);
 
@@ -514,53 +621,108 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
         const int32_t pr = P1[b + 1] - P1[b];
         return (unsigned long long)(len_ok(Lb) ? max(Lb, pr) : pr) * (unsigned long long)vpr;
     };
-    // Block-wide: wait for the proposal launch (first call: also lay out the
-    // missed rows in P2), then decide the deferred counts.
+    // Thread 0: count the vectors of request b that this CTA merged (one
+    // addition per request and run of pieces; release for the merges,
+    // acquire for the finisher) and keep the count it returned, with the
+    // slot, for the check (made once the lengths are known).
+    auto defer = [&](int32_t b, unsigned long long add) {
+        const unsigned long long c = atom_add_acq_rel(a.done + b, add) + add;
+        const int32_t slot = a.slots[b];  // the same round trip
+        const int32_t i = ss.nd;
+        ss.db[i] = b;
+        ss.dc[i] = c;
+        ss.ds[i] = slot;
+        ss.nd = i + 1;
+    };
+    // Block-wide: count what is still pending; the first call waits for the
+    // proposal launch and lays out the missed rows in P2; then decide the
+    // deferred counts.
     auto flush = [&]() {
+        // (uniform: these were last written before a barrier)
+        if (ss.waited && ss.acc_b < 0 && ss.nd == 0) return;
+        if (tid == 0 && ss.acc_b >= 0) {
+            defer(ss.acc_b, ss.acc_add);
+            ss.acc_b = -1;
+            ss.acc_add = 0ull;
+        }
+        __syncthreads();
         if (!ss.waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            block_prefix(B, [&a, P1, Lc](int32_t b) {
-                const int32_t Lb = __ldcg(a.len + b);
-                Lc[b] = Lb;
-                return len_ok(Lb) ? max(0, Lb - (P1[b + 1] - P1[b])) : 0;
-            }, P2, sm.warp);
+            // Only now let the next launch (the next proposal) be scheduled:
+            // the proposal after it may then start the next fused verify at
+            // once, and by now the previous verify, which used the same half
+            // of the scratch as that one, has completed.  The next proposal
+            // waits for this grid before it reads anything this grid writes.
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            if (tid < 32) {
+                // A count that reached the request's predicted vectors
+                // finishes it whenever its length is within the prediction
+                // (the common case): warp 0 reads that length with the
+                // finisher's loads, in one round trip, and finishes at once,
+                // while the other warps lay out the missed rows.
+                int32_t spec = -1;
+                for (int32_t i = 0; i < ss.nd; ++i) {
+                    const int32_t b = ss.db[i];
+                    if (ss.dc[i] == (unsigned long long)(P1[b + 1] - P1[b]) * (unsigned long long)vpr) spec = i;
+                }
+                if (spec >= 0) {
+                    const int32_t b = ss.db[spec];
+                    const FinLoads pre = finalize_loads<true>(a, L, b, ss.ds[spec]);
+                    const int32_t Lb = ld_cg_i32(a.len + b);
+                    if (ss.dc[spec] == total(b, Lb)) {
+                        finalize<true>(a, L, b, Lb, ss.ds[spec], true, pre);
+                        if (tid == 0) ss.dc[spec] = 0ull;  // decided: no later check matches it
+                    }
+                }
+            } else {
+                rest_prefix(B, [&a, P1, Lc](int32_t b) {
+                    const int32_t Lb = __ldcg(a.len + b);
+                    Lc[b] = Lb;
+                    return len_ok(Lb) ? max(0, Lb - (P1[b + 1] - P1[b])) : 0;
+                }, P2, sm.warp);
+            }
             if (tid == 0) ss.waited = 1;
-        }
-        const int32_t nd = ss.nd;
-        if (tid < nd) ss.dl[tid] = Lc[ss.db[tid]];
-        __syncthreads();
-        for (int32_t i = 0; i < nd; ++i) {
-            if (ss.dc[i] == total(ss.db[i], ss.dl[i])) finalize<true>(a, L, ss.db[i], ss.dl[i], sm);
             __syncthreads();
         }
-        if (tid == 0) ss.nd = 0;
+        // The finisher is warp 0 alone: the remaining checks need no barrier.
+        if (tid < 32) {
+            const int32_t nd = ss.nd;
+            for (int32_t i = 0; i < nd; ++i) {
+                const int32_t b = ss.db[i];
+                if (ss.dc[i] == total(b, Lc[b])) finalize<true>(a, L, b, Lc[b], ss.ds[i]);
+            }
+            __syncwarp();
+            if (tid == 0) ss.nd = 0;
+        }
         __syncthreads();
     };
-    // The predicted-row vectors [from, to) of the flat range, piece by piece
-    // (one piece per row).  Before the wait the counts are deferred.
-    auto phase1 = [&](int64_t from, int64_t to) {
+    // Vectors [from, to) of the flat range laid out by prefix P (row r of
+    // request b at position P[b] + r - row0), rows row0 + ... of each
+    // request, piece by piece (one piece per row).  A CTA counts once per
+    // run of pieces of the same request: before the wait the count is
+    // deferred (checked once the lengths are known); after it the count is
+    // checked at once.
+    auto stream = [&](const int32_t* P, bool missed, int64_t from, int64_t to) {
         if (from >= to) return;
         int64_t ri = from / vpr;
-        int32_t b = owner_of(P1, B, ri);
+        int32_t b = owner_of(P, B, ri);
         int64_t lo = from;
         while (lo < to) {
-            while (P1[b + 1] <= ri) ++b;
+            while (P[b + 1] <= ri) ++b;
             const int64_t s0 = lo - ri * vpr;
             const int64_t s1 = min(to, (ri + 1) * vpr) - ri * vpr;
-            piece_max<DT, VEC>(a, b, (int32_t)(ri - P1[b]), s0, s1, sm);
-            if (ss.waited) {
-                piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, Lc[b]), Lc[b], sm);
-            } else {
-                if (tid == 0) {
-                    __threadfence();
-                    const unsigned long long add = (unsigned long long)(s1 - s0);
-                    ss.db[ss.nd] = b;
-                    ss.dc[ss.nd] = atomicAdd(a.done + b, add) + add;
-                    ss.nd += 1;
+            const int32_t row0 = missed ? P1[b + 1] - P1[b] : 0;
+            piece_max<DT, VEC>(a, b, row0 + (int32_t)(ri - P[b]), s0, s1, sm);
+            if (tid == 0) {
+                if (b != ss.acc_b) {
+                    if (ss.acc_b >= 0) defer(ss.acc_b, ss.acc_add);
+                    ss.acc_b = b;
+                    ss.acc_add = 0ull;
                 }
-                __syncthreads();
-                if (ss.nd == kVMaxDefer) flush();
+                ss.acc_add += (unsigned long long)(s1 - s0);
             }
+            __syncthreads();
+            if (ss.waited ? ss.nd > 0 : ss.nd >= kVMaxDefer - 1) flush();
             ri += 1;
             lo = ri * vpr;
         }
@@ -586,28 +748,14 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
     const int64_t lo = start(blockIdx.x);
     const int64_t hi = start(blockIdx.x + 1);
     const int64_t mid = (hi - lo >= kVSplitMin) ? lo + (hi - lo) / 2 : hi;
-    phase1(lo, mid);
+    stream(P1, false, lo, mid);
     flush();
     // This CTA's share of the rows the prediction missed.
     const int64_t total2 = (int64_t)P2[B] * vpr;
-    int64_t lo2 = total2 * blockIdx.x / gridDim.x;
-    const int64_t hi2 = total2 * (blockIdx.x + 1) / gridDim.x;
-    if (lo2 < hi2) {
-        int64_t ri = lo2 / vpr;
-        int32_t b = owner_of(P2, B, ri);
-        while (lo2 < hi2) {
-            while (P2[b + 1] <= ri) ++b;
-            const int32_t pr = P1[b + 1] - P1[b];
-            const int64_t s0 = lo2 - ri * vpr;
-            const int64_t s1 = min(hi2, (ri + 1) * vpr) - ri * vpr;
-            piece_max<DT, VEC>(a, b, pr + (int32_t)(ri - P2[b]), s0, s1, sm);
-            const int32_t Lb = Lc[b];
-            piece_count<true>(a, L, b, (unsigned long long)(s1 - s0), total(b, Lb), Lb, sm);
-            ri += 1;
-            lo2 = ri * vpr;
-        }
-    }
-    phase1(mid, hi);
+    stream(P2, true, total2 * blockIdx.x / gridDim.x, total2 * (blockIdx.x + 1) / gridDim.x);
+    flush();
+    stream(P1, false, mid, hi);
+    flush();
 }
 
 // Resident CTAs per SM of kernel `Kern` and the SM count, packed as
@@ -794,15 +942,23 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.accept = d_accept;
     a.emitted = d_emitted;
     a.out_tok = d_out_tok;
-    a.keys = h->dev.vkeys;
-    a.done = h->dev.vdone;
+    const int par = h->vparity;
+    a.keys = h->dev.vkeys + (size_t)par * (size_t)h->dev.max_slots * kBlock;
+    a.done = h->dev.vdone + (size_t)par * (size_t)h->dev.max_slots;
     a.slots = d_slots;
     // The proposal launch this one overlaps runs one CTA of 14 warps per
     // request (at most 64 registers a thread): each such CTA leaves room for
     // 2 of the 4 CTAs of this launch on its SM.
     const int sms = num_sms();
     a.late = 2 * (B < sms ? B : (sms > 0 ? sms : 0));
-    return verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
+    rc = verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
+    if (rc == CLK_OK) {
+        h->vparity ^= 1;
+        h->last_fused = kFusedGreedy;
+    } else {
+        h->last_fused = kFusedNone;
+    }
+    return rc;
 }
 
 // ---------------------------------------------------------------------------

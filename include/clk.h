@@ -141,9 +141,12 @@ CLK_API const char* clk_status_string(int code);
 /* Bytes of device workspace for `max_slots` requests whose histories hold up
  * to `max_hist` tokens each (prompt plus every committed token).  The
  * workspace holds the histories, the per-request k-gram index (one
- * open-addressing table of 2^ceil(log2(2*max_hist)) 8-byte entries per match
- * length min_k..max_k), the scheduler state, the counters, the fused
- * verify's scratch and the status word.  Returns CLK_EINVAL for bad sizes. */
+ * open-addressing table of 2^ceil(log2(2*max_hist)) 4-byte entries per match
+ * length min_k..max_k: 8 * 9 = 72 bytes of index per history token at the
+ * defaults, before each table is rounded up to a power of two), the
+ * scheduler state with a copy of each history's last 64 tokens, the
+ * counters, the fused verify's scratch and the status word.  Returns
+ * CLK_EINVAL for bad sizes. */
 CLK_API int clk_lookup_workspace_bytes(const clk_params* p, int32_t max_slots, int64_t max_hist, size_t* bytes);
 
 /* Creates a host handle over a caller-owned device workspace of at least
@@ -238,7 +241,10 @@ CLK_API int clk_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, con
  * request).  Bit-identical to the three calls.  Like clk_lookup_propose it
  * first waits for the preceding launch on the stream (programmatic dependent
  * launch) and indexes the tokens that clk_verify_append committed since the
- * slot's last proposal. */
+ * slot's last proposal.  When the handle's last fused verify was
+ * clk_verify_append, the launch lets the next launch on the stream (the
+ * step's clk_verify_append, which starts streaming its predicted rows) begin
+ * before that wait; otherwise only after it. */
 CLK_API int clk_propose_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, const int32_t* d_head,
                                    const int32_t* d_prev_accept, const int32_t* d_prev_len, int32_t* d_draft,
                                    int32_t* d_k, int32_t* d_j, int32_t* d_len, int32_t* d_block, clk_stream_t s);
@@ -316,7 +322,11 @@ CLK_API int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_
  * the same results, a good one saves a second pass.  So the logits must
  * already be complete when this call is made (as after any ordinary kernel
  * or copy on the stream) and must hold every predicted row (16 rows per
- * request serve any hint). */
+ * request serve any hint).  Consecutive calls on a handle alternate between
+ * two halves of the scratch in the workspace, so that a call may start
+ * streaming while the previous one finishes (clk_propose_fuse_sched between
+ * them lets it); a call lets the next launch on the stream start only after
+ * its own wait. */
 CLK_API int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                               int64_t row_stride, int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block,
                               const int32_t* d_len, const int32_t* d_len_hint, int32_t* d_argmax,

@@ -80,8 +80,8 @@ def test_workspace_sizing(clk):
     assert rc == 0 and small > 0
     rc, big = ws(64, 40192)
     assert rc == 0
-    # 9 tables of 2^17 8-byte entries per slot dominate: about 604 MB for 64 slots
-    assert 9 * 2 ** 17 * 8 * 64 < big < 1.1 * 9 * 2 ** 17 * 8 * 64 + 64 * 40192 * 4 * 1.1
+    # 9 tables of 2^17 4-byte entries per slot dominate: about 302 MB for 64 slots
+    assert 9 * 2 ** 17 * 4 * 64 < big < 1.1 * 9 * 2 ** 17 * 4 * 64 + 64 * 40192 * 4 * 1.1
     assert ws(0, 100)[0] == clk.EINVAL
     assert ws(1, 0)[0] == clk.EINVAL
     assert L.clk_lookup_workspace_bytes(None, 1, 100, ctypes.byref(n)) == clk.EINVAL
