@@ -22,6 +22,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "clk.h"
 #include "clk_device.cuh"
 #include "clk_host.h"
@@ -764,14 +766,20 @@ template <auto Kern>
 int occupancy(size_t smem, int* packed)
 {
     constexpr int kDevices = 64;
-    static int cache[kDevices] = {0};  // one table per kernel (template argument)
+    // One table per kernel (template argument).  Calls may come from several
+    // host threads: the entries are atomic (any thread may fill an entry;
+    // they all compute the same value).
+    static std::atomic<int> cache[kDevices];
     const auto kern = Kern;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
     const bool cacheable = dev >= 0 && dev < kDevices && smem <= 4096;
-    if (cacheable && cache[dev] > 0) {
-        *packed = cache[dev];
-        return CLK_OK;
+    if (cacheable) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *packed = c;
+            return CLK_OK;
+        }
     }
     int occ = 0;
     if (smem > 48 * 1024 &&
@@ -785,7 +793,7 @@ int occupancy(size_t smem, int* packed)
     const int sms = num_sms();
     if (sms <= 0 || sms >= 1024) return CLK_ECUDA;
     *packed = occ * 1024 + sms;
-    if (cacheable) cache[dev] = *packed;
+    if (cacheable) cache[dev].store(*packed, std::memory_order_relaxed);
     return CLK_OK;
 }
 
@@ -972,6 +980,8 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
 static __device__ __align__(256) unsigned long long
     g_static_verify_scratch[(size_t)CLK_STATIC_VERIFY_MAX_BATCH * (kBlock + 1)];
 
+#include <cuda.h>
+
 #include <mutex>
 
 namespace {
@@ -979,18 +989,53 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void* g_static_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_static_ctx[kMaxDevices] = {0};  // id of the context the address belongs to
 
-// Device address of the static scratch on the current device (looked up on
-// the first call on that device), or nullptr on a CUDA error.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context (0 on failure), through the
+// driver entry points the runtime exposes (no link against the driver).
+unsigned long long current_context_id()
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (get_current == nullptr || get_id == nullptr) {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess)
+            return 0;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+        get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the static scratch in the current context.  It is
+// looked up on the first call on each device, and again whenever the
+// device's current context is another one than at the last lookup (after
+// cudaDeviceReset, say, the module is loaded anew, possibly elsewhere).
+// nullptr on a CUDA error.
 void* static_scratch_on_current_device()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const unsigned long long ctx = current_context_id();  // 0: none current yet on this thread
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (g_static_ptr[dev] == nullptr) {
+    if (ctx == 0 || g_static_ptr[dev] == nullptr || g_static_ctx[dev] != ctx) {
+        // (the lookup also makes the device's primary context current)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
+        const unsigned long long now = current_context_id();
+        if (now == 0) return nullptr;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = now;
     }
     return g_static_ptr[dev];
 }
@@ -1002,10 +1047,10 @@ extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int
                                         int32_t* d_argmax, int32_t* d_accept, int32_t* d_emitted,
                                         int32_t* d_out_tok, clk_stream_t s)
 {
+    if (B > CLK_STATIC_VERIFY_MAX_BATCH) return CLK_ECAPACITY;  // before the other checks: any larger B
     int rc = verify_check(d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_argmax, d_accept,
                           d_emitted, d_out_tok);
     if (rc != CLK_OK) return rc;
-    if (B > CLK_STATIC_VERIFY_MAX_BATCH) return CLK_ECAPACITY;
     if (B == 0) return CLK_OK;
     void* scratch = static_scratch_on_current_device();
     if (scratch == nullptr) return CLK_ECUDA;
@@ -1033,3 +1078,15 @@ extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int
     LookupDev none = {};
     return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
 }
+
+#ifdef CLK_TEST_HOOKS
+// Test builds only (never in the shipped library): fill the static scratch
+// with a byte, so that a test can show that clk_verify_greedy_static clears
+// what it needs before it uses it.
+extern "C" CLK_API int clk_test_fill_static_scratch(int byte, clk_stream_t s)
+{
+    void* scratch = static_scratch_on_current_device();
+    if (scratch == nullptr) return CLK_ECUDA;
+    return cuda_status(cudaMemsetAsync(scratch, byte, sizeof(g_static_verify_scratch), (cudaStream_t)s));
+}
+#endif

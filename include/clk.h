@@ -290,10 +290,11 @@ CLK_API int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t row_s
  * allocates nothing: its scratch is a fixed array of
  * CLK_STATIC_VERIFY_MAX_BATCH * 17 * 8 bytes (139,264 bytes) inside the
  * library, which every GPU that loads the library keeps until the process
- * exits.  B above CLK_STATIC_VERIFY_MAX_BATCH returns CLK_ECAPACITY and
- * launches nothing.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Each call clears the part of the array it uses on its
+ * exits.  B above CLK_STATIC_VERIFY_MAX_BATCH returns CLK_ECAPACITY (any such
+ * B, also beyond CLK_MAX_BATCH) and launches nothing.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress),
+ * and so does the first call after the device's context changed (after
+ * cudaDeviceReset, say); make that first call before any stream capture.  Each call clears the part of the array it uses on its
  * stream and then launches the verify kernel.  All calls share the one
  * array, so calls whose executions overlap on the GPU (other streams, other
  * threads) race and corrupt each other's results: serialise them.  The
