@@ -547,6 +547,13 @@ int launch_lookup_step(const clk_lookup* h, const int32_t* slots, int32_t B, con
                                           len, block, early));
 }
 
+int proposal_cta_regs(int nlev)
+{
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, k_lookup_step<true>) != cudaSuccess) return -1;
+    return cta_regs(fa.numRegs, 32 * (nlev + kInsertWarps));
+}
+
 }  // namespace clk
 
 using namespace clk;

@@ -30,6 +30,7 @@
 // stateless entry point; k_sample_step, fused with the token commit, starts
 // streaming predicted rows before the proposal launch it depends on ends.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -921,7 +922,7 @@ int sample_sizes(int32_t dtype, int32_t V, int32_t B, int32_t* S, size_t* bytes)
 template <int DT, bool VEC, bool FUSED>
 int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
 {
-    static int cache[64] = {0};  // resident CTAs per SM, per device
+    static std::atomic<int> cache[64];  // resident CTAs per SM, per device (calls from any host thread)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
     const size_t smem = (size_t)(FUSED ? 3 : 1) * (a.B + 1) * sizeof(int32_t);
@@ -929,20 +930,23 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CLK_ECUDA;
-    int occ = (dev >= 0 && dev < 64 && smem <= 4096) ? cache[dev] : 0;
+    int occ = (dev >= 0 && dev < 64 && smem <= 4096) ? cache[dev].load(std::memory_order_relaxed) : 0;
     if (occ <= 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSThreads, smem <= 4096 ? 4096 : smem) !=
                 cudaSuccess ||
             occ < 1)
             return CLK_ECUDA;
-        if (dev >= 0 && dev < 64 && smem <= 4096) cache[dev] = occ;
+        if (dev >= 0 && dev < 64 && smem <= 4096) cache[dev].store(occ, std::memory_order_relaxed);
     }
     const int sms = num_sms();
     if (sms <= 0) return CLK_ECUDA;
+    SampleArgs args = a;
+    if (FUSED && a.late > 0)  // CTAs dispatched behind the proposal launch's CTAs (see clk_verify.cu)
+        args.late = displaced_by_proposal<k_sample_step<DT, VEC>>(kSThreads, Ldev.nlev, occ) * (a.B < sms ? a.B : sms);
     const int64_t segs = (int64_t)a.B * kBlock * a.S;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)occ * sms, segs));
     if (!FUSED) {
-        kern<<<(unsigned)grid, kSThreads, smem, s>>>(a, Ldev);
+        kern<<<(unsigned)grid, kSThreads, smem, s>>>(args, Ldev);
         return launch_status();
     }
     cudaLaunchConfig_t cfg = {};
@@ -955,7 +959,7 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, a, Ldev));
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, Ldev));
 }
 
 }  // namespace
@@ -1014,11 +1018,9 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     a.done = static_cast<uint32_t*>(d_scratch);
     a.part = reinterpret_cast<float2*>(static_cast<char*>(d_scratch) + align_up((size_t)B * sizeof(uint32_t), 16));
     a.slots = d_slots;
-    // Fused: the proposal launch this one overlaps runs one CTA of 14 warps
-    // per request, which leaves room for 2 of the 4 CTAs of this launch on
-    // its SM.
-    const int sms = num_sms();
-    a.late = h != nullptr ? 2 * (B < sms ? B : (sms > 0 ? sms : 0)) : 0;
+    // Fused: it may overlap the proposal launch before it; the count of its
+    // CTAs that start behind that launch is worked out at launch.
+    a.late = h != nullptr ? 1 : 0;
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
     const bool bf = dtype == CLK_DTYPE_BF16;

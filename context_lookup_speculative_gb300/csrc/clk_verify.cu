@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 // other CTAs stream, and the launch ends soon after its last bytes arrive.
 // A CTA with a short share (small batches) streams all of it first.
 constexpr int kVMaxDefer = 32;
-constexpr int64_t kVSplitMin = 16 * kVThreads;  // vectors: shares below this are not split
+constexpr int64_t kVSplitMin = 64 * kVThreads;  // vectors: shares below this are not split
 constexpr int64_t kLateBytes = 60ll << 20;      // HBM bytes in the ~10 us a proposal launch runs
 
 // Rows read before the wait for request b.
@@ -829,6 +829,19 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
     auto kern = k_verify_step<DT, VEC>;
     int rc = verify_grid<k_verify_step<DT, VEC>>(smem, a.B, vpr, &grid);
     if (rc != CLK_OK) return rc;
+    VerifyArgs args = a;
+    if (a.late > 0) {
+        // a.late > 0: the call follows a proposal launch it may overlap.
+        // The last CTAs to be dispatched wait for the proposal's CTAs to
+        // leave: the verify CTAs each of those displaces, on min(B, SMs) SMs.
+        int packed = 0;
+        if (occupancy<k_verify_step<DT, VEC>>(smem, &packed) == CLK_OK) {
+            const int occ = packed / 1024, sms = packed % 1024;
+            args.late = displaced_by_proposal<k_verify_step<DT, VEC>>(kVThreads, L.nlev, occ) * (a.B < sms ? a.B : sms);
+        } else {
+            args.late = 0;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kVThreads);
@@ -839,7 +852,7 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, a, L));
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, L));
 }
 
 int verify_dispatch(const VerifyArgs& a, int32_t dtype, bool fused, const LookupDev& L, cudaStream_t s)
@@ -954,11 +967,9 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.keys = h->dev.vkeys + (size_t)par * (size_t)h->dev.max_slots * kBlock;
     a.done = h->dev.vdone + (size_t)par * (size_t)h->dev.max_slots;
     a.slots = d_slots;
-    // The proposal launch this one overlaps runs one CTA of 14 warps per
-    // request (at most 64 registers a thread): each such CTA leaves room for
-    // 2 of the 4 CTAs of this launch on its SM.
-    const int sms = num_sms();
-    a.late = 2 * (B < sms ? B : (sms > 0 ? sms : 0));
+    // It may overlap the proposal launch before it: the count of its CTAs
+    // that start behind that launch is worked out at launch.
+    a.late = 1;
     rc = verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
     if (rc == CLK_OK) {
         h->vparity ^= 1;
