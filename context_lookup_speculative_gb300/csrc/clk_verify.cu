@@ -128,23 +128,24 @@ struct Elem<CLK_DTYPE_F32> {
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
-// Loads vectors base + u * kVThreads (u < kUnroll) that lie below v1.
+// Loads vectors base + u * kVThreads (u < U) that lie below v1.
 // Vector indices inside a row fit in 32 bits (V < 2^31).
+template <int U>
 __device__ __forceinline__ void load_group(const uint4* row, int32_t base, int32_t v1, uint4* x)
 {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int32_t vi = base + u * kVThreads;
         if (vi < v1) x[u] = ld_stream(row + vi);
     }
 }
 
-template <int DT>
+template <int DT, int U>
 __device__ __forceinline__ void reduce_group(const uint4* x, int32_t base, int32_t v1, float& best, int32_t& bvi,
                                              uint4& bvec, uint32_t& nanacc)
 {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int32_t vi = base + u * kVThreads;
         if (vi < v1) {
             const float m = Elem<DT>::vec_max(x[u], nanacc);
@@ -158,16 +159,16 @@ __device__ __forceinline__ void reduce_group(const uint4* x, int32_t base, int32
 }
 
 // This thread's packed key over vectors [v0, v1) of a row (vector path).
-// Two register groups alternate: the next group's loads are issued before
-// the current group is reduced, so up to 2 x kUnroll 16-byte loads per
-// thread are in flight.  The index inside the winning vector is recovered
-// from the vector kept in registers.
-template <int DT>
+// Two register groups of U vectors alternate: the next group's loads are
+// issued before the current group is reduced, so up to 2 x U 16-byte loads
+// per thread are in flight.  The index inside the winning vector is
+// recovered from the vector kept in registers.
+template <int DT, int U = kUnroll>
 __device__ __forceinline__ unsigned long long scan_vec(const void* row_ptr, int32_t v0, int32_t v1)
 {
     using E = Elem<DT>;
     constexpr int W = E::W;
-    constexpr int32_t S = kUnroll * kVThreads;
+    constexpr int32_t S = U * kVThreads;
     const uint4* row = reinterpret_cast<const uint4*>(row_ptr);
     const int32_t first = v0 + (int32_t)threadIdx.x;
     if (first >= v1) return 0ull;
@@ -175,14 +176,14 @@ __device__ __forceinline__ unsigned long long scan_vec(const void* row_ptr, int3
     int32_t bvi = -1;
     uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
     uint32_t nanacc = 0u;
-    uint4 a[kUnroll], b[kUnroll];
-    load_group(row, first, v1, a);
+    uint4 a[U], b[U];
+    load_group<U>(row, first, v1, a);
     for (int32_t base = first; base < v1; base += 2 * S) {
-        load_group(row, base + S, v1, b);
-        reduce_group<DT>(a, base, v1, best, bvi, bvec, nanacc);
+        load_group<U>(row, base + S, v1, b);
+        reduce_group<DT, U>(a, base, v1, best, bvi, bvec, nanacc);
         if (base + S >= v1) break;
-        load_group(row, base + 2 * S, v1, a);
-        reduce_group<DT>(b, base + S, v1, best, bvi, bvec, nanacc);
+        load_group<U>(row, base + 2 * S, v1, a);
+        reduce_group<DT, U>(b, base + S, v1, best, bvi, bvec, nanacc);
     }
     if (nanacc & E::kNanMask) {
         // Rare path: the first NaN of this thread's elements.
@@ -347,14 +348,14 @@ struct VerifySmem {
 
 // One row piece: this CTA's maximum over vectors [s0, s1) of row r of
 // request b, merged into the row's key.
-template <int DT, bool VEC>
+template <int DT, bool VEC, int U = kUnroll>
 __device__ __forceinline__ void piece_max(const VerifyArgs& a, int32_t b, int32_t r, int64_t s0, int64_t s1,
                                           VerifySmem& sm)
 {
     using T = typename Elem<DT>::T;
     const char* row = static_cast<const char*>(a.logits) +
                       ((int64_t)b * a.req_stride + (int64_t)r * a.row_stride) * (int64_t)sizeof(T);
-    unsigned long long key = VEC ? scan_vec<DT>(row, (int32_t)s0, (int32_t)s1) : scan_scalar<DT>(row, s0, s1);
+    unsigned long long key = VEC ? scan_vec<DT, U>(row, (int32_t)s0, (int32_t)s1) : scan_scalar<DT>(row, s0, s1);
     key = block_max_u64(key, sm.red);
     if (threadIdx.x == 0) atomicMax(a.keys + (int64_t)b * kBlock + r, key);
 }
@@ -575,7 +576,9 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 // A CTA with a short share (small batches) streams all of it first.
 constexpr int kVMaxDefer = 32;
 constexpr int64_t kVSplitMin = 64 * kVThreads;  // vectors: shares below this are not split
-constexpr int64_t kLateBytes = 60ll << 20;      // HBM bytes in the ~10 us a proposal launch runs
+constexpr int64_t kLateBytes = 60ll << 20;      // HBM bytes streamed before the late CTAs start (measured)
+constexpr int64_t kVSmallBytes = 32ll << 20;     // logits (16 rows a request) of a latency-bound launch
+constexpr int kVSmallPerSm = 2;                  // its CTAs per SM
 
 // Rows read before the wait for request b.
 __device__ __forceinline__ int32_t predicted_rows(const VerifyArgs& a, int32_t b, int32_t base)
@@ -594,9 +597,12 @@ struct StepSmem {
     unsigned long long acc_add;  // merged but not yet counted, and how many
 };
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
+// DEEP: the variant for latency-bound launches (few logits): two CTAs per
+// SM, twice the loads in flight per thread.
+template <int DT, bool VEC, bool DEEP>
+__global__ void __launch_bounds__(kVThreads, DEEP ? 2 : 4) k_verify_step(VerifyArgs a, LookupDev L)
 {
+    constexpr int U = DEEP ? 2 * kUnroll : kUnroll;
     // P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then Lc[B + 1]
     // (after the wait: each request's length, read once)
     extern __shared__ int32_t sm_prefix[];
@@ -714,7 +720,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, Look
             const int64_t s0 = lo - ri * vpr;
             const int64_t s1 = min(to, (ri + 1) * vpr) - ri * vpr;
             const int32_t row0 = missed ? P1[b + 1] - P1[b] : 0;
-            piece_max<DT, VEC>(a, b, row0 + (int32_t)(ri - P[b]), s0, s1, sm);
+            piece_max<DT, VEC, U>(a, b, row0 + (int32_t)(ri - P[b]), s0, s1, sm);
             if (tid == 0) {
                 if (b != ss.acc_b) {
                     if (ss.acc_b >= 0) defer(ss.acc_b, ss.acc_add);
@@ -812,6 +818,44 @@ int verify_grid(size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
     return CLK_OK;
 }
 
+// Launches the fused step with at most `per_sm_cap` CTAs per SM (0: as many
+// as fit).
+template <int DT, bool VEC, bool DEEP>
+int launch_step(const VerifyArgs& a, const LookupDev& L, size_t smem, int64_t vpr, int per_sm_cap, cudaStream_t s)
+{
+    auto kern = k_verify_step<DT, VEC, DEEP>;
+    int64_t grid = 0;
+    int rc = verify_grid<k_verify_step<DT, VEC, DEEP>>(smem, a.B, vpr, &grid);
+    if (rc != CLK_OK) return rc;
+    int packed = 0;
+    rc = occupancy<k_verify_step<DT, VEC, DEEP>>(smem, &packed);
+    if (rc != CLK_OK) return rc;
+    const int occ = packed / 1024, sms = packed % 1024;
+    if (per_sm_cap > 0 && grid > (int64_t)per_sm_cap * sms) grid = (int64_t)per_sm_cap * sms;
+    VerifyArgs args = a;
+    if (a.late > 0) {
+        // a.late > 0: the call follows a proposal launch it may overlap.  The
+        // proposal's CTAs (one a request, on min(B, SMs) SMs) each take the
+        // place of some CTAs of this launch; the CTAs beyond the places left
+        // (dispatched last) start only when the proposal's leave.
+        const int64_t taken = (int64_t)displaced_by_proposal<k_verify_step<DT, VEC, DEEP>>(kVThreads, L.nlev, occ) *
+                              (a.B < sms ? a.B : sms);
+        const int64_t late = grid - ((int64_t)occ * sms - taken);
+        args.late = late > 0 ? (int32_t)late : 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kVThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, L));
+}
+
 template <int DT, bool VEC, bool FUSED>
 int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
 {
@@ -826,33 +870,24 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
         kern<<<(unsigned)grid, kVThreads, smem, s>>>(a, L);
         return launch_status();
     }
-    auto kern = k_verify_step<DT, VEC>;
-    int rc = verify_grid<k_verify_step<DT, VEC>>(smem, a.B, vpr, &grid);
+    // A launch whose logits are few (at most kVSmallBytes for all 16 rows of
+    // every request) is latency-bound.  It keeps to two CTAs per SM, so that
+    // the next step's proposal finds room beside it; where a thread then has
+    // more vectors to read than the two register groups of the ordinary
+    // kernel hold, the DEEP variant (two CTAs per SM by its register use)
+    // keeps twice as many loads in flight.
+    const int64_t max_work = (int64_t)a.B * kBlock * vpr;
+    const int64_t max_bytes = max_work * (int64_t)(VEC ? 16 : sizeof(typename Elem<DT>::T));
+    if (max_bytes > kVSmallBytes) return launch_step<DT, VEC, false>(a, L, smem, vpr, 0, s);
+    int packed = 0;
+    const int rc = occupancy<k_verify_step<DT, VEC, false>>(smem, &packed);
     if (rc != CLK_OK) return rc;
-    VerifyArgs args = a;
-    if (a.late > 0) {
-        // a.late > 0: the call follows a proposal launch it may overlap.
-        // The last CTAs to be dispatched wait for the proposal's CTAs to
-        // leave: the verify CTAs each of those displaces, on min(B, SMs) SMs.
-        int packed = 0;
-        if (occupancy<k_verify_step<DT, VEC>>(smem, &packed) == CLK_OK) {
-            const int occ = packed / 1024, sms = packed % 1024;
-            args.late = displaced_by_proposal<k_verify_step<DT, VEC>>(kVThreads, L.nlev, occ) * (a.B < sms ? a.B : sms);
-        } else {
-            args.late = 0;
-        }
+    const int sms = packed % 1024;
+    if constexpr (VEC) {
+        if (max_work > (int64_t)kVSmallPerSm * sms * kVThreads * 2 * kUnroll)
+            return launch_step<DT, VEC, true>(a, L, smem, vpr, 0, s);
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kVThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, L));
+    return launch_step<DT, VEC, false>(a, L, smem, vpr, kVSmallPerSm, s);
 }
 
 int verify_dispatch(const VerifyArgs& a, int32_t dtype, bool fused, const LookupDev& L, cudaStream_t s)
