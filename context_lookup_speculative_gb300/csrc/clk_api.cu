@@ -15,7 +15,7 @@ using namespace clk;
 namespace {
 
 struct Layout {
-    size_t status, state, vkeys, vdone, skeys, hist, tab, total;
+    size_t status, state, vkeys, vdone, skeys, ins, hist, tab, total;
     int64_t hstride;
     uint64_t tsize;
     int32_t nlev;
@@ -64,6 +64,8 @@ int layout_of(const clk_params* p, int32_t max_slots, int64_t max_hist, Layout* 
     off = align_up(off + 2 * ns * sizeof(unsigned long long), kAlign);
     L.skeys = off;
     off = align_up(off + ns * sizeof(unsigned long long), kAlign);
+    L.ins = off;
+    off = align_up(off + 2 * ns * sizeof(int4), kAlign);  // two halves by tag parity
     L.hist = off;
     off = align_up(off + ns * (size_t)L.hstride * sizeof(int32_t), kAlign);
     L.tab = off;
@@ -143,6 +145,7 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     D.vkeys = reinterpret_cast<unsigned long long*>(base + L.vkeys);
     D.vdone = reinterpret_cast<unsigned long long*>(base + L.vdone);
     D.skeys = reinterpret_cast<unsigned long long*>(base + L.skeys);
+    D.ins = reinterpret_cast<int4*>(base + L.ins);
     D.hist = reinterpret_cast<int32_t*>(base + L.hist);
     D.tab = reinterpret_cast<uint32_t*>(base + L.tab);
     D.hstride = L.hstride;
@@ -160,6 +163,9 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     hh->device = 0;
     hh->vparity = 0;
     hh->last_fused = kFusedNone;
+    hh->ptag = 0;
+    hh->defer_tag = 0;
+    hh->vsince = 0;
     cudaGetDevice(&hh->device);
     *h = hh;
     return CLK_OK;
@@ -168,6 +174,7 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
 extern "C" int clk_lookup_reset(clk_lookup* h, clk_stream_t s)
 {
     if (!handle_ok(h)) return CLK_ESTATE;
+    h->defer_tag = 0;
     return cuda_status(cudaMemsetAsync(h->ws, 0, h->bytes, (cudaStream_t)s));
 }
 

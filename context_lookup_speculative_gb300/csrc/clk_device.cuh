@@ -7,6 +7,7 @@
 //   vdone   u64[2][max_slots]           fused verify: vectors verified per request
 //                                       (two halves: consecutive fused verifies alternate)
 //   skeys   u64[max_slots]              full-scan lookup: best (length, position) per request
+//   ins     int4[2][max_slots]          per batch position: insertions a proposal left (see below)
 //   hist    int32[max_slots][hstride]   token histories
 //   tab     u32[max_slots][nlev][tsize] k-gram index, one table per match length
 //
@@ -31,11 +32,15 @@
 // Deferred inserts.  A slot records nidx, the history length up to which its
 // tables are complete: they hold every k-gram ending at q <= nidx - 2.  The
 // fused verify only writes the emitted tokens (n grows, nidx does not); the
-// next proposal launch indexes the pending end positions nidx-1 .. n-2 in
-// dedicated warps while its lookup warps check those pending positions
-// directly against the suffix (they are the most recent candidates) and the
-// tables for everything older.  The answer is the same as with a complete
-// index, and the insert latency leaves the verify kernel.
+// end positions nidx-1 .. n-2 stay pending until they are indexed, and every
+// proposal checks the pending positions directly against the suffix (they
+// are the most recent candidates) and the tables for everything older, so
+// the answer is the same as with a complete index.  The proposal launch
+// indexes them in dedicated warps: after its wait, beside its lookup warps;
+// or, for small batches, it leaves at most kDeferMax of them to the next
+// proposal launch, whose dedicated warps index them before that launch's
+// wait, while the verify in between finishes.  nidx only grows (atomicMax)
+// between initialisations.
 //
 // The last kRing tokens of every history are also kept in the slot's record
 // (ring[p mod kRing] = h[p]), next to n and the scheduler state, so that the
@@ -75,6 +80,7 @@ struct LookupDev {
     unsigned long long* vkeys;
     unsigned long long* vdone;
     unsigned long long* skeys;  // full-scan lookup: packed (length, end + 1) per batch position
+    int4* ins;                  // per batch position: index insertions left by the proposal launch
     int32_t* hist;
     uint32_t* tab;
     int64_t hstride;  // int32 elements per history
@@ -376,7 +382,8 @@ __device__ __forceinline__ bool block_commit_tokens(const LookupDev& L, int32_t 
 
 // Index every k-gram (all levels) that ends at q in [q_lo, q_hi], reading the
 // tokens from the history.  Work items (q, level) are spread over the
-// `nthr` threads whose rank is `rank`.
+// `nthr` threads whose rank is `rank`.  WIDE: probe 8 entries a round trip.
+template <bool WIDE = false>
 __device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, int32_t q_lo, int32_t q_hi,
                                             int32_t rank, int32_t nthr)
 {
@@ -399,9 +406,21 @@ __device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, in
             }
         }
         auto same = [&](int32_t pos) { return kgram_at(h, pos, w, k); };
-        if (!index_insert(L, table_of(L, slot, lvl), kg_final(acc, k), q, same))
-            latch(L.status, CLK_ECAPACITY, slot);
+        const bool ok = WIDE ? index_insert8(L, table_of(L, slot, lvl), kg_final(acc, k), q, same)
+                             : index_insert(L, table_of(L, slot, lvl), kg_final(acc, k), q, same);
+        if (!ok) latch(L.status, CLK_ECAPACITY, slot);
     }
 }
 
+// Insertions left by a proposal launch to the next one: it records
+// {tag, slot, from, n} in ins[tag & 1][b] (tag != 0 names the launch): the
+// k-grams ending at [max(from - 1, 0), n - 2] are still to be indexed, and
+// nidx may then rise to n.  The next proposal launch, when it follows a
+// fused greedy verify (so the recording launch has completed), takes the
+// records of that tag before its own wait, while the verify finishes.  A
+// proposal leaves at most kDeferMax positions this way, so that after one
+// commit of at most kBlock tokens the next proposal still finds at most
+// kDeferMax + kBlock pending, within its direct check; a record nobody takes
+// costs only time.
+constexpr int32_t kDeferMax = kBlock;
 }  // namespace clk

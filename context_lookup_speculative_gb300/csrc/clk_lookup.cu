@@ -313,6 +313,7 @@ constexpr int kMaxPending = 32;  // pending end positions checked directly
 constexpr int kInsertWarps = 5;  // warps that index the pending positions
 constexpr int kStepWarps = kMaxK + kInsertWarps;
 static_assert(kMaxPending + kMaxK <= kRing, "the ring must cover the pending window");
+static_assert(kDeferMax + kBlock <= kMaxPending, "what a launch leaves plus one commit stays within the direct check");
 
 __device__ __forceinline__ void named_barrier(int id, int threads)
 {
@@ -329,15 +330,18 @@ __device__ __forceinline__ void named_barrier(int id, int threads)
 //     and each one whose fingerprint matches (before the first empty entry)
 //     is checked token by token by one warp-wide load, which also fetches the
 //     16 tokens that follow the occurrence.
-//   the last kInsertWarps warps: index the pending positions meanwhile; they
-//     synchronise only among themselves, so the proposal never waits for them.
+//   the last kInsertWarps warps: index pending positions, either before the
+//     wait (those the previous proposal launch left in an ins record, see
+//     deferred inserts in clk_device.cuh) or after it, beside the lookup
+//     warps; the proposal never waits for them.  They raise nidx at the end,
+//     once every lookup warp has read it.
 //   warp 0 then takes the longest level that matched (ballot), builds the
 //   LZ77 draft, and with FUSE runs the scheduler and the fusion rule.
 template <bool FUSE>
 __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ head, const int32_t* prev_a,
     const int32_t* prev_len, int32_t* __restrict__ draft, int32_t* __restrict__ k_out, int32_t* __restrict__ j_out,
-    int32_t* len_out, int32_t* __restrict__ block, int32_t early)
+    int32_t* len_out, int32_t* __restrict__ block, int32_t early, int32_t tag, int32_t take)
 {
     __shared__ __align__(16) int32_t sm_win[kStepWarps][kRing];  // each warp's copy of the ring (16-byte stores)
     __shared__ int32_t sm_q[kMaxK];
@@ -355,6 +359,16 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     // half of the scratch and let this launch start only after its own wait)
     // or only after that wait.
     if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // take != 0: the previous proposal launch (completed: a fused greedy
+    // verify waited for it before letting this launch start) left index
+    // insertions to this one (its ins record for this batch position).  The
+    // insert warps run them now, while that verify finishes; they are
+    // published (nidx) only at the end of this launch.
+    int4 prev = make_int4(0, 0, 0, 0);
+    if (take != 0) prev = __ldcg(L.ins + (size_t)(take & 1) * (size_t)L.max_slots + b);
+    const bool took = take != 0 && prev.x == take && prev.y >= 0 && prev.y < L.max_slots && prev.z < prev.w;
+    if (took && warp >= nlev)
+        index_range<true>(L, prev.y, max(prev.z - 1, 0), prev.w - 2, tid - nlev * 32, (int32_t)blockDim.x - nlev * 32);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -376,6 +390,10 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     if (FUSE) asm volatile("" ::"r"(m_lane), "r"(pa), "r"(pl));
     const int32_t n = __shfl_sync(full, rec.x, 0);
     int32_t nidx = min(__shfl_sync(full, rec.z, 1), n);
+    // This launch raises nidx only after every lookup warp has read it
+    // (barrier 3: lookup warps arrive here, insert warps wait before the
+    // update), so a lookup never trusts entries still in flight.
+    if (warp < nlev) asm volatile("bar.arrive 3, %0;" ::"r"((int)blockDim.x) : "memory");
     int32_t* win = sm_win[warp];
     if (lane >= 2 && lane < 2 + kRing / 4) reinterpret_cast<int4*>(win)[lane - 2] = rec;
     __syncwarp();
@@ -391,10 +409,18 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
         // Many commits without a lookup in between: index them all first.
         index_range(L, slot, max(nidx - 1, 0), n - 2, tid, blockDim.x);
         __syncthreads();
-        if (tid == 0) L.state[slot].nidx = n;
         nidx = n;
     }
     const int32_t pend_lo = max(nidx - 1, 0);  // first end position not in the tables
+    // nidx once the insert warps are done with the positions taken before
+    // the wait.
+    const int32_t covered = min(n, took && prev.y == slot ? max(nidx, prev.w) : nidx);
+    // tag != 0: at most kDeferMax positions still pending after that are
+    // left to the next proposal launch (an ins record); more are indexed
+    // here, after the wait.
+    const bool deferred = tag != 0 && ok == 1 && n - covered <= kDeferMax;
+    if (tag != 0 && tid == 0)
+        L.ins[(size_t)(tag & 1) * (size_t)L.max_slots + b] = make_int4(tag, slot, deferred ? covered : n, n);
     const int32_t wlo = max(0, n - kRing);     // the ring holds positions [wlo, n)
     // Token at position x < n: from the ring when it holds x, else from the history.
     auto tok_at = [&](int32_t x) { return x >= wlo ? win[x  & (kRing - 1)] : __ldcg(h + x); };
@@ -448,12 +474,13 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
         __syncwarp();
         named_barrier(1, nlev * 32);
     } else {
-        if (ok == 1 && n - 2 >= pend_lo) {
+        const int32_t ins_lo = max(covered - 1, 0);
+        const int32_t rank = tid - nlev * 32, nthr = (int32_t)blockDim.x - nlev * 32;
+        if (ok == 1 && n - 2 >= ins_lo && !deferred) {
             // Index the pending end positions, tokens from the ring.
-            const int32_t rank = tid - nlev * 32, nthr = (int32_t)blockDim.x - nlev * 32;
-            const int32_t tasks = (n - 1 - pend_lo) * nlev;
+            const int32_t tasks = (n - 1 - ins_lo) * nlev;
             for (int32_t task = rank; task < tasks; task += nthr) {
-                const int32_t q = pend_lo + task / nlev;
+                const int32_t q = ins_lo + task / nlev;
                 const int32_t lvl = task % nlev;
                 const int32_t k = p.min_k + lvl;
                 if (q < k - 1) continue;
@@ -482,10 +509,13 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
                 if (!index_insert8(L, table_of(L, slot, lvl), kg_final(acc, k), q, same))
                     latch(L.status, CLK_ECAPACITY, slot);
             }
-            __syncwarp();
-            named_barrier(2, (int)blockDim.x - nlev * 32);
-            if (rank == 0) L.state[slot].nidx = n;
         }
+        // Publish what this launch indexed: everything below n, or below
+        // `covered` when the rest is left to the next launch.
+        __syncwarp();
+        named_barrier(2, nthr);
+        asm volatile("bar.sync 3, %0;" ::"r"((int)blockDim.x) : "memory");
+        if (rank == 0 && ok == 1) atomicMax(&L.state[slot].nidx, deferred ? covered : n);
         return;
     }
     if (warp != 0) return;
@@ -526,13 +556,24 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
 
 // One CTA per request, launched as a programmatic dependent of the previous
 // launch in the stream (see k_lookup_step).
+// Batches of at most kDeferBatch requests leave few pending insertions to
+// the next proposal launch (ins records): there the proposal is on the
+// step's critical path, and the next one runs them before its wait, beside
+// the verify's commit.  Larger batches index them after the wait, where the
+// proposal overlaps the verify's streaming anyway.
+constexpr int32_t kDeferBatch = 32;
+
 template <bool FUSE>
-int launch_lookup_step(const clk_lookup* h, const int32_t* slots, int32_t B, const int32_t* head,
-                       const int32_t* prev_a, const int32_t* prev_len, int32_t* draft, int32_t* k, int32_t* j,
-                       int32_t* len, int32_t* block, cudaStream_t s)
+int launch_lookup_step(clk_lookup* h, const int32_t* slots, int32_t B, const int32_t* head, const int32_t* prev_a,
+                       const int32_t* prev_len, int32_t* draft, int32_t* k, int32_t* j, int32_t* len, int32_t* block,
+                       cudaStream_t s)
 {
     const LookupDev& L = h->dev;
     const int32_t early = h->last_fused == kFusedGreedy ? 1 : 0;
+    // Tags alternate in parity (the record half), wrapping from 2^30 to 1.
+    int32_t tag = 0;
+    if (B <= kDeferBatch) tag = h->ptag = h->ptag >= (1 << 30) || h->ptag < 1 ? 1 : h->ptag + 1;
+    const int32_t take = early && h->vsince ? h->defer_tag : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(32u * (unsigned)(L.nlev + kInsertWarps));  // <= 32 * kStepWarps
@@ -543,8 +584,11 @@ int launch_lookup_step(const clk_lookup* h, const int32_t* slots, int32_t B, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, k_lookup_step<FUSE>, L, slots, head, prev_a, prev_len, draft, k, j,
-                                          len, block, early));
+    const int rc = cuda_status(cudaLaunchKernelEx(&cfg, k_lookup_step<FUSE>, L, slots, head, prev_a, prev_len, draft,
+                                                  k, j, len, block, early, tag, take));
+    h->defer_tag = rc == CLK_OK ? tag : 0;
+    h->vsince = 0;
+    return rc;
 }
 
 int proposal_cta_regs(int nlev)
@@ -568,6 +612,7 @@ extern "C" int clk_lookup_init(clk_lookup* h, const int32_t* d_slots, int32_t B,
         return CLK_EINVAL;
     const LookupDev& L = h->dev;
     cudaStream_t st = (cudaStream_t)s;
+    h->defer_tag = 0;
     k_init_state<<<(B + 127) / 128, 128, 0, st>>>(L, d_slots, d_prompt_off, B);
     if ((rc = launch_status()) != CLK_OK) return rc;
     const int64_t copy_chunks = (L.cap + kThreads * 4 - 1) / (kThreads * 4);
@@ -592,6 +637,7 @@ extern "C" int clk_lookup_append(clk_lookup* h, const int32_t* d_slots, int32_t 
     if (rc != CLK_OK) return rc;
     if (B == 0) return CLK_OK;
     if (!ok_i32(d_slots) || !ok_i32(d_tok) || !ok_i32(d_count)) return CLK_EINVAL;
+    h->defer_tag = 0;  // this launch indexes every pending position
     k_append<<<B, 192, 0, (cudaStream_t)s>>>(h->dev, d_slots, d_tok, d_count);
     return launch_status();
 }

@@ -940,11 +940,17 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     }
     const int sms = num_sms();
     if (sms <= 0) return CLK_ECUDA;
-    SampleArgs args = a;
-    if (FUSED && a.late > 0)  // CTAs dispatched behind the proposal launch's CTAs (see clk_verify.cu)
-        args.late = displaced_by_proposal<k_sample_step<DT, VEC>>(kSThreads, Ldev.nlev, occ) * (a.B < sms ? a.B : sms);
     const int64_t segs = (int64_t)a.B * kBlock * a.S;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)occ * sms, segs));
+    SampleArgs args = a;
+    if (FUSED && a.late > 0) {
+        // CTAs dispatched behind the proposal launch's CTAs: those beyond the
+        // places the proposal leaves (as in the fused greedy verification).
+        const int64_t taken = (int64_t)displaced_by_proposal<k_sample_step<DT, VEC>>(kSThreads, Ldev.nlev, occ) *
+                              (a.B < sms ? a.B : sms);
+        const int64_t late = grid - ((int64_t)occ * sms - taken);
+        args.late = late > 0 ? (int32_t)late : 0;
+    }
     if (!FUSED) {
         kern<<<(unsigned)grid, kSThreads, smem, s>>>(args, Ldev);
         return launch_status();

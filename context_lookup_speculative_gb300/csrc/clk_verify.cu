@@ -1009,6 +1009,7 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     if (rc == CLK_OK) {
         h->vparity ^= 1;
         h->last_fused = kFusedGreedy;
+        h->vsince = 1;
     } else {
         h->last_fused = kFusedNone;
     }

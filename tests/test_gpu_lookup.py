@@ -197,9 +197,12 @@ def test_commits_without_lookup_in_between(commits):
         toks[::3] = np.resize([1, 2, 3], 16)  # periodic runs: long, overlapping matches
         _commit_by_verify(lk, s, toks)
         hists = [np.concatenate([h, toks[b].astype(np.int32)]) for b, h in enumerate(hists)]
-    assert lk.slot_info(0)["n_indexed"] < lk.slot_info(0)["n"]
+    n, nidx = lk.slot_info(0)["n"], lk.slot_info(0)["n_indexed"]
+    assert nidx < n
     _assert_same(_propose(lk, s), hists)
-    assert lk.slot_info(0)["n_indexed"] == lk.slot_info(0)["n"]
+    # up to 16 pending positions are left to the next proposal launch; more
+    # are indexed by the proposal itself
+    assert lk.slot_info(0)["n_indexed"] == (nidx if n - nidx <= 16 else n)
     # commit again, then an unfused append on top of the pending positions
     toks = rng.integers(0, 8, size=(B, 16))
     _commit_by_verify(lk, s, toks)
@@ -267,3 +270,75 @@ def test_full_scan_lookup_matches_oracle_and_index(kind):
     assert lk.status() == (0, 0)
     with pytest.raises(clk.ClkError):
         _propose_scan(lk, s, ctas_per_request=-1)
+
+
+def test_insertions_left_to_the_next_proposal():
+    """A proposal that still finds at most 16 end positions pending leaves
+    their index insertions to the next proposal launch (an ins record).
+    That launch runs them before its wait, and raises n_indexed to the
+    length the recording launch saw, only when a fused greedy verify came in
+    between (which completes only after the recording launch).  Records
+    nobody takes, or that a re-initialisation made stale, are never applied;
+    every proposal equals the full scan."""
+    rng = np.random.default_rng(58)
+    B, V = 6, 5
+    hists = [rng.integers(0, V, size=int(rng.integers(30, 90))).astype(np.int32) for _ in range(B)]
+    lk, s = _setup(hists, 400, vocab=V)
+
+    def commit():
+        nonlocal hists
+        toks = rng.integers(0, V, size=(B, 16))
+        _commit_by_verify(lk, s, toks)
+        hists = [np.concatenate([h, toks[b].astype(np.int32)]) for b, h in enumerate(hists)]
+
+    def info():
+        return [(lk.slot_info(b)["n"], lk.slot_info(b)["n_indexed"]) for b in range(B)]
+
+    commit()  # 16 pending positions a slot
+    before = info()
+    _assert_same(_propose(lk, s), hists)
+    assert info() == before  # left to the next proposal
+    commit()
+    _assert_same(_propose(lk, s), hists)
+    assert [ni for _, ni in info()] == [n for n, _ in before]  # taken before its wait
+    # two proposals in a row: the second does not take the first's records
+    mid = info()
+    _assert_same(_propose(lk, s), hists)
+    assert info() == mid
+    commit()
+    _assert_same(_propose(lk, s), hists)
+    assert [ni for _, ni in info()] == [n for n, _ in mid]
+    # a sampled verify in between: the next proposal takes nothing before its
+    # wait and indexes the 32 pending positions itself
+    x = torch.zeros((B, 16, V), dtype=torch.float32)
+    x[:, :, 2] = 50.0
+    blk = torch.full((B, 16), 2, dtype=torch.int32)
+    L = torch.full((B,), 16, dtype=torch.int32, device="cuda")
+    t = torch.ones(B, dtype=torch.float32, device="cuda")
+    u = torch.full((B, 16, 2), 0.5, dtype=torch.float32, device="cuda")
+    acc, em = torch.zeros(B, dtype=torch.int32, device="cuda"), torch.zeros(B, dtype=torch.int32, device="cuda")
+    out = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
+    clk.verify_sample_append(lk, s, x.cuda(), blk.cuda(), L, t, u, acc, em, out,
+                             clk.verify_sample_scratch(torch.float32, V, B))
+    torch.cuda.synchronize()
+    hists = [lk.history(b) for b in range(B)]
+    assert all(n - ni > 16 for n, ni in info())
+    _assert_same(_propose(lk, s), hists)
+    assert all(n == ni for n, ni in info())
+    # a re-initialisation between a recording proposal and the verify: the
+    # records are dropped, the fresh index stays complete
+    commit()
+    _assert_same(_propose(lk, s), hists)
+    fresh = [rng.integers(0, V, size=int(rng.integers(10, 40))).astype(np.int32) for _ in range(B)]
+    tok, off = _csr(fresh)
+    clk.lookup_init(lk, s, tok, off)
+    hists = fresh
+    assert all(ni == n for n, ni in info())
+    commit()
+    _assert_same(_propose(lk, s), hists)
+    assert all(n - ni == 16 for n, ni in info())
+    for _ in range(4):
+        commit()
+        _assert_same(_propose(lk, s), hists)
+        assert all(n - ni == 16 for n, ni in info())
+    assert lk.status() == (0, 0)
