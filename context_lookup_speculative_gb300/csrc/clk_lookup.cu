@@ -369,12 +369,20 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     const bool took = take != 0 && prev.x == take && prev.y >= 0 && prev.y < L.max_slots && prev.z < prev.w;
     if (took && warp >= nlev)
         index_range<true>(L, prev.y, max(prev.z - 1, 0), prev.w - 2, tid - nlev * 32, (int32_t)blockDim.x - nlev * 32);
+    // The slot, read once more after the wait: this early copy only lets the
+    // record load go out together with that read.
+    const int32_t slot_guess = slots[b];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (!early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Round trip 1: the slot (every warp); warp 0 also loads the inputs that
-    // do not depend on it.
-    const int32_t slot = slots[b];
+    // One round trip: the slot (every warp), the record of the slot read
+    // before the wait (up to the end of the ring, 18 x 16 B), and for warp 0
+    // the inputs that do not depend on it.  A slot that changed meanwhile
+    // costs a second round trip for its record.
+    const int32_t slot = __ldcg(slots + b);
+    int4 rec = make_int4(0, 0, 0, 0);
+    const bool guess_ok = slot_guess >= 0 && slot_guess < L.max_slots;
+    if (guess_ok && lane < 2 + kRing / 4) rec = __ldcg(reinterpret_cast<const int4*>(L.state + slot_guess) + lane);
     int32_t m_lane = CLK_SENT, pa = 0, pl = 0;
     if (FUSE && warp == 0) {
         if (lane < p.head) m_lane = head[(int64_t)b * p.head + lane];
@@ -382,9 +390,10 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
         pl = prev_len[b];
     }
     const bool valid = slot >= 0 && slot < L.max_slots;
-    // Round trip 2: the slot's record up to the end of the ring (18 x 16 B).
-    int4 rec = make_int4(0, 0, 0, 0);
-    if (valid && lane < 2 + kRing / 4) rec = __ldcg(reinterpret_cast<const int4*>(L.state + slot) + lane);
+    if (slot != slot_guess) {
+        rec = make_int4(0, 0, 0, 0);
+        if (valid && lane < 2 + kRing / 4) rec = __ldcg(reinterpret_cast<const int4*>(L.state + slot) + lane);
+    }
     // Keep the compiler from sinking round trip 1's loads to their first use
     // after the lookup: their values are needed by then anyway.
     if (FUSE) asm volatile("" ::"r"(m_lane), "r"(pa), "r"(pl));

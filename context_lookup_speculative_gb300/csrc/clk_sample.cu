@@ -266,8 +266,14 @@ __device__ __forceinline__ void rows_prefix(int32_t B, Rows rows, int32_t* P, in
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t per = (B + kSThreads - 1) / kSThreads;
     const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    // rows(b) is read once (it may load from global memory): kept in P[b]
+    // (this thread's own entries) until the prefix overwrites it
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) local += rows(b);
+    for (int32_t b = b0; b < b1; ++b) {
+        const int32_t r = rows(b);
+        P[b] = r;
+        local += r;
+    }
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -288,8 +294,9 @@ __device__ __forceinline__ void rows_prefix(int32_t B, Rows rows, int32_t* P, in
     __syncthreads();
     int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
+        const int32_t r = P[b];
         P[b] = run;
-        run += rows(b);
+        run += r;
     }
     if (tid == kSThreads - 1) P[B] = sm_warp[kSWarpsPerCta - 1];
     __syncthreads();

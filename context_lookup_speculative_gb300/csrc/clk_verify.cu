@@ -261,8 +261,14 @@ __device__ __forceinline__ void block_prefix(int32_t B, Rows rows, int32_t* P, i
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t per = (B + kVThreads - 1) / kVThreads;
     const int32_t b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    // rows(b) is read once (it may load from global memory): kept in P[b]
+    // (this thread's own entries) until the prefix overwrites it
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) local += rows(b);
+    for (int32_t b = b0; b < b1; ++b) {
+        const int32_t r = rows(b);
+        P[b] = r;
+        local += r;
+    }
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -283,8 +289,9 @@ __device__ __forceinline__ void block_prefix(int32_t B, Rows rows, int32_t* P, i
     __syncthreads();
     int32_t run = (incl - local) + (warp > 0 ? sm_warp[warp - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
+        const int32_t r = P[b];
         P[b] = run;
-        run += rows(b);
+        run += r;
     }
     if (tid == kVThreads - 1) P[B] = sm_warp[kVWarps - 1];
     __syncthreads();
@@ -305,7 +312,11 @@ __device__ __forceinline__ void rest_prefix(int32_t B, Rows rows, int32_t* P, in
     const int32_t per = (B + kT - 1) / kT;
     const int32_t b0 = min(B, t * per), b1 = min(B, b0 + per);
     int32_t local = 0;
-    for (int32_t b = b0; b < b1; ++b) local += rows(b);
+    for (int32_t b = b0; b < b1; ++b) {  // rows(b) read once, kept in P[b] (as in block_prefix)
+        const int32_t r = rows(b);
+        P[b] = r;
+        local += r;
+    }
     int32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -326,8 +337,9 @@ __device__ __forceinline__ void rest_prefix(int32_t B, Rows rows, int32_t* P, in
     named_barrier(1, kT);
     int32_t run = (incl - local) + (w > 0 ? sm_warp[w - 1] : 0);
     for (int32_t b = b0; b < b1; ++b) {
+        const int32_t r = P[b];
         P[b] = run;
-        run += rows(b);
+        run += r;
     }
     if (t == kT - 1) P[B] = sm_warp[kW - 1];
 }
