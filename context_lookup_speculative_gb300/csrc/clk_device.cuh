@@ -29,7 +29,7 @@
 // slot and an atomicMax on the same word (same fingerprint, larger q) to
 // keep the most recent occurrence.
 //
-// Deferred inserts.  A slot records nidx, the history length up to which its
+// Deferred inserts.  A slot records nidx, a history length up to which its
 // tables are complete: they hold every k-gram ending at q <= nidx - 2.  The
 // fused verify only writes the emitted tokens (n grows, nidx does not); the
 // end positions nidx-1 .. n-2 stay pending until they are indexed, and every
@@ -39,8 +39,11 @@
 // indexes them in dedicated warps: after its wait, beside its lookup warps;
 // or, for small batches, it leaves at most kDeferMax of them to the next
 // proposal launch, whose dedicated warps index them before that launch's
-// wait, while the verify in between finishes.  nidx only grows (atomicMax)
-// between initialisations.
+// wait, while the verify in between finishes.  A launch never raises nidx
+// over entries it inserted itself: its ins record says what it leaves
+// complete, and the next launch (which starts reading only once this one
+// has completed) trusts that and raises nidx (atomicMax: it only grows
+// between initialisations).
 //
 // The last kRing tokens of every history are also kept in the slot's record
 // (ring[p mod kRing] = h[p]), next to n and the scheduler state, so that the
@@ -412,12 +415,13 @@ __device__ __forceinline__ void index_range(const LookupDev& L, int32_t slot, in
     }
 }
 
-// Insertions left by a proposal launch to the next one: it records
-// {tag, slot, from, n} in ins[tag & 1][b] (tag != 0 names the launch): the
-// k-grams ending at [max(from - 1, 0), n - 2] are still to be indexed, and
-// nidx may then rise to n.  The next proposal launch, when it follows a
-// fused greedy verify (so the recording launch has completed), takes the
-// records of that tag before its own wait, while the verify finishes.  A
+// The record of a proposal launch for batch position b, in ins[tag & 1][b]
+// (tag != 0 names the launch): {tag, slot, z, w}.  Every k-gram of the slot
+// ending before z - 1 is in the tables once the launch has completed; those
+// ending at [z - 1, w - 2] are left to the next launch.  The next proposal
+// launch reads the record of that tag after its wait, or, when it follows a
+// fused greedy verify (so the recording launch has completed already),
+// before it, and then runs the insertions while the verify finishes.  A
 // proposal leaves at most kDeferMax positions this way, so that after one
 // commit of at most kBlock tokens the next proposal still finds at most
 // kDeferMax + kBlock pending, within its direct check; a record nobody takes

@@ -20,12 +20,12 @@ struct clk_lookup {
     // (last_fused = kFusedGreedy), whose scratch use it then cannot disturb.
     int vparity;
     int last_fused;
-    // Proposal launches that leave index insertions to the next one (ins
-    // records) number themselves with ptag; defer_tag is the tag of the last
-    // proposal launch if it left records (0 if not, or once a call rebuilt
-    // histories or tables).  The next proposal takes them before its wait
-    // only when a fused greedy verify came after the recording launch
-    // (vsince = 1), which completes only after it.
+    // Proposal launches number themselves with ptag and leave ins records
+    // (what they leave complete in the index, and insertions left to the
+    // next one); defer_tag is the tag of the last proposal launch (0 once a
+    // call rebuilt histories or tables).  The next proposal reads those
+    // records after its wait, or before it when a fused greedy verify came
+    // after the recording launch (vsince = 1), which completes only after it.
     int32_t ptag;
     int32_t defer_tag;
     int vsince;

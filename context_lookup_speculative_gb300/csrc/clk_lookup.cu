@@ -333,15 +333,19 @@ __device__ __forceinline__ void named_barrier(int id, int threads)
 //   the last kInsertWarps warps: index pending positions, either before the
 //     wait (those the previous proposal launch left in an ins record, see
 //     deferred inserts in clk_device.cuh) or after it, beside the lookup
-//     warps; the proposal never waits for them.  They raise nidx at the end,
-//     once every lookup warp has read it.
+//     warps; the proposal never waits for them.  They raise nidx to what the
+//     previous launch left complete; what this one indexes is published the
+//     same way by the next launch (or by clk_lookup_append).
 //   warp 0 then takes the longest level that matched (ballot), builds the
 //   LZ77 draft, and with FUSE runs the scheduler and the fusion rule.
+// 64 registers a thread: a CTA of up to 32 * kStepWarps threads fits an SM
+// beside the verify launch's CTAs.
 template <bool FUSE>
-__global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
+__global__ void __maxnreg__(64) k_lookup_step(
     LookupDev L, const int32_t* __restrict__ slots, const int32_t* __restrict__ head, const int32_t* prev_a,
     const int32_t* prev_len, int32_t* __restrict__ draft, int32_t* __restrict__ k_out, int32_t* __restrict__ j_out,
-    int32_t* len_out, int32_t* __restrict__ block, int32_t early, int32_t tag, int32_t take)
+    int32_t* len_out, int32_t* __restrict__ block, int32_t early, int32_t tag, int32_t take, int32_t pre,
+    int32_t defer)
 {
     __shared__ __align__(16) int32_t sm_win[kStepWarps][kRing];  // each warp's copy of the ring (16-byte stores)
     __shared__ int32_t sm_q[kMaxK];
@@ -359,16 +363,19 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     // half of the scratch and let this launch start only after its own wait)
     // or only after that wait.
     if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // take != 0: the previous proposal launch (completed: a fused greedy
-    // verify waited for it before letting this launch start) left index
-    // insertions to this one (its ins record for this batch position).  The
-    // insert warps run them now, while that verify finishes; they are
-    // published (nidx) only at the end of this launch.
+    // take != 0: the ins records of the previous proposal launch (tag take)
+    // are read after the wait (that launch has completed by then).  pre: it
+    // has completed already (a fused greedy verify waited for it before
+    // letting this launch start), so the insert warps run the insertions it
+    // left for this batch position now, while that verify finishes.
     int4 prev = make_int4(0, 0, 0, 0);
-    if (take != 0) prev = __ldcg(L.ins + (size_t)(take & 1) * (size_t)L.max_slots + b);
-    const bool took = take != 0 && prev.x == take && prev.y >= 0 && prev.y < L.max_slots && prev.z < prev.w;
-    if (took && warp >= nlev)
-        index_range<true>(L, prev.y, max(prev.z - 1, 0), prev.w - 2, tid - nlev * 32, (int32_t)blockDim.x - nlev * 32);
+    const int4* prev_at = L.ins + (size_t)(take & 1) * (size_t)L.max_slots + b;
+    if (pre && warp >= nlev) {
+        prev = __ldcg(prev_at);
+        if (prev.x == take && prev.y >= 0 && prev.y < L.max_slots && prev.z < prev.w)
+            index_range<true>(L, prev.y, max(prev.z - 1, 0), prev.w - 2, tid - nlev * 32,
+                              (int32_t)blockDim.x - nlev * 32);
+    }
     // The slot, read once more after the wait: this early copy only lets the
     // record load go out together with that read.
     const int32_t slot_guess = slots[b];
@@ -380,6 +387,7 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     // the inputs that do not depend on it.  A slot that changed meanwhile
     // costs a second round trip for its record.
     const int32_t slot = __ldcg(slots + b);
+    if (take != 0) prev = __ldcg(prev_at);
     int4 rec = make_int4(0, 0, 0, 0);
     const bool guess_ok = slot_guess >= 0 && slot_guess < L.max_slots;
     if (guess_ok && lane < 2 + kRing / 4) rec = __ldcg(reinterpret_cast<const int4*>(L.state + slot_guess) + lane);
@@ -399,10 +407,14 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
     if (FUSE) asm volatile("" ::"r"(m_lane), "r"(pa), "r"(pl));
     const int32_t n = __shfl_sync(full, rec.x, 0);
     int32_t nidx = min(__shfl_sync(full, rec.z, 1), n);
-    // This launch raises nidx only after every lookup warp has read it
-    // (barrier 3: lookup warps arrive here, insert warps wait before the
-    // update), so a lookup never trusts entries still in flight.
-    if (warp < nlev) asm volatile("bar.arrive 3, %0;" ::"r"((int)blockDim.x) : "memory");
+    // The previous launch's record for this request: every k-gram ending
+    // before prev.z - 1 is in the tables (that launch completed), whatever
+    // nidx says; nidx itself is raised only by a later launch (below), never
+    // by the launch that made the insertions, so a lookup never trusts
+    // entries still in flight.
+    const bool prev_ok = take != 0 && prev.x == take && prev.y >= 0 && prev.y < L.max_slots && prev.z <= prev.w;
+    const bool mine = prev_ok && prev.y == slot;
+    if (mine) nidx = max(nidx, min(prev.z, n));
     int32_t* win = sm_win[warp];
     if (lane >= 2 && lane < 2 + kRing / 4) reinterpret_cast<int4*>(win)[lane - 2] = rec;
     __syncwarp();
@@ -418,16 +430,19 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
         // Many commits without a lookup in between: index them all first.
         index_range(L, slot, max(nidx - 1, 0), n - 2, tid, blockDim.x);
         __syncthreads();
+        // (every warp of this CTA has read the slot's record by now)
+        if (tid == 0) atomicMax(&L.state[slot].nidx, n);
         nidx = n;
     }
     const int32_t pend_lo = max(nidx - 1, 0);  // first end position not in the tables
     // nidx once the insert warps are done with the positions taken before
     // the wait.
-    const int32_t covered = min(n, took && prev.y == slot ? max(nidx, prev.w) : nidx);
-    // tag != 0: at most kDeferMax positions still pending after that are
-    // left to the next proposal launch (an ins record); more are indexed
-    // here, after the wait.
-    const bool deferred = tag != 0 && ok == 1 && n - covered <= kDeferMax;
+    const int32_t covered = min(n, pre && mine && prev.z < prev.w ? max(nidx, prev.w) : nidx);
+    // defer: at most kDeferMax positions still pending after that are left
+    // to the next proposal launch; more are indexed here, after the wait.
+    // The record says what this launch leaves complete (z) and to what
+    // length the next one is to index (w).
+    const bool deferred = defer && ok == 1 && n - covered <= kDeferMax;
     if (tag != 0 && tid == 0)
         L.ins[(size_t)(tag & 1) * (size_t)L.max_slots + b] = make_int4(tag, slot, deferred ? covered : n, n);
     const int32_t wlo = max(0, n - kRing);     // the ring holds positions [wlo, n)
@@ -519,12 +534,8 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
                     latch(L.status, CLK_ECAPACITY, slot);
             }
         }
-        // Publish what this launch indexed: everything below n, or below
-        // `covered` when the rest is left to the next launch.
-        __syncwarp();
-        named_barrier(2, nthr);
-        asm volatile("bar.sync 3, %0;" ::"r"((int)blockDim.x) : "memory");
-        if (rank == 0 && ok == 1) atomicMax(&L.state[slot].nidx, deferred ? covered : n);
+        // Raise nidx to what the previous launch left complete.
+        if (rank == 0 && prev_ok) atomicMax(&L.state[prev.y].nidx, prev.z);
         return;
     }
     if (warp != 0) return;
@@ -565,11 +576,13 @@ __global__ void __launch_bounds__(32 * kStepWarps) k_lookup_step(
 
 // One CTA per request, launched as a programmatic dependent of the previous
 // launch in the stream (see k_lookup_step).
-// Batches of at most kDeferBatch requests leave few pending insertions to
-// the next proposal launch (ins records): there the proposal is on the
-// step's critical path, and the next one runs them before its wait, beside
-// the verify's commit.  Larger batches index them after the wait, where the
-// proposal overlaps the verify's streaming anyway.
+// Every launch records, per batch position, what it leaves complete in the
+// index (ins records; the next launch raises nidx to it).  Batches of at
+// most kDeferBatch requests also leave few pending insertions to the next
+// launch: there the proposal is on the step's critical path, and the next
+// one runs them before its wait, beside the verify's commit.  Larger
+// batches index them after the wait, where the proposal overlaps the
+// verify's streaming anyway.
 constexpr int32_t kDeferBatch = 32;
 
 template <bool FUSE>
@@ -580,9 +593,10 @@ int launch_lookup_step(clk_lookup* h, const int32_t* slots, int32_t B, const int
     const LookupDev& L = h->dev;
     const int32_t early = h->last_fused == kFusedGreedy ? 1 : 0;
     // Tags alternate in parity (the record half), wrapping from 2^30 to 1.
-    int32_t tag = 0;
-    if (B <= kDeferBatch) tag = h->ptag = h->ptag >= (1 << 30) || h->ptag < 1 ? 1 : h->ptag + 1;
-    const int32_t take = early && h->vsince ? h->defer_tag : 0;
+    const int32_t tag = h->ptag = h->ptag >= (1 << 30) || h->ptag < 1 ? 1 : h->ptag + 1;
+    const int32_t take = h->defer_tag;
+    const int32_t pre = take != 0 && early && h->vsince ? 1 : 0;
+    const int32_t defer = B <= kDeferBatch ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(32u * (unsigned)(L.nlev + kInsertWarps));  // <= 32 * kStepWarps
@@ -594,7 +608,7 @@ int launch_lookup_step(clk_lookup* h, const int32_t* slots, int32_t B, const int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int rc = cuda_status(cudaLaunchKernelEx(&cfg, k_lookup_step<FUSE>, L, slots, head, prev_a, prev_len, draft,
-                                                  k, j, len, block, early, tag, take));
+                                                  k, j, len, block, early, tag, take, pre, defer));
     h->defer_tag = rc == CLK_OK ? tag : 0;
     h->vsince = 0;
     return rc;

@@ -765,8 +765,20 @@ __global__ void __launch_bounds__(kVThreads, DEEP ? 2 : 4) k_verify_step(VerifyA
         const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
         return (total1 / Wtot) * w + (total1 % Wtot) * w / Wtot;
     };
-    const int64_t lo = start(blockIdx.x);
-    const int64_t hi = start(blockIdx.x + 1);
+    int64_t lo = start(blockIdx.x);
+    int64_t hi = start(blockIdx.x + 1);
+    if (DEEP && P1[B] > 0 && P1[B] <= G - D) {
+        // Few rows (a latency-bound launch): equal parts of whole rows, m a
+        // row, one part per CTA (the first ones), so that no CTA's share
+        // crosses a row boundary, where its loads would drain and restart.
+        const int64_t R1 = P1[B], m = (G - D) / R1, c = blockIdx.x;
+        lo = hi = 0;
+        if (c < R1 * m) {
+            const int64_t row = c / m, part = c % m;
+            lo = row * vpr + vpr * part / m;
+            hi = row * vpr + vpr * (part + 1) / m;
+        }
+    }
     const int64_t mid = (hi - lo >= kVSplitMin) ? lo + (hi - lo) / 2 : hi;
     stream(P1, false, lo, mid);
     flush();

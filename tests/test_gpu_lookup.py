@@ -200,9 +200,10 @@ def test_commits_without_lookup_in_between(commits):
     n, nidx = lk.slot_info(0)["n"], lk.slot_info(0)["n_indexed"]
     assert nidx < n
     _assert_same(_propose(lk, s), hists)
-    # up to 16 pending positions are left to the next proposal launch; more
-    # are indexed by the proposal itself
-    assert lk.slot_info(0)["n_indexed"] == (nidx if n - nidx <= 16 else n)
+    # n_indexed rises only when a later launch vouches for the insertions
+    # (the next proposal), except after the catch-up of more than 32 pending
+    # positions, which completes before the lookups run
+    assert lk.slot_info(0)["n_indexed"] == (n if n - nidx > 32 else nidx)
     # commit again, then an unfused append on top of the pending positions
     toks = rng.integers(0, 8, size=(B, 16))
     _commit_by_verify(lk, s, toks)
@@ -274,16 +275,17 @@ def test_full_scan_lookup_matches_oracle_and_index(kind):
 
 def test_insertions_left_to_the_next_proposal():
     """A proposal that still finds at most 16 end positions pending leaves
-    their index insertions to the next proposal launch (an ins record).
-    That launch runs them before its wait, and raises n_indexed to the
-    length the recording launch saw, only when a fused greedy verify came in
-    between (which completes only after the recording launch).  Records
-    nobody takes, or that a re-initialisation made stale, are never applied;
-    every proposal equals the full scan."""
+    their index insertions to the next proposal launch (an ins record); that
+    launch runs them before its wait when a fused greedy verify came in
+    between (the recording launch has then completed), else after it.  A
+    launch never raises n_indexed over its own insertions: the next launch
+    does, from the record.  Records of an older launch, or made stale by a
+    re-initialisation, are never applied; every proposal equals the full
+    scan."""
     rng = np.random.default_rng(58)
     B, V = 6, 5
     hists = [rng.integers(0, V, size=int(rng.integers(30, 90))).astype(np.int32) for _ in range(B)]
-    lk, s = _setup(hists, 400, vocab=V)
+    lk, s = _setup(hists, 500, vocab=V)
 
     def commit():
         nonlocal hists
@@ -299,15 +301,12 @@ def test_insertions_left_to_the_next_proposal():
     _assert_same(_propose(lk, s), hists)
     assert info() == before  # left to the next proposal
     commit()
-    _assert_same(_propose(lk, s), hists)
-    assert [ni for _, ni in info()] == [n for n, _ in before]  # taken before its wait
-    # two proposals in a row: the second does not take the first's records
-    mid = info()
-    _assert_same(_propose(lk, s), hists)
-    assert info() == mid
+    _assert_same(_propose(lk, s), hists)  # runs them before its wait
+    assert [ni for _, ni in info()] == [ni for _, ni in before]
+    _assert_same(_propose(lk, s), hists)  # a second proposal vouches for them
+    assert [ni for _, ni in info()] == [n for n, _ in before]
     commit()
     _assert_same(_propose(lk, s), hists)
-    assert [ni for _, ni in info()] == [n for n, _ in mid]
     # a sampled verify in between: the next proposal takes nothing before its
     # wait and indexes the 32 pending positions itself
     x = torch.zeros((B, 16, V), dtype=torch.float32)
@@ -322,7 +321,8 @@ def test_insertions_left_to_the_next_proposal():
                              clk.verify_sample_scratch(torch.float32, V, B))
     torch.cuda.synchronize()
     hists = [lk.history(b) for b in range(B)]
-    assert all(n - ni > 16 for n, ni in info())
+    assert all(n - ni > 32 for n, ni in info())
+    _assert_same(_propose(lk, s), hists)
     _assert_same(_propose(lk, s), hists)
     assert all(n == ni for n, ni in info())
     # a re-initialisation between a recording proposal and the verify: the
@@ -340,5 +340,5 @@ def test_insertions_left_to_the_next_proposal():
     for _ in range(4):
         commit()
         _assert_same(_propose(lk, s), hists)
-        assert all(n - ni == 16 for n, ni in info())
+        assert all(n - ni == 32 for n, ni in info())
     assert lk.status() == (0, 0)
