@@ -51,6 +51,7 @@ struct VerifyArgs {
     unsigned long long* done;  // [B]
     const int32_t* slots;      // fused only
     int32_t late;              // fused: trailing CTAs that start behind the proposal launch (0: none)
+    int32_t aligned;           // fused: split few rows in whole-row parts (latency-bound launches)
 };
 
 // Order-preserving 32-bit key of a float: larger value, larger key; +0 == -0.
@@ -609,12 +610,9 @@ struct StepSmem {
     unsigned long long acc_add;  // merged but not yet counted, and how many
 };
 
-// DEEP: the variant for latency-bound launches (few logits): two CTAs per
-// SM, twice the loads in flight per thread.
-template <int DT, bool VEC, bool DEEP>
-__global__ void __launch_bounds__(kVThreads, DEEP ? 2 : 4) k_verify_step(VerifyArgs a, LookupDev L)
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kVThreads, 4) k_verify_step(VerifyArgs a, LookupDev L)
 {
-    constexpr int U = DEEP ? 2 * kUnroll : kUnroll;
     // P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then Lc[B + 1]
     // (after the wait: each request's length, read once)
     extern __shared__ int32_t sm_prefix[];
@@ -732,7 +730,7 @@ __global__ void __launch_bounds__(kVThreads, DEEP ? 2 : 4) k_verify_step(VerifyA
             const int64_t s0 = lo - ri * vpr;
             const int64_t s1 = min(to, (ri + 1) * vpr) - ri * vpr;
             const int32_t row0 = missed ? P1[b + 1] - P1[b] : 0;
-            piece_max<DT, VEC, U>(a, b, row0 + (int32_t)(ri - P[b]), s0, s1, sm);
+            piece_max<DT, VEC>(a, b, row0 + (int32_t)(ri - P[b]), s0, s1, sm);
             if (tid == 0) {
                 if (b != ss.acc_b) {
                     if (ss.acc_b >= 0) defer(ss.acc_b, ss.acc_add);
@@ -767,10 +765,11 @@ __global__ void __launch_bounds__(kVThreads, DEEP ? 2 : 4) k_verify_step(VerifyA
     };
     int64_t lo = start(blockIdx.x);
     int64_t hi = start(blockIdx.x + 1);
-    if (DEEP && P1[B] > 0 && P1[B] <= G - D) {
-        // Few rows (a latency-bound launch): equal parts of whole rows, m a
-        // row, one part per CTA (the first ones), so that no CTA's share
-        // crosses a row boundary, where its loads would drain and restart.
+    if (a.aligned && P1[B] > 0 && P1[B] <= G - D && 3 * (int64_t)P1[B] > G - D) {
+        // Rows about as many as the CTAs (a latency-bound launch with short
+        // rows): one or two equal parts of a row per CTA (the first ones), so
+        // that no CTA's share crosses a row boundary, where its loads would
+        // drain and restart.  (With many parts a row, few shares cross one.)
         const int64_t R1 = P1[B], m = (G - D) / R1, c = blockIdx.x;
         lo = hi = 0;
         if (c < R1 * m) {
@@ -844,25 +843,26 @@ int verify_grid(size_t smem, int32_t B, int64_t vpr, int64_t* grid_out)
 
 // Launches the fused step with at most `per_sm_cap` CTAs per SM (0: as many
 // as fit).
-template <int DT, bool VEC, bool DEEP>
+template <int DT, bool VEC>
 int launch_step(const VerifyArgs& a, const LookupDev& L, size_t smem, int64_t vpr, int per_sm_cap, cudaStream_t s)
 {
-    auto kern = k_verify_step<DT, VEC, DEEP>;
+    auto kern = k_verify_step<DT, VEC>;
     int64_t grid = 0;
-    int rc = verify_grid<k_verify_step<DT, VEC, DEEP>>(smem, a.B, vpr, &grid);
+    int rc = verify_grid<k_verify_step<DT, VEC>>(smem, a.B, vpr, &grid);
     if (rc != CLK_OK) return rc;
     int packed = 0;
-    rc = occupancy<k_verify_step<DT, VEC, DEEP>>(smem, &packed);
+    rc = occupancy<k_verify_step<DT, VEC>>(smem, &packed);
     if (rc != CLK_OK) return rc;
     const int occ = packed / 1024, sms = packed % 1024;
     if (per_sm_cap > 0 && grid > (int64_t)per_sm_cap * sms) grid = (int64_t)per_sm_cap * sms;
     VerifyArgs args = a;
+    args.aligned = per_sm_cap > 0 ? 1 : 0;
     if (a.late > 0) {
         // a.late > 0: the call follows a proposal launch it may overlap.  The
         // proposal's CTAs (one a request, on min(B, SMs) SMs) each take the
         // place of some CTAs of this launch; the CTAs beyond the places left
         // (dispatched last) start only when the proposal's leave.
-        const int64_t taken = (int64_t)displaced_by_proposal<k_verify_step<DT, VEC, DEEP>>(kVThreads, L.nlev, occ) *
+        const int64_t taken = (int64_t)displaced_by_proposal<k_verify_step<DT, VEC>>(kVThreads, L.nlev, occ) *
                               (a.B < sms ? a.B : sms);
         const int64_t late = grid - ((int64_t)occ * sms - taken);
         args.late = late > 0 ? (int32_t)late : 0;
@@ -896,22 +896,10 @@ int launch_verify(const VerifyArgs& a, const LookupDev& L, cudaStream_t s)
     }
     // A launch whose logits are few (at most kVSmallBytes for all 16 rows of
     // every request) is latency-bound.  It keeps to two CTAs per SM, so that
-    // the next step's proposal finds room beside it; where a thread then has
-    // more vectors to read than the two register groups of the ordinary
-    // kernel hold, the DEEP variant (two CTAs per SM by its register use)
-    // keeps twice as many loads in flight.
-    const int64_t max_work = (int64_t)a.B * kBlock * vpr;
-    const int64_t max_bytes = max_work * (int64_t)(VEC ? 16 : sizeof(typename Elem<DT>::T));
-    if (max_bytes > kVSmallBytes) return launch_step<DT, VEC, false>(a, L, smem, vpr, 0, s);
-    int packed = 0;
-    const int rc = occupancy<k_verify_step<DT, VEC, false>>(smem, &packed);
-    if (rc != CLK_OK) return rc;
-    const int sms = packed % 1024;
-    if constexpr (VEC) {
-        if (max_work > (int64_t)kVSmallPerSm * sms * kVThreads * 2 * kUnroll)
-            return launch_step<DT, VEC, true>(a, L, smem, vpr, 0, s);
-    }
-    return launch_step<DT, VEC, false>(a, L, smem, vpr, kVSmallPerSm, s);
+    // the next step's proposal finds room beside it, and splits few rows in
+    // whole-row parts.
+    const int64_t max_bytes = (int64_t)a.B * kBlock * vpr * (int64_t)(VEC ? 16 : sizeof(typename Elem<DT>::T));
+    return launch_step<DT, VEC>(a, L, smem, vpr, max_bytes <= kVSmallBytes ? kVSmallPerSm : 0, s);
 }
 
 int verify_dispatch(const VerifyArgs& a, int32_t dtype, bool fused, const LookupDev& L, cudaStream_t s)
@@ -992,6 +980,7 @@ extern "C" int clk_verify_greedy(const void* d_logits, int32_t dtype, int64_t ro
     a.done = a.keys + (size_t)B * kBlock;
     a.slots = nullptr;
     a.late = 0;
+    a.aligned = 0;
     LookupDev none = {};
     return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
 }
@@ -1029,6 +1018,7 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     // It may overlap the proposal launch before it: the count of its CTAs
     // that start behind that launch is worked out at launch.
     a.late = 1;
+    a.aligned = 0;
     rc = verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
     if (rc == CLK_OK) {
         h->vparity ^= 1;
@@ -1146,6 +1136,7 @@ extern "C" int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int
     a.done = a.keys + (size_t)B * kBlock;
     a.slots = nullptr;
     a.late = 0;
+    a.aligned = 0;
     LookupDev none = {};
     return verify_dispatch(a, dtype, false, none, (cudaStream_t)s);
 }
