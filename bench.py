@@ -680,7 +680,7 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp=None):
     from workload import drive
 
     W = args.warmup
-    n = min(args.steps, args.e2e_steps)
+    n = min(args.steps, args.e2e_steps, pos_hist.shape[0] - 1 - W)  # within the workload's steps
     B, V = w.B, w.V
     per_step = B * 16 * V * (2 if w.dtype == wl.BF16 else 4)
     chunk = max(1, min(n, int(args.e2e_gb * 2 ** 30 // per_step)))
