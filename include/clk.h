@@ -118,7 +118,8 @@ typedef struct clk_slot_info {
     int32_t has_prev; /* a scheduler step has run since the slot was set up */
     int32_t cur_len;  /* block length chosen by the last scheduler step, 0 after append */
     int32_t n_indexed; /* the index holds every k-gram ending before position n_indexed - 1; the
-                          positions committed since are indexed by the next proposal launch */
+                          positions committed since are indexed by the next proposal launches, and
+                          n_indexed is raised by the launch after the one that indexed them */
 } clk_slot_info;
 
 typedef struct clk_lookup clk_lookup; /* opaque host handle */
@@ -190,8 +191,12 @@ CLK_API int clk_lookup_append(clk_lookup* h, const int32_t* d_slots, int32_t B, 
  * i = 0..15: the tokens that followed the occurrence, continued as an LZ77
  * copy at distance n - j past the end of the history (all CLK_SENT when
  * k = 0).  Outputs: d_draft [B,16], d_k [B], d_j [B].  The launch also
- * indexes any tokens committed by clk_verify_append since the slot's last
- * proposal. */
+ * indexes tokens committed by clk_verify_append since the slot's earlier
+ * proposals: all of them when more than 16 are pending or B > 32; else it
+ * may leave up to 16 to the next proposal launch on the handle (which runs
+ * them before its own wait when a clk_verify_append came in between).  The
+ * answers never depend on which launch indexes a position: pending
+ * positions are checked directly. */
 CLK_API int clk_lookup_propose(clk_lookup* h, const int32_t* d_slots, int32_t B, int32_t* d_draft, int32_t* d_k,
                                int32_t* d_j, clk_stream_t s);
 
@@ -241,7 +246,8 @@ CLK_API int clk_fuse_sched(clk_lookup* h, const int32_t* d_slots, int32_t B, con
  * request).  Bit-identical to the three calls.  Like clk_lookup_propose it
  * first waits for the preceding launch on the stream (programmatic dependent
  * launch) and indexes the tokens that clk_verify_append committed since the
- * slot's last proposal.  When the handle's last fused verify was
+ * slot's earlier proposals (some of them possibly left to the next
+ * proposal, as there).  When the handle's last fused verify was
  * clk_verify_append, the launch lets the next launch on the stream (the
  * step's clk_verify_append, which starts streaming its predicted rows) begin
  * before that wait; otherwise only after it. */
@@ -308,8 +314,8 @@ CLK_API int clk_verify_greedy_static(const void* d_logits, int32_t dtype, int64_
 /* clk_verify_greedy followed by clk_lookup_append of its d_out_tok /
  * d_emitted, in one launch: each request's tokens are committed to its
  * history as soon as its rows are verified; the k-grams they complete are
- * indexed by the next clk_lookup_propose / clk_propose_fuse_sched /
- * clk_lookup_append on the slot (which see the same answers as with an
+ * indexed by the following clk_lookup_propose / clk_propose_fuse_sched /
+ * clk_lookup_append calls on the slot (which see the same answers as with an
  * immediate index update).  Uses the scratch inside the lookup workspace.
  * Results are bit-identical to the two calls.
  * Launch order: the launch is a programmatic dependent of the preceding
