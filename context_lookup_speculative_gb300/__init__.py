@@ -371,13 +371,16 @@ def verify_greedy_static(logits, block, length, argmax, accept, emitted, out_tok
                                           _ptr(out_tok, shape=(B, BLOCK)), _stream(stream)))
 
 
-def verify_sample_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None) -> torch.Tensor:
+def verify_sample_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None, halves: int = 1) -> torch.Tensor:
     """A zeroed scratch buffer for verify_sample with vocabulary V and up to
-    B requests (logits_dtype: torch.bfloat16 or torch.float32)."""
+    B requests (logits_dtype: torch.bfloat16 or torch.float32).  halves=2:
+    two halves (each rounded up to 256 bytes), which verify_sample_append
+    alternates so that a call may start while the previous one finishes."""
     dt = BF16 if logits_dtype == torch.bfloat16 else F32
     n = ctypes.c_size_t()
     _check("clk_verify_sample_scratch_bytes", lib().clk_verify_sample_scratch_bytes(dt, V, B, ctypes.byref(n)))
-    t = torch.empty(n.value, dtype=torch.uint8, device=device)
+    size = n.value if halves == 1 else 2 * ((n.value + 255) // 256 * 256)
+    t = torch.empty(size, dtype=torch.uint8, device=device)
     _check("clk_verify_scratch_init", lib().clk_verify_scratch_init(t.data_ptr(), t.numel(), _stream(stream)))
     return t
 
@@ -516,7 +519,8 @@ class Step:
             raise ValueError(f"logits must be [{self.B}, >= {self._rows}, V]")
         if self._sscratch is None or self._sscratch[0] != (logits.dtype, V):
             self._sscratch = ((logits.dtype, V), verify_sample_scratch(logits.dtype, V, self.B,
-                                                                       device=self.slots.device, stream=stream))
+                                                                       device=self.slots.device, stream=stream,
+                                                                       halves=2))
         p = self._p
         sc = self._sscratch[1]
         _check("clk_verify_sample_append",

@@ -162,6 +162,7 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     hh->bytes = L.total;
     hh->device = 0;
     hh->vparity = 0;
+    hh->sparity = 0;
     hh->last_fused = kFusedNone;
     hh->ptag = 0;
     hh->defer_tag = 0;

@@ -14,11 +14,14 @@ struct clk_lookup {
     void* ws;
     size_t bytes;
     int device;
-    // The fused greedy verify alternates between two scratch halves (vparity)
-    // so that it may start streaming while the previous one finishes; the
-    // proposal lets its dependent start at once only after such a verify
-    // (last_fused = kFusedGreedy), whose scratch use it then cannot disturb.
+    // The fused greedy verify alternates between two scratch halves (vparity),
+    // and so does the fused sampled verify given a caller scratch of two
+    // halves (sparity), so that each may start streaming while the previous
+    // one finishes; the proposal lets its dependent start at once only after
+    // such a verify (last_fused = kFusedGreedy or kFusedSampledPaired), whose
+    // scratch use it then cannot disturb.
     int vparity;
+    int sparity;
     int last_fused;
     // Proposal launches number themselves with ptag and leave ins records
     // (what they leave complete in the index, and insertions left to the
@@ -34,7 +37,7 @@ struct clk_lookup {
 namespace clk {
 
 constexpr size_t kAlign = 256;
-constexpr int kFusedNone = 0, kFusedGreedy = 1, kFusedSampled = 2;
+constexpr int kFusedNone = 0, kFusedGreedy = 1, kFusedSampled = 2, kFusedSampledPaired = 3;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

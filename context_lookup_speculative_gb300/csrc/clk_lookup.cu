@@ -359,9 +359,9 @@ __global__ void __maxnreg__(64) k_lookup_step(
     // Launched as a programmatic dependent of the previous step's verify
     // launch, which commits the tokens this launch reads: wait for it.  This
     // step's verify launch may start streaming its first rows before (early:
-    // the previous launch was a fused greedy verify, which uses the other
-    // half of the scratch and let this launch start only after its own wait)
-    // or only after that wait.
+    // the previous launch was a fused verify that uses the other half of its
+    // scratch and let this launch start only after its own wait) or only
+    // after that wait.
     if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // take != 0: the ins records of the previous proposal launch (tag take)
     // are read after the wait (that launch has completed by then).  pre: it
@@ -591,7 +591,7 @@ int launch_lookup_step(clk_lookup* h, const int32_t* slots, int32_t B, const int
                        cudaStream_t s)
 {
     const LookupDev& L = h->dev;
-    const int32_t early = h->last_fused == kFusedGreedy ? 1 : 0;
+    const int32_t early = h->last_fused == kFusedGreedy || h->last_fused == kFusedSampledPaired ? 1 : 0;
     // Tags alternate in parity (the record half), wrapping from 2^30 to 1.
     const int32_t tag = h->ptag = h->ptag >= (1 << 30) || h->ptag < 1 ? 1 : h->ptag + 1;
     const int32_t take = h->defer_tag;

@@ -76,6 +76,7 @@ struct SampleArgs {
     float2* part;    // [B][16][S][kSWarpsPerCta] (m, s) per warp
     const int32_t* slots;  // fused with the commit only: the requests' slots
     int32_t late;          // fused: trailing CTAs that start behind the proposal launch (0: none)
+    int32_t paired;        // fused: scratch in two halves; the next launch is let go after the wait
 };
 
 __device__ __forceinline__ bool len_valid(int32_t l) { return l >= 1 && l <= kBlock; }
@@ -777,8 +778,11 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
     __shared__ FinSmem fs;
     __shared__ SampleStepSmem ss;
     // Let the next launch (the next proposal) be scheduled; it waits for
-    // this grid to complete before it reads anything this grid writes.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid to complete before it reads anything this grid writes.  With
+    // paired scratch halves only after this launch's own wait: the next
+    // proposal may then let the next sampled verify start at once (on the
+    // other half), and by then the verify before this one has completed.
+    if (!a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int32_t B = a.B;
     int32_t* P1 = sm_p;
@@ -887,6 +891,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
             if (tid == 0) ss.ci += 1;
         } else {  // kActWait
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             rows_prefix(B, [&a, P1, Lc](int32_t b) {
                 const int32_t pr = P1[b + 1] - P1[b];
                 const int32_t Lb = __ldcg(a.len + b);
@@ -993,7 +998,7 @@ namespace {
 int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype, int64_t row_stride,
                  int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
                  const int32_t* d_len_hint, const float* d_inv_temp, const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
-                 int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs)
+                 int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs, bool paired = false)
 {
     int32_t S = 0;
     size_t need = 0;
@@ -1034,6 +1039,7 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     // Fused: it may overlap the proposal launch before it; the count of its
     // CTAs that start behind that launch is worked out at launch.
     a.late = h != nullptr ? 1 : 0;
+    a.paired = paired ? 1 : 0;
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
     const bool bf = dtype == CLK_DTYPE_BF16;
@@ -1072,10 +1078,26 @@ extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, c
                                         size_t scratch_bytes, clk_stream_t s)
 {
     if (h == nullptr) return CLK_EINVAL;
-    // Its scratch is the caller's, one buffer for every step: the next
-    // proposal must not let the next verify start before this one completes.
-    h->last_fused = kFusedSampled;
-    return sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_len_hint,
-                        d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
-                        (cudaStream_t)s);
+    // A scratch of two halves (each the size this batch needs, rounded up to
+    // 256 bytes): consecutive calls alternate them, and the next proposal may
+    // let the next call start streaming before its own wait.  One buffer:
+    // the next proposal must not let the next verify start before this one
+    // completes.
+    int32_t S = 0;
+    size_t need = 0;
+    const bool paired = sample_sizes(dtype, V, B, &S, &need) == CLK_OK && d_scratch != nullptr &&
+                        scratch_bytes >= 2 * align_up(need, 256);
+    void* half = paired ? static_cast<char*>(d_scratch) + (size_t)h->sparity * align_up(need, 256) : d_scratch;
+    const size_t half_bytes = paired ? align_up(need, 256) : scratch_bytes;
+    const int rc = sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len,
+                                d_len_hint, d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, half, half_bytes,
+                                (cudaStream_t)s, paired);
+    if (rc == CLK_OK && paired) {
+        h->sparity ^= 1;
+        h->last_fused = kFusedSampledPaired;
+        h->vsince = 1;
+    } else {
+        h->last_fused = rc == CLK_OK ? kFusedSampled : kFusedNone;
+    }
+    return rc;
 }

@@ -402,7 +402,13 @@ CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_s
  * latches CLK_EINVAL in the handle's status (as do a bad slot, an
  * out-of-vocabulary token or a full history, which clk_lookup_append would
  * reject).  Scratch as for clk_verify_sample; calls sharing it must not
- * overlap on the GPU. */
+ * overlap on the GPU.  A scratch of at least twice the needed size rounded
+ * up to 256 bytes is used as two halves that consecutive calls on the
+ * handle alternate (all of it zeroed before the first use): then, as after
+ * clk_verify_append, the next clk_propose_fuse_sched lets the next call
+ * start streaming before its own wait, and a call lets the next launch on
+ * the stream start only after its own wait.  With a smaller scratch the next
+ * proposal lets the next call start only after that wait. */
 CLK_API int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
                                      int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
                                      const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
