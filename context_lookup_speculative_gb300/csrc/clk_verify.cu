@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(kVThreads, 4) k_verify(VerifyArgs a, LookupDev
 // A CTA with a short share (small batches) streams all of it first.
 constexpr int kVMaxDefer = 32;
 constexpr int64_t kVSplitMin = 64 * kVThreads;  // vectors: shares below this are not split
-constexpr int64_t kLateBytes = 60ll << 20;      // HBM bytes streamed before the late CTAs start (measured)
+constexpr int64_t kLateBytes = 120ll << 20;     // HBM bytes streamed before the late CTAs start (tuned)
 constexpr int64_t kVSmallBytes = 32ll << 20;     // logits (16 rows a request) of a latency-bound launch
 constexpr int kVSmallPerSm = 2;                  // its CTAs per SM
 
