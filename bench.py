@@ -281,11 +281,13 @@ def run_ours(args, world, rank, local, dist):
         return g
 
     # Pass B: the first steps once more with an event around every launch, for
-    # each kernel's own duration (launches serialised by the events).
+    # each kernel's own duration (launches serialised by the events, so the
+    # verify launches are made as launched alone: every CTA an even share).
     warmup()
     nb = min(chunk, K)
     generate(W, nb)
     lens_b = torch.zeros((nb, B), dtype=torch.int32, device=device)
+    lk.set_alone(True)
     try:
         # events recorded inside a graph must be "external" to be timed
         ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 * nb)]
@@ -304,6 +306,7 @@ def run_ours(args, world, rank, local, dist):
             ev[3 * i + 2].record(stream)
             lens_b[i].copy_(st.length)
         torch.cuda.synchronize()
+    lk.set_alone(False)
     pre_ms = sum(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(nb))
     verify_ms = sum(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(nb))
     cb = lk.counters(-1)

@@ -90,6 +90,7 @@ _SIGS = [
     ("clk_lookup_workspace_bytes", ctypes.c_int, [_P, _I32, _I64, ctypes.POINTER(ctypes.c_size_t)]),
     ("clk_lookup_create", ctypes.c_int, [ctypes.POINTER(_P), _P, _I32, _I64, _I32, _P, ctypes.c_size_t]),
     ("clk_lookup_reset", ctypes.c_int, [_P, _P]),
+    ("clk_lookup_set_alone", ctypes.c_int, [_P, _I32]),
     ("clk_lookup_init", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_append", ctypes.c_int, [_P, _P, _I32, _P, _P, _P]),
     ("clk_lookup_propose", ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P]),
@@ -207,6 +208,11 @@ class Lookup:
             except Exception:
                 pass
             self.handle = None
+
+    def set_alone(self, alone: bool):
+        """clk_lookup_set_alone: True when the fused verify calls are launched
+        with nothing to overlap (timing only; results are the same)."""
+        _check("clk_lookup_set_alone", lib().clk_lookup_set_alone(self.handle, 1 if alone else 0))
 
     # -- inspection (synchronising) -------------------------------------
     def status(self, stream=None):

@@ -167,8 +167,16 @@ extern "C" int clk_lookup_create(clk_lookup** h, const clk_params* p, int32_t ma
     hh->ptag = 0;
     hh->defer_tag = 0;
     hh->vsince = 0;
+    hh->alone = 0;
     cudaGetDevice(&hh->device);
     *h = hh;
+    return CLK_OK;
+}
+
+extern "C" int clk_lookup_set_alone(clk_lookup* h, int32_t alone)
+{
+    if (!handle_ok(h)) return CLK_ESTATE;
+    h->alone = alone != 0 ? 1 : 0;
     return CLK_OK;
 }
 

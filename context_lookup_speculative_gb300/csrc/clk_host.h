@@ -32,6 +32,9 @@ struct clk_lookup {
     int32_t ptag;
     int32_t defer_tag;
     int vsince;
+    // 1: fused verify calls are launched with nothing to overlap
+    // (clk_lookup_set_alone), so no CTA of theirs starts late.
+    int alone;
 };
 
 namespace clk {

@@ -1038,7 +1038,7 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     a.slots = d_slots;
     // Fused: it may overlap the proposal launch before it; the count of its
     // CTAs that start behind that launch is worked out at launch.
-    a.late = h != nullptr ? 1 : 0;
+    a.late = h != nullptr && !h->alone ? 1 : 0;
     a.paired = paired ? 1 : 0;
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;

@@ -1015,9 +1015,10 @@ extern "C" int clk_verify_append(clk_lookup* h, const int32_t* d_slots, const vo
     a.keys = h->dev.vkeys + (size_t)par * (size_t)h->dev.max_slots * kBlock;
     a.done = h->dev.vdone + (size_t)par * (size_t)h->dev.max_slots;
     a.slots = d_slots;
-    // It may overlap the proposal launch before it: the count of its CTAs
-    // that start behind that launch is worked out at launch.
-    a.late = 1;
+    // It may overlap the proposal launch before it (unless the handle says
+    // it is launched alone): the count of its CTAs that start behind that
+    // launch is worked out at launch.
+    a.late = h->alone ? 0 : 1;
     a.aligned = 0;
     rc = verify_dispatch(a, dtype, true, h->dev, (cudaStream_t)s);
     if (rc == CLK_OK) {

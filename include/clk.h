@@ -453,6 +453,17 @@ CLK_API int clk_lookup_read_history(clk_lookup* h, int32_t slot, int32_t* h_out,
 CLK_API int clk_lookup_restore_state(clk_lookup* h, int32_t slot, const clk_slot_info* info,
                                      const clk_counters* counters, clk_stream_t s);
 
+/* Launch setting of the handle's fused verify calls (clk_verify_append,
+ * clk_verify_sample_append).  alone = 0 (the default): a call expects to
+ * follow the step's proposal launch directly on the stream and to overlap
+ * it, so it gives its CTAs that will be dispatched behind the proposal's
+ * CTAs a smaller share of the rows.  alone = 1: each call is launched with
+ * nothing to overlap (e.g. other work or event records between the
+ * launches), and every CTA gets an even share.  Results do not depend on it;
+ * only the timing does.  Host-side only: affects the calls made after it.
+ * CLK_ESTATE for a bad handle. */
+CLK_API int clk_lookup_set_alone(clk_lookup* h, int32_t alone);
+
 /* Frees the host handle (not the workspace). */
 CLK_API void clk_lookup_destroy(clk_lookup* h);
 

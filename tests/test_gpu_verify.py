@@ -226,6 +226,36 @@ def test_fused_verify_results_do_not_depend_on_the_length_hint(hint):
     assert lk.status()[0] == (clk.EINVAL if (L == 0).any() else 0)
 
 
+@pytest.mark.parametrize("alone", [False, True])
+def test_fused_verify_split_setting_changes_no_result(alone):
+    """A launch large enough (67 MB of rows) that, expecting to overlap the
+    proposal launch, it gives its trailing CTAs a smaller share; launched
+    alone (clk_lookup_set_alone) it splits evenly.  Outputs and commits are
+    the oracle's either way."""
+    rng = np.random.default_rng(9)
+    B, V = 64, 32768
+    x = torch.from_numpy(rng.integers(-20, 20, size=(B, 16, V)).astype(np.float32)).to("cuda").to(torch.bfloat16)
+    L = rng.choice([8, 16], size=B).astype(np.int32)
+    block = _blocks_from(_np_view(x), L, rng, p_agree=0.9)
+    want = _oracle_rows(_np_view(x), block, L)
+    lk = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+    lk.set_alone(alone)
+    s = torch.arange(B, dtype=torch.int32, device="cuda")
+    clk.lookup_init(lk, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                    torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+    z = lambda *sh: torch.full(sh, 77, dtype=torch.int32, device="cuda")  # noqa: E731
+    g, a, e, out = z(B, 16), z(B), z(B), z(B, 16)
+    hint = torch.from_numpy(rng.choice([8, 16], size=B).astype(np.int32)).cuda()
+    clk.verify_append(lk, s, x, torch.from_numpy(block).cuda(), torch.from_numpy(L).cuda(), g, a, e, out,
+                      length_hint=hint)
+    torch.cuda.synchronize()
+    for name, gg, ww in zip(("argmax", "accept", "emitted", "out_tok"), (g, a, e, out), want):
+        assert np.array_equal(gg.cpu().numpy(), ww), name
+    for b in range(B):
+        assert lk.history(b).tolist() == [1] + want[3][b][:want[2][b]].tolist()
+    assert lk.status() == (0, 0)
+
+
 def test_maximum_batch():
     """B = CLK_MAX_BATCH (8,192) requests: the stateless verify against the
     oracle, and the static-scratch entry's limit (1,024 requests)."""
