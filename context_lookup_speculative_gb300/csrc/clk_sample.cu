@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
 // sets the counter back to zero.  The inverse temperatures are read before
 // the wait, so they must not come from the proposal launch.
 constexpr int kSMaxDefer = 32;
-constexpr int64_t kSLateBytes = 60ll << 20;  // HBM bytes in the ~10 us a proposal launch runs
+constexpr int64_t kSLateBytes = 90ll << 20;  // HBM bytes streamed before the late CTAs start (tuned)
 
 // The block's next action, chosen by thread 0.
 enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
