@@ -380,8 +380,9 @@ def verify_greedy_static(logits, block, length, argmax, accept, emitted, out_tok
 def verify_sample_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None, halves: int = 1) -> torch.Tensor:
     """A zeroed scratch buffer for verify_sample with vocabulary V and up to
     B requests (logits_dtype: torch.bfloat16 or torch.float32).  halves=2:
-    two halves (each rounded up to 256 bytes), which verify_sample_append
-    alternates so that a call may start while the previous one finishes."""
+    two halves (each the needed size rounded up to 256 bytes), which
+    verify_sample_append alternates so that a call may start while the
+    previous one finishes."""
     dt = BF16 if logits_dtype == torch.bfloat16 else F32
     n = ctypes.c_size_t()
     _check("clk_verify_sample_scratch_bytes", lib().clk_verify_sample_scratch_bytes(dt, V, B, ctypes.byref(n)))

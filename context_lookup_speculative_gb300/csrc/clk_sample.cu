@@ -1078,20 +1078,19 @@ extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, c
                                         size_t scratch_bytes, clk_stream_t s)
 {
     if (h == nullptr) return CLK_EINVAL;
-    // A scratch of two halves (each the size this batch needs, rounded up to
-    // 256 bytes): consecutive calls alternate them, and the next proposal may
-    // let the next call start streaming before its own wait.  One buffer:
-    // the next proposal must not let the next verify start before this one
-    // completes.
+    // A scratch of two halves (each half of the buffer, rounded down to 256
+    // bytes, whatever the batch, and each at least what this batch needs):
+    // consecutive calls alternate them, and the next proposal may let the
+    // next call start streaming before its own wait.  One buffer: the next
+    // proposal must not let the next verify start before this one completes.
     int32_t S = 0;
     size_t need = 0;
-    const bool paired = sample_sizes(dtype, V, B, &S, &need) == CLK_OK && d_scratch != nullptr &&
-                        scratch_bytes >= 2 * align_up(need, 256);
-    void* half = paired ? static_cast<char*>(d_scratch) + (size_t)h->sparity * align_up(need, 256) : d_scratch;
-    const size_t half_bytes = paired ? align_up(need, 256) : scratch_bytes;
+    const size_t half_bytes = (scratch_bytes / 2) & ~(size_t)255;
+    const bool paired = sample_sizes(dtype, V, B, &S, &need) == CLK_OK && d_scratch != nullptr && half_bytes >= need;
+    void* half = paired ? static_cast<char*>(d_scratch) + (size_t)h->sparity * half_bytes : d_scratch;
     const int rc = sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len,
-                                d_len_hint, d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, half, half_bytes,
-                                (cudaStream_t)s, paired);
+                                d_len_hint, d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, half,
+                                paired ? half_bytes : scratch_bytes, (cudaStream_t)s, paired);
     if (rc == CLK_OK && paired) {
         h->sparity ^= 1;
         h->last_fused = kFusedSampledPaired;

@@ -402,9 +402,11 @@ CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_s
  * latches CLK_EINVAL in the handle's status (as do a bad slot, an
  * out-of-vocabulary token or a full history, which clk_lookup_append would
  * reject).  Scratch as for clk_verify_sample; calls sharing it must not
- * overlap on the GPU.  A scratch of at least twice the needed size rounded
- * up to 256 bytes is used as two halves that consecutive calls on the
- * handle alternate (all of it zeroed before the first use): then, as after
+ * overlap on the GPU.  A scratch whose halves (each half of its size,
+ * rounded down to a multiple of 256 bytes) each hold the needed size is used
+ * as two halves that consecutive calls on the handle alternate (all of it
+ * zeroed before the first use; the halves do not move with the batch): then,
+ * as after
  * clk_verify_append, the next clk_propose_fuse_sched lets the next call
  * start streaming before its own wait, and a call lets the next launch on
  * the stream start only after its own wait.  With a smaller scratch the next
