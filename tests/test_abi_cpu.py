@@ -120,6 +120,9 @@ def test_handle_over_fake_workspace_validates_batches(clk):
         assert L.clk_lookup_propose(h, 0x1000, 5, 0x1000, 0x1000, 0x1000, None) == clk.EINVAL
         assert L.clk_lookup_append(h, 0x1000, -1, 0x1000, 0x1000, None) == clk.EINVAL
         assert L.clk_lookup_propose(h, 0x1000, 0, 0x1000, 0x1000, 0x1000, None) == 0  # empty batch: no-op
+        # the launch setting is host state only
+        assert L.clk_lookup_set_alone(h, 1) == 0 and L.clk_lookup_set_alone(h, 0) == 0
+        assert L.clk_lookup_set_alone(None, 1) == clk.ESTATE
         assert L.clk_read_counters(h, 9, ctypes.byref(clk.Counters()), None) == clk.EINVAL
         # a resume refuses a bad slot or scheduler state before touching the device
         ok = clk.SlotInfo(n=5, mode=1, streak=0, miss=2, has_prev=1, cur_len=16, n_indexed=5)
