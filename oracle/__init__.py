@@ -32,7 +32,8 @@ def build(verbose: bool = False) -> str:
     """Compile clk_oracle.c into liboracle.so (plain -O2, no vector intrinsics)."""
     src = os.path.join(HERE, "clk_oracle.c")
     out = os.path.join(HERE, LIB_NAME)
-    cmd = ["gcc", "-O2", "-std=c11", "-D_POSIX_C_SOURCE=200809L", "-Wall", "-fPIC", "-shared", "-pthread",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-D_POSIX_C_SOURCE=200809L", "-Wall", "-fPIC", "-shared",
+           "-pthread",
            "-o", out, src, "-lm"]
     if verbose:
         print(" ".join(cmd))
@@ -79,7 +80,7 @@ class RunArgs(ctypes.Structure):
     _fields_ = [("params", _P), ("n_req", ctypes.c_int32), ("req_ids", _P), ("prompt", _P), ("prompt_off", _P),
                 ("steps", ctypes.c_int32), ("V", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("gen_ctx", _P), ("logits_fn", _P), ("head_fn", _P),
-                ("uniform_fn", _P), ("inv_temp", ctypes.c_float), ("pad0", ctypes.c_int32),
+                ("uniform_fn", _P), ("inv_temp", ctypes.c_float), ("exact", ctypes.c_int32),
                 ("rec_k", _P), ("rec_j", _P), ("rec_L", _P), ("rec_a", _P), ("rec_c", _P), ("rec_blk", _P),
                 ("rec_g", _P), ("hist_out", _P), ("hist_off", _P), ("hist_len", _P), ("counters", _P),
                 ("timed_from", ctypes.c_int32), ("pad", ctypes.c_int32),
@@ -112,6 +113,13 @@ def _lib() -> ctypes.CDLL:
     lib.or_sample_verify.argtypes = [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int32,
                                      ctypes.c_float, _P, _P]
     lib.or_sample_verify.restype = ctypes.c_int32
+    lib.or_sample_verify_exact.argtypes = lib.or_sample_verify.argtypes
+    lib.or_sample_verify_exact.restype = ctypes.c_int32
+    lib.or_fx_weight.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int32]
+    lib.or_fx_weight.restype = ctypes.c_uint64
+    lib.or_fx_chunks.argtypes = [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, _P, _P]
+    lib.or_fx_chunks.restype = ctypes.c_int
+    lib.or_fx_poly_coefs.argtypes = [_P]
     lib.or_run.argtypes = [ctypes.POINTER(RunArgs)]
     lib.or_run.restype = ctypes.c_int
     lib.or_counters_size.restype = ctypes.c_size_t
@@ -216,6 +224,54 @@ def sample_verify(rows: np.ndarray, blk, L: int, inv_temp: float, u) -> tuple:
     return int(a), out
 
 
+def _rows_dtype(rows):
+    rows = np.ascontiguousarray(rows)
+    if rows.dtype == np.uint16:
+        return rows, 0
+    return np.ascontiguousarray(rows, dtype=np.float32), 1
+
+
+def sample_verify_exact(rows: np.ndarray, blk, L: int, inv_temp: float, u) -> tuple:
+    """sample_verify on the fixed-point weights (or_sample_verify_exact):
+    the same rule, every decision an integer comparison.  a = -1 (and no
+    tokens) for an invalid L or temperature or a block that cannot be
+    weighed."""
+    rows, dtype = _rows_dtype(rows)
+    blk = _i32(blk)
+    u = np.ascontiguousarray(u, dtype=np.float32).reshape(BLOCK, 2)
+    out = np.empty(BLOCK, np.int32)
+    a = _lib().or_sample_verify_exact(rows.ctypes.data, dtype, rows.shape[1], rows.shape[1], blk.ctypes.data,
+                                      int(L), float(inv_temp), u.ctypes.data, out.ctypes.data)
+    return int(a), out
+
+
+FX_CHUNK = 1024  # entries per chunk of the fixed-point weights
+
+
+def fx_weight(x: float, s: float, R: int) -> int:
+    """Fixed-point weight Q(fma(x, s, -R)) of one entry (x, s float32)."""
+    return int(_lib().or_fx_weight(float(x), float(s), int(R)))
+
+
+def fx_chunks(row: np.ndarray, inv_temp: float):
+    """Chunk totals S and references R of one row, or None if the row cannot
+    be weighed."""
+    row, dtype = _rows_dtype(row)
+    V = row.size
+    nc = (V + FX_CHUNK - 1) // FX_CHUNK
+    S = np.zeros(nc, np.uint64)
+    R = np.zeros(nc, np.int32)
+    rc = _lib().or_fx_chunks(row.ctypes.data, dtype, V, float(inv_temp), S.ctypes.data, R.ctypes.data)
+    return None if rc != 0 else (S, R)
+
+
+def fx_poly_coefs() -> np.ndarray:
+    """The weight polynomial's 7 float32 Horner coefficients."""
+    out = np.zeros(7, np.float32)
+    _lib().or_fx_poly_coefs(out.ctypes.data)
+    return out
+
+
 # --------------------------------------------------------------------------
 # The whole decode loop
 # --------------------------------------------------------------------------
@@ -228,7 +284,7 @@ class RunResult:
 
 def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
         params: Optional[Params] = None, threads: Optional[int] = None, head=None,
-        timed_from: int = 0, inv_temp: float = 0.0) -> RunResult:
+        timed_from: int = 0, inv_temp: float = 0.0, exact: bool = False) -> RunResult:
     """Run the oracle decode loop of workload `w` for the given requests.
 
     The target logits and head proposals come from the host generator of the
@@ -241,7 +297,8 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     being the history append and bookkeeping.
     `inv_temp` > 0 verifies by sampling (point-mass drafts) at that inverse
     temperature with the generator's uniforms; the records' `g` then holds
-    each step's emitted tokens instead of the argmax rows."""
+    each step's emitted tokens instead of the argmax rows.  `exact` samples
+    on the fixed-point weights (sample_verify_exact)."""
     import workload as wl  # the seeded input generator shared by both sides
 
     p = params or Params.default()
@@ -276,6 +333,7 @@ def run(w, req_ids: Optional[Sequence[int]] = None, steps: Optional[int] = None,
     args.head_fn = gen.head_fn
     args.uniform_fn = gen.uniform_fn
     args.inv_temp = float(inv_temp)
+    args.exact = 1 if exact else 0
     if head is not None:
         proto = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                  ctypes.POINTER(ctypes.c_int32))

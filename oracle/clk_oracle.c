@@ -331,6 +331,271 @@ int32_t or_sample_verify(const void* rows, int32_t dtype, int64_t row_stride, in
 }
 
 /* ------------------------------------------------------------------------ */
+/* Exact sampling verification: the same rule on fixed-point weights.        */
+/* ------------------------------------------------------------------------ */
+/*
+ * The rule of or_sample_verify (accept iff u_acc < p_r(c); the first
+ * rejection draws from p_r without c; a full acceptance draws from the last
+ * row) with the target's weights defined as integers, so that every
+ * acceptance and every draw is an integer comparison that two
+ * implementations reach bit for bit.  Where floating point decides an
+ * integer, both sides must take that decision in the same precision; here
+ * that precision is float32 with fused multiply-adds, then integers.
+ *
+ * Row x (V entries, bf16 widened exactly or float32), inverse temperature t:
+ *   s = fl32(t * fl32(log2 e)); the row is cut into chunks of 1024 entries
+ *   (the last one ragged).  Chunk k's reference is R_k = ceil(fl32(M_k * s))
+ *   with M_k its largest entry; a chunk of -inf only has no reference and
+ *   weight 0.  Entry i of chunk k weighs q_i = Q(fma(x_i, s, -R_k)), where
+ *   for d < -32: Q(d) = 0, else with n = rint(d) (ties to even) and
+ *   r = d - n (exact, |r| <= 1/2):
+ *     f = P(r), the degree-6 Taylor polynomial of 2^(r + 1/2) = sqrt(2) 2^r
+ *         (coefficients sqrt(2) (ln 2)^k / k! rounded to float, evaluated by
+ *         Horner's rule with fmaf), a float in [1, 2];
+ *     m = bits(f) - bits(0.5f), i.e. f * 2^23 as an integer;
+ *     Q(d) = floor(64 m / 2^-n + 1/2), the nearest integer (halves up).
+ *   So q_i is 2^(z_i - R_k + 29.5) (z = x s) to within 2^-22 relative plus
+ *   half a unit.  S_k = sum of the chunk's q_i (exact) and R = max_k R_k.
+ *   Row units are 2^-12 of a unit of the reference R: a chunk's total in
+ *   them is U(S_k, R - R_k), with U(v, e) = v 2^(12 - e) for e <= 12 and
+ *   floor(v / 2^(e - 12)) above (0 from e - 12 >= 64); the row's total is
+ *   T = sum_k U(S_k, R - R_k).  (The 12 guard bits keep the floors of the
+ *   chunk totals far below one token's weight.)
+ *   A row of more than 4,194,304 entries, or whose chunk maxima have
+ *   |fl32(M_k s)| > 2^22 (or is NaN), or whose entries are all -inf, cannot
+ *   be weighed: the request gets the empty result (as for an invalid
+ *   length).
+ * A uniform u becomes the integer k(u) = floor(u 2^24) clamped to
+ * [0, 2^24 - 1] (NaN: 0); the generator's uniforms are multiples of 2^-24,
+ * so k(u) = u 2^24 exactly.
+ * Acceptance of a draft c in [0, V) at row r: with q_c its weight in its
+ *   chunk kc and w = U(q_c, R - R_kc), accept iff
+ *   floor(k(u_acc) T / 2^24) < w (i.e. u_acc < w / T).  A sentinel draft is
+ *   rejected and removes nothing.
+ * The draw with u_smp (residual after removing c, or the last row): the
+ *   chunk weights become T'_k = U(S_k - [k = kc] q_c, R - R_k),
+ *   T' = sum T'_k, t = floor(k(u_smp) T' / 2^24); the chunk is the first
+ *   whose running sum of T'_k exceeds t, and inside it, with t_c the
+ *   remainder t - (earlier chunks' T'_k) taken back to chunk units
+ *   (times 2^(e - 12), or floor(/ 2^(12 - e)), e = R - R_k), the token is
+ *   the first entry (c skipped) whose running sum of q_i exceeds t_c.  One
+ *   always exists.
+ */
+#define OR_FX_CHUNK 1024
+#define OR_FX_NOREF (-16777216) /* a chunk of -inf only */
+
+/* Horner coefficients c[k] = sqrt(2) (ln 2)^k / k!, from the recurrence
+ * t_0 = sqrt(2), t_{k+1} = t_k * ln2 / (k + 1) in double, each rounded to
+ * float. */
+static void or_fx_coefs(float c[7])
+{
+    double t = 1.4142135623730951;           /* sqrt(2), correctly rounded */
+    const double ln2 = 0.6931471805599453;   /* ln 2, correctly rounded */
+    for (int k = 0; k < 7; ++k) {
+        c[k] = (float)t;
+        t = t * ln2 / (double)(k + 1);
+    }
+}
+
+static float or_row_value(const void* row, int32_t dtype, int64_t v)
+{
+    return dtype == 0 ? or_bf16_value(((const uint16_t*)row)[v]) : ((const float*)row)[v];
+}
+
+/* Q(d) of one entry with d = fma(x, s, -R). */
+static uint64_t or_fx_q(float x, float s, float R, const float c[7])
+{
+    const float d = fmaf(x, s, -R);
+    if (!(d >= -32.0f)) return 0;  /* also -inf */
+    const float n = rintf(d);
+    const float r = d - n;
+    float f = c[6];
+    for (int k = 5; k >= 0; --k) f = fmaf(f, r, c[k]);
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    const uint64_t m = (uint64_t)(bits - 0x3F000000u);
+    const int sh = (int)(-n); /* 0..32: d <= 1/4 for every entry */
+    return (((m << 7) >> sh) + 1) >> 1;
+}
+
+/* floor(k v / 2^24) for k < 2^24 and v < 2^62, without 128-bit products. */
+static uint64_t or_fx_mulshift(uint32_t k, uint64_t v)
+{
+    return (uint64_t)k * (v >> 24) + (((uint64_t)k * (v & 0xFFFFFFu)) >> 24);
+}
+
+static uint32_t or_fx_unit(float u)
+{
+    const float v = u * 16777216.0f;
+    if (!(v > 0.0f)) return 0;
+    if (v >= 16777215.0f) return 16777215u;
+    return (uint32_t)v;
+}
+
+#define OR_FX_GUARD 12
+#define OR_FX_VMAX 4194304
+
+/* U(v, e): a chunk quantity v in row units, e = R - R_k >= 0. */
+static uint64_t or_fx_rowunits(uint64_t v, int32_t e)
+{
+    if (e <= OR_FX_GUARD) return v << (OR_FX_GUARD - e);
+    return e - OR_FX_GUARD >= 64 ? 0 : v >> (e - OR_FX_GUARD);
+}
+
+/* A row-unit remainder back in chunk units. */
+static uint64_t or_fx_chunkunits(uint64_t v, int32_t e)
+{
+    return e >= OR_FX_GUARD ? v << (e - OR_FX_GUARD) : v >> (OR_FX_GUARD - e);
+}
+
+/* Chunk references R[k] and totals S[k] of one row; returns -1 when the row
+ * cannot be weighed. */
+static int or_fx_row(const void* row, int32_t dtype, int64_t V, float s, const float c[7], uint64_t* S, int32_t* R)
+{
+    const int64_t nc = (V + OR_FX_CHUNK - 1) / OR_FX_CHUNK;
+    int any = 0;
+    for (int64_t k = 0; k < nc; ++k) {
+        const int64_t v0 = k * OR_FX_CHUNK, v1 = v0 + OR_FX_CHUNK < V ? v0 + OR_FX_CHUNK : V;
+        float M = -INFINITY;
+        for (int64_t v = v0; v < v1; ++v) {
+            const float x = or_row_value(row, dtype, v);
+            if (x > M) M = x;
+        }
+        S[k] = 0;
+        if (M == -INFINITY) {
+            R[k] = OR_FX_NOREF;
+            continue;
+        }
+        const float y = M * s;
+        if (!(fabsf(y) <= 4194304.0f)) return -1;
+        R[k] = (int32_t)ceilf(y);
+        any = 1;
+        for (int64_t v = v0; v < v1; ++v) S[k] += or_fx_q(or_row_value(row, dtype, v), s, (float)R[k], c);
+    }
+    return any ? 0 : -1;
+}
+
+static int32_t or_fx_ref(const int32_t* R, int64_t nc)
+{
+    int32_t m = OR_FX_NOREF;
+    for (int64_t k = 0; k < nc; ++k)
+        if (R[k] > m) m = R[k];
+    return m;
+}
+
+/* The draw from a weighed row with token excl (weight qx) removed; excl
+ * outside [0, V) removes nothing. */
+static int32_t or_fx_draw(const void* row, int32_t dtype, int64_t V, float s, const float c[7], const uint64_t* S,
+                          const int32_t* R, int32_t excl, uint64_t qx, float u)
+{
+    const int64_t nc = (V + OR_FX_CHUNK - 1) / OR_FX_CHUNK;
+    const int32_t Rr = or_fx_ref(R, nc);
+    const int64_t kx = (excl >= 0 && excl < V) ? excl / OR_FX_CHUNK : -1;
+    uint64_t total = 0;
+    for (int64_t k = 0; k < nc; ++k) total += or_fx_rowunits(S[k] - (k == kx ? qx : 0), Rr - R[k]);
+    const uint64_t t = or_fx_mulshift(or_fx_unit(u), total);
+    uint64_t before = 0;
+    for (int64_t k = 0; k < nc; ++k) {
+        const uint64_t tk = or_fx_rowunits(S[k] - (k == kx ? qx : 0), Rr - R[k]);
+        if (before + tk > t) {
+            const uint64_t tc = or_fx_chunkunits(t - before, Rr - R[k]);
+            const int64_t v0 = k * OR_FX_CHUNK, v1 = v0 + OR_FX_CHUNK < V ? v0 + OR_FX_CHUNK : V;
+            uint64_t run = 0;
+            for (int64_t v = v0; v < v1; ++v) {
+                if (v == excl) continue;
+                run += or_fx_q(or_row_value(row, dtype, v), s, (float)R[k], c);
+                if (run > tc) return (int32_t)v;
+            }
+            return OR_SENT; /* not reached: tc < the chunk's sum */
+        }
+        before += tk;
+    }
+    return OR_SENT; /* not reached: t < total */
+}
+
+/* One request, as or_sample_verify, on the fixed-point weights.  Returns the
+ * number of accepted drafts, or -1 (and no tokens) for an invalid L or
+ * temperature or a row that cannot be weighed. */
+int32_t or_sample_verify_exact(const void* rows, int32_t dtype, int64_t row_stride, int64_t V, const int32_t* blk,
+                               int32_t L, float inv_temp, const float* u, int32_t* out_tok)
+{
+    for (int i = 0; i < OR_BLOCK; ++i) out_tok[i] = OR_SENT;
+    if (L < 1 || L > OR_BLOCK || V < 1 || V > OR_FX_VMAX) return -1;
+    if (!(inv_temp > 0.0f && inv_temp < INFINITY)) return -1;
+    const size_t rb = (size_t)row_stride * (dtype == 0 ? sizeof(uint16_t) : sizeof(float)); /* bytes per row */
+    const int64_t nc = (V + OR_FX_CHUNK - 1) / OR_FX_CHUNK;
+    const float s = inv_temp * 1.44269504088896341f;
+    float c[7];
+    or_fx_coefs(c);
+    uint64_t* S = (uint64_t*)malloc((size_t)(nc * L) * sizeof(uint64_t));
+    int32_t* R = (int32_t*)malloc((size_t)(nc * L) * sizeof(int32_t));
+    if (S == NULL || R == NULL) {
+        free(S);
+        free(R);
+        return -1;
+    }
+    /* every row of the block must be weighable, whichever rows are used */
+    for (int32_t r = 0; r < L; ++r) {
+        const void* row = (const char*)rows + (size_t)r * rb;
+        if (or_fx_row(row, dtype, V, s, c, S + r * nc, R + r * nc) != 0) {
+            free(S);
+            free(R);
+            return -1;
+        }
+    }
+    int32_t a = 0, tok = OR_SENT;
+    for (int32_t r = 0; r < L; ++r) {
+        const void* row = (const char*)rows + (size_t)r * rb;
+        const uint64_t* Sr = S + r * nc;
+        const int32_t* Rrow = R + r * nc;
+        if (r == L - 1) {
+            tok = or_fx_draw(row, dtype, V, s, c, Sr, Rrow, -1, 0, u[2 * r + 1]);
+            break;
+        }
+        const int32_t cd = blk[r + 1];
+        if (cd >= 0 && cd < V) {
+            const int32_t Rr = or_fx_ref(Rrow, nc);
+            uint64_t T = 0;
+            for (int64_t k = 0; k < nc; ++k) T += or_fx_rowunits(Sr[k], Rr - Rrow[k]);
+            const int64_t kc = cd / OR_FX_CHUNK;
+            const uint64_t qc = or_fx_q(or_row_value(row, dtype, cd), s, (float)Rrow[kc], c);
+            const uint64_t w = or_fx_rowunits(qc, Rr - Rrow[kc]);
+            if (or_fx_mulshift(or_fx_unit(u[2 * r]), T) < w) {
+                out_tok[r] = cd;
+                a += 1;
+                continue;
+            }
+            tok = or_fx_draw(row, dtype, V, s, c, Sr, Rrow, cd, qc, u[2 * r + 1]);
+        } else {
+            tok = or_fx_draw(row, dtype, V, s, c, Sr, Rrow, -1, 0, u[2 * r + 1]);
+        }
+        break;
+    }
+    out_tok[a] = tok;
+    free(S);
+    free(R);
+    return a;
+}
+
+/* Test access to the pieces of the exact rule (one entry's weight, a row's
+ * chunk references and totals, the uniform's integer). */
+uint64_t or_fx_weight(float x, float s, int32_t R)
+{
+    float c[7];
+    or_fx_coefs(c);
+    return or_fx_q(x, s, (float)R, c);
+}
+
+int or_fx_chunks(const void* row, int32_t dtype, int64_t V, float inv_temp, uint64_t* S, int32_t* R)
+{
+    float c[7];
+    or_fx_coefs(c);
+    return or_fx_row(row, dtype, V, inv_temp * 1.44269504088896341f, c, S, R);
+}
+
+void or_fx_poly_coefs(float* out) { or_fx_coefs(out); }
+
+/* ------------------------------------------------------------------------ */
 /* Whole decode loop over a set of requests.                                 */
 /* ------------------------------------------------------------------------ */
 
@@ -355,7 +620,7 @@ typedef struct or_run_args {
     or_head_fn head_fn;
     or_uniform_fn uniform_fn; /* sampling verification only */
     float inv_temp;           /* > 0: sampling verification at this 1/temperature; 0: greedy */
-    int32_t pad0;
+    int32_t exact;            /* sampling on the fixed-point weights (or_sample_verify_exact) */
     /* outputs, indexed [t][i] or [t][i][16] with i the request's position */
     int32_t* rec_k;
     int32_t* rec_j;
@@ -450,7 +715,12 @@ static int or_run_request(or_run_args* a, int32_t i, int64_t* method_ns, int64_t
             for (int32_t r = 0; r < L; ++r) a->logits_fn(a->gen_ctx, b, n + r, (char*)row + (size_t)r * a->V * esz);
             a->uniform_fn(a->gen_ctx, b, t, u);
             prov += or_now_ns() - u0;
-            acc = or_sample_verify(row, a->dtype, a->V, a->V, blk, L, a->inv_temp, u, g);
+            acc = a->exact ? or_sample_verify_exact(row, a->dtype, a->V, a->V, blk, L, a->inv_temp, u, g)
+                           : or_sample_verify(row, a->dtype, a->V, a->V, blk, L, a->inv_temp, u, g);
+            if (acc < 0) {
+                rc = -3;
+                break;
+            }
         } else {
             for (int32_t r = 0; r < L; ++r) {
                 u0 = or_now_ns();
@@ -527,7 +797,8 @@ static void* or_worker(void* arg)
 }
 
 /* Runs the decode loop for every request, `threads` requests at a time.
- * Returns 0, -1 (out of memory) or -2 (history capacity). */
+ * Returns 0, -1 (out of memory), -2 (history capacity) or -3 (a sampled block
+ * that cannot be weighed: see or_sample_verify_exact). */
 int or_run(or_run_args* a)
 {
     or_shared sh;
