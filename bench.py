@@ -498,7 +498,9 @@ def run_sample_verify(args, world, rank, local, dist):
     each launch reads its own pre-generated logits (larger than L2) at
     temperature 0.3, with drafts that follow the synthetic target's favoured
     token except for 20 % random ones; long blocks for the copy-heavy
-    requests, short ones for the chat-like.  CUDA events around every launch."""
+    requests, short ones for the chat-like.  CUDA events around every launch.
+    With --exact: the exact sampler (clk_verify_sample_exact, fixed-point
+    weights) on the same inputs."""
     import numpy as np
     import torch
 
@@ -530,11 +532,16 @@ def run_sample_verify(args, world, rank, local, dist):
     u = torch.rand((K, B, 16, 2), generator=g, device=device)
     acc = torch.zeros(B, dtype=torch.int32, device=device)
     em, out = torch.zeros_like(acc), torch.zeros((B, 16), dtype=torch.int32, device=device)
-    scratch = clk.verify_sample_scratch(bufs.dtype, V, B, device=device)
+    exact = bool(getattr(args, "exact", False))
+    if exact:
+        verify = clk.verify_sample_exact
+        scratch = clk.verify_sample_exact_scratch(bufs.dtype, V, B, device=device)
+    else:
+        verify = clk.verify_sample
+        scratch = clk.verify_sample_scratch(bufs.dtype, V, B, device=device)
     flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
     for i in range(W):
-        clk.verify_sample(bufs[i % K], blks[i % K], L, t, u[i % K], acc, em, out, scratch)
+        verify(bufs[i % K], blks[i % K], L, t, u[i % K], acc, em, out, scratch)
     flush.zero_()
     torch.cuda.synchronize()
     # The K launches as one CUDA graph with an event around each (no host
@@ -545,7 +552,7 @@ def run_sample_verify(args, world, rank, local, dist):
     def launches(ev):
         for i in range(K):
             ev[2 * i].record()
-            clk.verify_sample(bufs[i], blks[i], L, t, u[i], acc, em, out, scratch)
+            verify(bufs[i], blks[i], L, t, u[i], acc, em, out, scratch)
             ev[2 * i + 1].record()
             emitted.add_(em)
 
@@ -569,15 +576,19 @@ def run_sample_verify(args, world, rank, local, dist):
     mean_us = float(np.mean(us))
     esz = 2 if w.dtype == wl.BF16 else 4
     rows = int(L.sum().item())
-    alg = rows * V * esz + B * min(V, 16384) * esz  # the verified rows, plus the drawn row's segment
+    # the verified rows, plus the drawn row's segment (exact: its 1024-entry chunk)
+    alg = rows * V * esz + B * min(V, 1024 if exact else 16384) * esz
     peak, peak_kind = _peaks()
-    return {"metric": "sampled verify launches/s (point-mass drafts)", "value": round(1e6 / mean_us, 2),
+    name = "exact sampled verify launches/s (fixed-point weights)" if exact else \
+        "sampled verify launches/s (point-mass drafts)"
+    kern = "k_sample_fx (verify_sample_exact)" if exact else "k_sample (verify_sample)"
+    return {"metric": name, "value": round(1e6 / mean_us, 2),
             "unit": "launches/s", "n_gpus": world, "steps": K, "warmup": W, "us_per_launch": round(mean_us, 3),
             "higher_is_better": True, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}", "batch": B, "vocab": V,
                        "temperature": 0.3, "block": "16 for copy-heavy requests, 8 for chat-like",
                        "l2": "every launch reads its own pre-generated logits (larger than L2)"},
-            "roofline": {"bound": "hbm", "kernel": "k_sample (verify_sample)", "achieved": round(alg / mean_us / 1e3, 1),
+            "roofline": {"bound": "hbm", "kernel": kern, "achieved": round(alg / mean_us / 1e3, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(alg / mean_us / 1e3 / peak, 4),
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
             "exp_per_launch": rows * V, "tokens_per_request_launch": round(emitted.sum().item() / (B * K), 4),
@@ -871,6 +882,8 @@ def main(argv=None):
                     help="verify by sampling (point-mass drafts) at temperature T instead of greedily")
     ap.add_argument("--sample-verify", action="store_true",
                     help="time the sampling verification (point-mass drafts) on --config's shapes, one JSON line")
+    ap.add_argument("--exact", action="store_true",
+                    help="with --sample-verify: time the exact sampler (fixed-point weights) instead")
     ap.add_argument("--sweep", action="store_true",
                     help="block-size and sticky variants of the measured step on --config, one JSON line")
     ap.add_argument("--ablation-sweep", action="store_true",

@@ -109,6 +109,9 @@ _SIGS = [
     ("clk_verify_sample_scratch_bytes", ctypes.c_int, [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     ("clk_verify_sample", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
+    ("clk_verify_sample_exact_scratch_bytes", ctypes.c_int, [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
+    ("clk_verify_sample_exact", ctypes.c_int, [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               ctypes.c_size_t, _P]),
     ("clk_verify_sample_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                                 _P, _P, _P, ctypes.c_size_t, _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
@@ -404,6 +407,33 @@ def verify_sample(logits, block, length, inv_temp, uniform, accept, emitted, out
                                    _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
                                    _ptr(out_tok, shape=(B, BLOCK)), _ptr(scratch, torch.uint8, name="scratch"),
                                    scratch.numel(), _stream(stream)))
+
+
+def verify_sample_exact_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zeroed scratch buffer for verify_sample_exact with vocabulary V and
+    up to B requests."""
+    dt = BF16 if logits_dtype == torch.bfloat16 else F32
+    n = ctypes.c_size_t()
+    _check("clk_verify_sample_exact_scratch_bytes",
+           lib().clk_verify_sample_exact_scratch_bytes(dt, V, B, ctypes.byref(n)))
+    t = torch.empty(n.value, dtype=torch.uint8, device=device)
+    _check("clk_verify_scratch_init", lib().clk_verify_scratch_init(t.data_ptr(), t.numel(), _stream(stream)))
+    return t
+
+
+def verify_sample_exact(logits, block, length, inv_temp, uniform, accept, emitted, out_tok, scratch, stream=None):
+    """Sampling verification on the fixed-point weights
+    (clk_verify_sample_exact): the rule of verify_sample with every decision
+    an integer comparison."""
+    dt, rs, qs, V = _logits_args(logits)
+    B = block.shape[0]
+    _check("clk_verify_sample_exact",
+           lib().clk_verify_sample_exact(logits.data_ptr(), dt, rs, qs, V, B, _ptr(block, shape=(B, BLOCK)),
+                                         _ptr(length, shape=(B,)), _ptr(inv_temp, torch.float32, (B,), "inv_temp"),
+                                         _ptr(uniform, torch.float32, (B, BLOCK, 2), "uniform"),
+                                         _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
+                                         _ptr(out_tok, shape=(B, BLOCK)), _ptr(scratch, torch.uint8, name="scratch"),
+                                         scratch.numel(), _stream(stream)))
 
 
 def verify_sample_append(h: Lookup, slots, logits, block, length, inv_temp, uniform, accept, emitted, out_tok,

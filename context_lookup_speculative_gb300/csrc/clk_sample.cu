@@ -920,6 +920,550 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(Samp
     }
 }
 
+// ---------------------------------------------------------------------------
+// Exact sampling (clk_verify_sample_exact): the same rule on weights defined
+// as integers, so that every acceptance and every draw is an integer
+// comparison and the result is a fixed function of the logits, uniforms and
+// drafts (where floating point decides an integer, the precision is part of
+// the definition: float32 with fused multiply-adds, then integers).
+//
+// s = fl32(t * fl32(log2 e)).  A row is cut into chunks of kFxChunk entries;
+// chunk k's reference is R_k = ceil(fl32(M_k * s)), M_k its largest entry.
+// Entry x of chunk k weighs q = Q(d), d = fma(x, s, -R_k): for d >= -32,
+// with n = rint(d) and r = d - n, f = P(r) is the degree-6 Taylor polynomial
+// of 2^(r + 1/2) (coefficients sqrt(2) (ln 2)^j / j! rounded to float,
+// Horner's rule with fused multiply-adds), a float in [1, 2], and
+// q = floor(64 (bits(f) - bits(0.5f)) / 2^-n + 1/2), about 2^(d + 29.5);
+// below -32, q = 0.  The chunk keeps S_k = sum of its q (exact) and R_k.
+// Row units are 2^-12 of a unit of the row's reference R = max_k R_k: a
+// chunk quantity v is U(v, e) = v 2^(12 - e), floored, with e = R - R_k, and
+// the row's total is T = sum_k U(S_k, e_k).  A draft c in chunk kc (weight
+// q_c) is accepted iff floor(k(u) T / 2^24) < U(q_c, e_kc), with
+// k(u) = floor(u 2^24) clamped to [0, 2^24 - 1].  The draw takes
+// t = floor(k(u) T' / 2^24) of the chunk totals with c's weight removed from
+// its chunk, finds the chunk whose running total passes t and, inside it,
+// the entry whose running sum of q passes the remainder taken back to chunk
+// units.
+//
+// The streaming pass: each warp takes whole chunks of its CTA's share (the
+// flat (request, row, chunk) list), one load per vector of the chunk, then a
+// warp maximum, the weights in packed f32x2 arithmetic and a warp sum; one
+// 64-bit record per chunk, (S_k << 24) | (R_k mod 2^24).  The CTA that
+// completes a request's count finishes it: rows' totals from the records,
+// all drafts at once, the chunk of the draw, the entry inside it.
+// ---------------------------------------------------------------------------
+constexpr int32_t kFxChunk = 1024;                  // entries per chunk
+constexpr int32_t kFxNoRef = -(1 << 23);             // a chunk of -inf only
+constexpr unsigned long long kFxBad = ~0ull;         // a chunk that cannot be weighed
+constexpr float kFxZMax = 4194304.0f;                // 2^22: largest |M_k * s|
+constexpr float kFxMagic = 12582912.0f;              // 1.5 * 2^23: d + magic rounds d to an integer
+constexpr int32_t kFxGuard = 12;                     // row units: 2^-12 of a unit of the row's reference
+constexpr int32_t kFxVMax = 4194304;                 // longest row (4096 chunks: T stays below 2^64)
+constexpr int kFxCtas = 4;                           // resident CTAs per SM the kernel is compiled for
+
+// The weight polynomial's coefficients, packed twice for f32x2 arithmetic.
+struct FxPoly {
+    unsigned long long c2[7];
+    float c[7];
+};
+
+__device__ __forceinline__ int32_t fx_ref(unsigned long long rec)
+{
+    return (int32_t)((uint32_t)rec << 8) >> 8;  // the low 24 bits, sign-extended
+}
+__device__ __forceinline__ unsigned long long fx_sum(unsigned long long rec) { return rec >> 24; }
+// U(v, e): a chunk quantity in row units, e = R - R_k >= 0.
+__device__ __forceinline__ unsigned long long fx_rowunits(unsigned long long v, int32_t e)
+{
+    if (e <= kFxGuard) return v << (kFxGuard - e);
+    return e - kFxGuard >= 64 ? 0ull : v >> (e - kFxGuard);
+}
+// A row-unit remainder back in chunk units.
+__device__ __forceinline__ unsigned long long fx_chunkunits(unsigned long long v, int32_t e)
+{
+    return e >= kFxGuard ? v << (e - kFxGuard) : v >> (kFxGuard - e);
+}
+// floor(k v / 2^24) for k < 2^24 and v < 2^62 (exact, in 64-bit parts).
+__device__ __forceinline__ unsigned long long fx_mulshift(uint32_t k, unsigned long long v)
+{
+    return (unsigned long long)k * (v >> 24) + (((unsigned long long)k * (v & 0xFFFFFFull)) >> 24);
+}
+__device__ __forceinline__ uint32_t fx_unit(float u)
+{
+    const float v = u * 16777216.0f;
+    if (!(v > 0.0f)) return 0u;
+    if (v >= 16777215.0f) return 16777215u;
+    return (uint32_t)v;
+}
+
+// q from f = P(r) and t = fl32(d + magic) = magic + n: v = floor(128 (bits(f)
+// - bits(0.5f)) / 2^-n), -n = bits(magic) - bits(t), then q = (v + 1) / 2
+// rounded down, i.e. v - v / 2.  For d below -2^22, -inf or NaN, t is no
+// longer magic + n but the shift amount, read unsigned, is 32 or more, and
+// the clamped funnel shift of (0:lo) gives 0.  q <= 2^29.75 + 1, so four
+// weights add up below 2^32.
+__device__ __forceinline__ uint32_t fx_q_bits(float f, float t)
+{
+    const uint32_t lo = __float_as_uint(f) * 128u + 0x80000000u;
+    const uint32_t sh = 0x4B400000u - __float_as_uint(t);
+    uint32_t v;
+    asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(lo), "r"(0u), "r"(sh));
+    return v - (v >> 1);
+}
+
+// The weight of one entry against its chunk's reference R.
+__device__ __forceinline__ uint32_t fx_q1(float x, float s, int32_t R, const FxPoly& P)
+{
+    const float d = fmaf(x, s, -(float)R);
+    const float t = __fadd_rn(d, kFxMagic);
+    const float nf = __fadd_rn(t, -kFxMagic);
+    const float r = __fadd_rn(d, -nf);
+    float f = P.c[6];
+#pragma unroll
+    for (int j = 5; j >= 0; --j) f = fmaf(f, r, P.c[j]);
+    return fx_q_bits(f, t);
+}
+
+// The weights of two entries (packed) against -R (packed in nR2).
+__device__ __forceinline__ uint32_t fx_q2(unsigned long long x2, unsigned long long s2, unsigned long long nR2,
+                                          const FxPoly& P)
+{
+    const unsigned long long d = fma2(x2, s2, nR2);
+    const unsigned long long t = add2(d, pk(kFxMagic, kFxMagic));
+    const unsigned long long nf = add2(t, pk(-kFxMagic, -kFxMagic));
+    const unsigned long long r = fma2(nf, pk(-1.0f, -1.0f), d);  // d - nf, one rounding
+    unsigned long long f = P.c2[6];
+#pragma unroll
+    for (int j = 5; j >= 0; --j) f = fma2(f, r, P.c2[j]);
+    float f0, f1, t0, t1;
+    pk_split(f, f0, f1);
+    pk_split(t, t0, t1);
+    return fx_q_bits(f0, t0) + fx_q_bits(f1, t1);
+}
+
+// Order-preserving int of a float (not NaN), for the warp maximum.
+__device__ __forceinline__ int32_t fx_key(float x)
+{
+    const int32_t i = __float_as_int(x);
+    return i ^ ((i >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float fx_warp_max(float x)
+{
+    const int32_t k = __reduce_max_sync(0xFFFFFFFFu, fx_key(x));
+    return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF));
+}
+// Sum over the warp of lane values below 2^48, exact, in 16-bit parts.
+__device__ __forceinline__ unsigned long long fx_warp_sum(unsigned long long v)
+{
+    const uint32_t a = __reduce_add_sync(0xFFFFFFFFu, (uint32_t)v & 0xFFFFu);
+    const uint32_t b = __reduce_add_sync(0xFFFFFFFFu, (uint32_t)(v >> 16) & 0xFFFFu);
+    const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, (uint32_t)(v >> 32) & 0xFFFFu);
+    return ((unsigned long long)c << 32) + ((unsigned long long)b << 16) + a;
+}
+
+template <int DT>
+struct FxVec;
+template <>
+struct FxVec<CLK_DTYPE_BF16> {
+    __device__ static uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+    // the 8 weights of one vector, in pairs, then two sums of four
+    __device__ static unsigned long long weights(const uint4& v, unsigned long long s2, unsigned long long nR2,
+                                                 const FxPoly& P)
+    {
+        const uint32_t a = fx_q2(pk(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)), s2, nR2, P) +
+                           fx_q2(pk(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)), s2, nR2, P);
+        const uint32_t b = fx_q2(pk(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)), s2, nR2, P) +
+                           fx_q2(pk(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)), s2, nR2, P);
+        return (unsigned long long)a + b;
+    }
+};
+template <>
+struct FxVec<CLK_DTYPE_F32> {
+    __device__ static uint4 neg_inf() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+    __device__ static unsigned long long weights(const uint4& v, unsigned long long s2, unsigned long long nR2,
+                                                 const FxPoly& P)
+    {
+        return fx_q2(pk(__uint_as_float(v.x), __uint_as_float(v.y)), s2, nR2, P) +
+               fx_q2(pk(__uint_as_float(v.z), __uint_as_float(v.w)), s2, nR2, P);
+    }
+};
+
+// The record of a chunk from its maximum (warp-uniform) and its weights.
+__device__ __forceinline__ unsigned long long fx_record(unsigned long long S, int32_t R)
+{
+    return (S << 24) | ((uint32_t)R & 0xFFFFFFu);
+}
+
+// Streams chunks [k0, k1) of request b (flat chunk k is chunk k % NC of the
+// request's row k / NC - P[b]): warp w takes chunks k0 + w, k0 + w + 8, ...
+// Every lane holds 32 entries of its chunk (vector path: vectors lane + 32 u);
+// weights are added in 32 bits four at a time, then in 64 bits.
+template <int DT, bool VEC>
+__device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k0, int64_t k1,
+                                          const FxPoly& poly, unsigned long long* rec)
+{
+    using E = SElem<DT>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t NC = a.S;
+    const float s = a.inv_temp[b] * kLog2e;
+    const unsigned long long s2 = pk(s, s);
+    const typename E::T* req = static_cast<const typename E::T*>(a.logits) + (int64_t)b * a.req_stride;
+    for (int64_t k = k0 + warp; k < k1; k += kSWarpsPerCta) {
+        const int64_t ri = k / NC;
+        const int32_t ck = (int32_t)(k - ri * NC);
+        const int32_t r = (int32_t)(ri - P[b]);
+        const typename E::T* row = req + (int64_t)r * a.row_stride;
+        const int32_t e0 = ck * kFxChunk, n = min(kFxChunk, a.V - e0);  // entries of this chunk
+        unsigned long long out;
+        if (VEC) {
+            constexpr int NV = kFxChunk / (E::W * 32);  // vectors per lane
+            const uint4* rv = reinterpret_cast<const uint4*>(row + e0);
+            const int32_t nvec = n / E::W;
+            uint4 X[NV];
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int32_t vi = lane + 32 * u;
+                X[u] = vi < nvec ? __ldcs(rv + vi) : FxVec<DT>::neg_inf();
+            }
+            float mx = E::vmax(X[0]);
+#pragma unroll
+            for (int u = 1; u < NV; ++u) mx = fmaxf(mx, E::vmax(X[u]));
+            mx = fx_warp_max(mx);
+            if (mx == -INFINITY) {
+                out = fx_record(0ull, kFxNoRef);
+            } else {
+                const float y = mx * s;
+                if (!(fabsf(y) <= kFxZMax)) {
+                    out = kFxBad;
+                } else {
+                    const float R = ceilf(y);
+                    const unsigned long long nR2 = pk(-R, -R);
+                    unsigned long long sum = 0ull;
+#pragma unroll
+                    for (int u = 0; u < NV; ++u) sum += FxVec<DT>::weights(X[u], s2, nR2, poly);
+                    out = fx_record(fx_warp_sum(sum), (int32_t)R);
+                }
+            }
+        } else {
+            float x[32];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int32_t v = lane + 32 * i;
+                x[i] = v < n ? E::value(row[e0 + v]) : -INFINITY;
+                mx = fmaxf(mx, x[i]);
+            }
+            mx = fx_warp_max(mx);
+            if (mx == -INFINITY) {
+                out = fx_record(0ull, kFxNoRef);
+            } else {
+                const float y = mx * s;
+                if (!(fabsf(y) <= kFxZMax)) {
+                    out = kFxBad;
+                } else {
+                    const int32_t R = (int32_t)ceilf(y);
+                    unsigned long long sum = 0ull;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        sum += fx_q1(x[i], s, R, poly) + fx_q1(x[i + 1], s, R, poly) + fx_q1(x[i + 2], s, R, poly) +
+                               fx_q1(x[i + 3], s, R, poly);
+                    out = fx_record(fx_warp_sum(sum), R);
+                }
+            }
+        }
+        if (lane == 0) rec[((int64_t)b * kBlock + r) * NC + ck] = out;
+    }
+}
+
+struct FxFinSmem {
+    int32_t R[kBlock];             // each row's reference (largest chunk reference)
+    unsigned long long T[kBlock];  // each row's total in row units
+    int32_t rbad[kBlock];          // the row cannot be weighed
+    unsigned long long qx;         // the removed draft's weight in its chunk
+    unsigned long long tc;         // the draw's target inside its chunk
+    unsigned long long wsum[kSWarpsPerCta];
+    int32_t a, excl, kstar, tok;
+};
+
+// Request b is complete: decide the drafts, draw the token, write the
+// outputs, rewind the counter.  Block-wide.
+template <int DT>
+__device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long long* rec, int32_t b, FxFinSmem& fs,
+                                       const FxPoly& poly)
+{
+    using E = SElem<DT>;
+    const unsigned full = 0xFFFFFFFFu;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t L = a.len[b], NC = a.S, V = a.V;
+    const float s = a.inv_temp[b] * kLog2e;
+    const typename E::T* base = static_cast<const typename E::T*>(a.logits) + (int64_t)b * a.req_stride;
+    const unsigned long long* rb = rec + (int64_t)b * kBlock * NC;
+    __threadfence();
+    // Each row's reference and total: 16 threads per row (row = tid / 16),
+    // each taking the row's chunks sub, sub + 16, ..., then a butterfly over
+    // the 16 (the same result in all of them).
+    {
+        const int32_t r = tid >> 4, sub = tid & 15;
+        int32_t Rm = kFxNoRef, bad = 0;
+        if (r < L) {
+            for (int32_t k = sub; k < NC; k += 16) {
+                const unsigned long long q = __ldcg(rb + (int64_t)r * NC + k);
+                if (q == kFxBad) bad = 1;
+                else Rm = max(Rm, fx_ref(q));
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            Rm = max(Rm, __shfl_xor_sync(full, Rm, o));
+            bad |= __shfl_xor_sync(full, bad, o);
+        }
+        unsigned long long T = 0ull;
+        if (r < L && !bad) {
+            for (int32_t k = sub; k < NC; k += 16) {
+                const unsigned long long q = __ldcg(rb + (int64_t)r * NC + k);
+                T += fx_rowunits(fx_sum(q), Rm - fx_ref(q));
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) T += __shfl_xor_sync(full, T, o);
+        if (sub == 0 && r < L) {
+            fs.R[r] = Rm;
+            fs.T[r] = T;
+            fs.rbad[r] = bad || Rm == kFxNoRef;
+        }
+    }
+    __syncthreads();
+    int32_t bad = 0;
+    for (int32_t r = 0; r < L; ++r) bad |= fs.rbad[r];
+    if (bad) {  // some row cannot be weighed: the empty result
+        if (tid < kBlock) a.out_tok[(int64_t)b * kBlock + tid] = CLK_SENT;
+        if (tid == 0) {
+            a.accept[b] = 0;
+            a.emitted[b] = 0;
+            a.done[b] = 0u;
+        }
+        __syncthreads();
+        return;
+    }
+    // Every draft at once (lane r: row r's draft blk[r + 1]).
+    if (warp == 0) {
+        const bool has = lane < L - 1;
+        const int32_t c = has ? a.block[(int64_t)b * kBlock + lane + 1] : CLK_SENT;
+        const bool inv = c >= 0 && c < V;
+        bool acc = false;
+        unsigned long long qc = 0ull;
+        if (has && inv) {
+            const int32_t Rk = fx_ref(__ldcg(rb + (int64_t)lane * NC + c / kFxChunk));
+            qc = fx_q1(E::value(base[(int64_t)lane * a.row_stride + c]), s, Rk, poly);
+            const unsigned long long w = fx_rowunits(qc, fs.R[lane] - Rk);
+            acc = fx_mulshift(fx_unit(a.uniform[((int64_t)b * kBlock + lane) * 2]), fs.T[lane]) < w;
+        }
+        const unsigned rej = __ballot_sync(full, has && !acc);
+        const int32_t an = rej ? __ffs(rej) - 1 : L - 1;
+        if (lane == an) {
+            fs.a = an;
+            fs.excl = (has && inv) ? c : -1;
+            fs.qx = qc;
+            fs.tok = CLK_SENT;
+        }
+    }
+    __syncthreads();
+    const int32_t ra = fs.a, excl = fs.excl;
+    const unsigned long long* rr = rb + (int64_t)ra * NC;
+    // The chunk of the draw: the chunks' totals with the removed draft taken
+    // out of its chunk, summed once for T' and again, in order, to find the
+    // chunk whose running sum passes t = floor(k(u) T' / 2^24).
+    if (warp == 0) {
+        const int32_t Rr = fs.R[ra];
+        const int32_t kx = excl >= 0 ? excl / kFxChunk : -1;
+        const unsigned long long qx = fs.qx;
+        auto tk = [&](int32_t k) -> unsigned long long {
+            if (k >= NC) return 0ull;
+            const unsigned long long q = __ldcg(rr + k);
+            return fx_rowunits(fx_sum(q) - (k == kx ? qx : 0ull), Rr - fx_ref(q));
+        };
+        unsigned long long total = 0ull;
+        for (int32_t k0 = 0; k0 < NC; k0 += 32) {
+            unsigned long long w = tk(k0 + lane);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(full, w, o);
+            total += w;
+        }
+        const unsigned long long t = fx_mulshift(fx_unit(a.uniform[((int64_t)b * kBlock + ra) * 2 + 1]), total);
+        unsigned long long carry = 0ull, before = 0ull;
+        int32_t found = -1;
+        for (int32_t k0 = 0; k0 < NC && found < 0; k0 += 32) {
+            const int32_t k = k0 + lane;
+            const unsigned long long w = tk(k);
+            unsigned long long incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(full, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned cross = __ballot_sync(full, k < NC && carry + incl > t);
+            if (cross) {
+                const int32_t l = __ffs(cross) - 1;
+                found = k0 + l;
+                before = carry + __shfl_sync(full, incl - w, l);
+            }
+            carry += __shfl_sync(full, incl, 31);
+        }
+        if (lane == 0) {
+            fs.kstar = found;
+            if (found >= 0) fs.tc = fx_chunkunits(t - before, Rr - fx_ref(__ldcg(rr + found)));
+        }
+    }
+    __syncthreads();
+    // Inside the chunk: 4 consecutive entries per thread, a block-wide
+    // exclusive scan of their sums, and the thread whose run holds the target
+    // walks its 4 (c skipped: weight 0).
+    const int32_t ks = fs.kstar;
+    if (ks >= 0) {
+        const int32_t Rk = fx_ref(__ldcg(rr + ks));
+        const typename E::T* row = base + (int64_t)ra * a.row_stride;
+        const int64_t v0 = (int64_t)ks * kFxChunk + 4 * tid;
+        uint32_t q[4], own = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t v = v0 + i;
+            q[i] = (v < V && v != excl) ? fx_q1(E::value(row[v]), s, Rk, poly) : 0u;
+            own += q[i];
+        }
+        unsigned long long incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) fs.wsum[warp] = incl;
+        __syncthreads();
+        unsigned long long pre = incl - own;
+        for (int w = 0; w < warp; ++w) pre += fs.wsum[w];
+        const unsigned long long tc = fs.tc;
+        if (pre <= tc && tc < pre + own) {  // one thread: the runs partition [0, chunk total)
+            unsigned long long run = pre;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                run += q[i];
+                if (run > tc) {
+                    fs.tok = (int32_t)(v0 + i);
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < kBlock) {
+        const int32_t r = tid;
+        a.out_tok[(int64_t)b * kBlock + r] =
+            r < ra ? a.block[(int64_t)b * kBlock + r + 1] : (r == ra ? fs.tok : CLK_SENT);
+    }
+    if (tid == 0) {
+        a.accept[b] = ra;
+        a.emitted[b] = ra + 1;
+        a.done[b] = 0u;
+    }
+    __syncthreads();
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSThreads, kFxCtas) k_sample_fx(SampleArgs a, FxPoly poly)
+{
+    extern __shared__ int32_t P[];  // B + 1
+    __shared__ int32_t sm_warp[kSWarpsPerCta];
+    __shared__ int32_t sm_last;
+    __shared__ FxFinSmem fs;
+    const int tid = threadIdx.x;
+    const int32_t B = a.B;
+    unsigned long long* rec = reinterpret_cast<unsigned long long*>(a.part);
+    sample_prefix(a, P, sm_warp);
+    // Requests with no rows (invalid length or temperature): empty result.
+    if (blockIdx.x == 0) {
+        for (int32_t b = tid; b < B; b += kSThreads) {
+            if (sample_rows(a, b) != 0) continue;
+            for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
+            a.accept[b] = 0;
+            a.emitted[b] = 0;
+        }
+    }
+    const int64_t NC = a.S;
+    const int64_t N = (int64_t)P[B] * NC;
+    const int64_t lo = N * blockIdx.x / gridDim.x;
+    const int64_t hi = N * (blockIdx.x + 1) / gridDim.x;
+    int64_t k = lo;
+    while (k < hi) {
+        const int32_t b = sample_owner(P, B, k / NC);
+        const int64_t k1 = min(hi, (int64_t)P[b + 1] * NC);
+        fx_stream<DT, VEC>(a, P, b, k, k1, poly, rec);
+        __syncthreads();  // every warp's records are stored
+        if (tid == 0) {
+            __threadfence();
+            const uint32_t n = (uint32_t)(k1 - k);
+            const uint32_t need = (uint32_t)(P[b + 1] - P[b]) * (uint32_t)NC;
+            sm_last = atomicAdd(a.done + b, n) + n == need;
+        }
+        __syncthreads();
+        if (sm_last) fx_finish<DT>(a, rec, b, fs, poly);
+        k = k1;
+    }
+}
+
+int fx_sizes(int32_t dtype, int32_t V, int32_t B, int32_t* NC, size_t* bytes)
+{
+    if ((dtype != CLK_DTYPE_BF16 && dtype != CLK_DTYPE_F32) || V < 1 || V > kFxVMax || B < 0 || B > CLK_MAX_BATCH)
+        return CLK_EINVAL;
+    const int64_t nc = ((int64_t)V + kFxChunk - 1) / kFxChunk;
+    *NC = (int32_t)nc;
+    const size_t nb = (size_t)(B > 0 ? B : 1);
+    *bytes = align_up(nb * sizeof(uint32_t), 16) + nb * kBlock * (size_t)nc * sizeof(unsigned long long);
+    return CLK_OK;
+}
+
+// c_j = sqrt(2) (ln 2)^j / j! rounded to float, from the recurrence
+// t_0 = sqrt(2), t_{j+1} = t_j ln2 / (j + 1) in double.
+FxPoly fx_poly()
+{
+    FxPoly p;
+    double t = 1.4142135623730951;
+    const double ln2 = 0.6931471805599453;
+    for (int j = 0; j < 7; ++j) {
+        p.c[j] = (float)t;
+        uint32_t bits;
+        memcpy(&bits, &p.c[j], sizeof bits);
+        p.c2[j] = ((unsigned long long)bits << 32) | bits;
+        t = t * ln2 / (double)(j + 1);
+    }
+    return p;
+}
+
+template <int DT, bool VEC>
+int launch_fx(const SampleArgs& a, cudaStream_t s)
+{
+    static std::atomic<int> cache[64];  // resident CTAs per SM, per device (calls from any host thread)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
+    const size_t smem = (size_t)(a.B + 1) * sizeof(int32_t);
+    auto kern = k_sample_fx<DT, VEC>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CLK_ECUDA;
+    int occ = (dev >= 0 && dev < 64 && smem <= 4096) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (occ <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSThreads, smem <= 4096 ? 4096 : smem) !=
+                cudaSuccess ||
+            occ < 1)
+            return CLK_ECUDA;
+        if (dev >= 0 && dev < 64 && smem <= 4096) cache[dev].store(occ, std::memory_order_relaxed);
+    }
+    const int sms = num_sms();
+    if (sms <= 0) return CLK_ECUDA;
+    const int64_t chunks = (int64_t)a.B * kBlock * a.S;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)occ * sms, chunks));
+    kern<<<(unsigned)grid, kSThreads, smem, s>>>(a, fx_poly());
+    return launch_status();
+}
+
 int sample_sizes(int32_t dtype, int32_t V, int32_t B, int32_t* S, size_t* bytes)
 {
     if ((dtype != CLK_DTYPE_BF16 && dtype != CLK_DTYPE_F32) || V < 1 || B < 0 || B > CLK_MAX_BATCH)
@@ -992,17 +1536,25 @@ extern "C" int clk_verify_sample_scratch_bytes(int32_t dtype, int32_t V, int32_t
     return sample_sizes(dtype, V, B, &S, bytes);
 }
 
+extern "C" int clk_verify_sample_exact_scratch_bytes(int32_t dtype, int32_t V, int32_t B, size_t* bytes)
+{
+    if (bytes == nullptr) return CLK_EINVAL;
+    int32_t NC = 0;
+    return fx_sizes(dtype, V, B, &NC, bytes);
+}
+
 namespace {
 
 // Checks and launches both entry points; h == nullptr: stateless.
 int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype, int64_t row_stride,
                  int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
                  const int32_t* d_len_hint, const float* d_inv_temp, const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
-                 int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs, bool paired = false)
+                 int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, cudaStream_t cs, bool paired = false,
+                 bool exact = false)
 {
     int32_t S = 0;
     size_t need = 0;
-    int rc = sample_sizes(dtype, V, B, &S, &need);
+    int rc = exact ? fx_sizes(dtype, V, B, &S, &need) : sample_sizes(dtype, V, B, &S, &need);
     if (rc != CLK_OK) return rc;
     if (h != nullptr) {
         rc = check_batch(h, B);
@@ -1043,6 +1595,10 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
     const bool bf = dtype == CLK_DTYPE_BF16;
+    if (exact) {  // stateless only
+        if (bf) return vec ? launch_fx<CLK_DTYPE_BF16, true>(a, cs) : launch_fx<CLK_DTYPE_BF16, false>(a, cs);
+        return vec ? launch_fx<CLK_DTYPE_F32, true>(a, cs) : launch_fx<CLK_DTYPE_F32, false>(a, cs);
+    }
     if (h != nullptr) {
         const LookupDev& L = h->dev;
         if (bf) return vec ? launch_sample<CLK_DTYPE_BF16, true, true>(a, L, cs)
@@ -1068,6 +1624,17 @@ extern "C" int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t ro
     return sample_entry(nullptr, nullptr, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, nullptr,
                         d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
                         (cudaStream_t)s);
+}
+
+extern "C" int clk_verify_sample_exact(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                       int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                       const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                       int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                                       clk_stream_t s)
+{
+    return sample_entry(nullptr, nullptr, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, nullptr,
+                        d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes,
+                        (cudaStream_t)s, false, true);
 }
 
 extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,

@@ -382,6 +382,55 @@ CLK_API int clk_verify_sample(const void* d_logits, int32_t dtype, int64_t row_s
                               int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
                               clk_stream_t s);
 
+/* clk_verify_sample with the target's weights defined as integers, so that
+ * every acceptance and every draw is an integer comparison: the results are
+ * a fixed function of the logits, drafts, lengths, temperatures and
+ * uniforms, which another implementation of the same definition reproduces
+ * bit for bit.  The rule (accept iff u_acc < p_r(c), draw from the residual
+ * or the last row, inverse CDF) is clk_verify_sample's; only p_r changes:
+ *
+ *   s = fl32(inv_temp * fl32(log2 e)); each row is cut into chunks of 1024
+ *   entries (the last one ragged).  Chunk k's reference is
+ *   R_k = ceil(fl32(M_k * s)), M_k its largest entry.  An entry x of chunk k
+ *   weighs q = Q(fma(x, s, -R_k)) with, for d >= -32, n = rint(d) (ties to
+ *   even), r = d - n, f = P(r) the degree-6 Taylor polynomial of
+ *   2^(r + 1/2) (coefficients sqrt(2) (ln 2)^j / j! rounded to float,
+ *   evaluated by Horner's rule with fused multiply-adds) and
+ *   Q(d) = floor(64 (bits(f) - bits(0.5f)) / 2^-n + 1/2), about
+ *   2^(d + 29.5); Q(d) = 0 below -32.  S_k = the chunk's sum of q.  Row
+ *   units are 2^-12 of a unit of the row's reference R = max_k R_k: a chunk
+ *   quantity v counts U(v, e) = floor(v * 2^(12 - e)), e = R - R_k, and the
+ *   row's total is T = sum_k U(S_k, e_k).
+ *   A draft c in chunk kc is accepted iff floor(k(u_acc) T / 2^24) <
+ *   U(q_c, e_kc), with k(u) = floor(u * 2^24) clamped to [0, 2^24 - 1].
+ *   The draw with u_smp takes t = floor(k(u_smp) T' / 2^24), T' the sum of
+ *   the chunks' totals with c's weight taken out of its chunk (nothing taken
+ *   out after a full acceptance or a sentinel draft); the chunk is the
+ *   first whose running total exceeds t, and the token the first entry of
+ *   it (c skipped) whose running sum of q exceeds the remainder of t taken
+ *   back to chunk units (times 2^(e - 12), rounded down).
+ *
+ * p_r differs from the float softmax by about 2^-22 relative per weight
+ * (the polynomial and float rounding) plus half a unit of each weight;
+ * entries more than about 30 binades below their chunk's largest entry
+ * weigh 0.  A request any of whose L_b rows has a chunk with
+ * |fl32(M_k * s)| > 2^22, or only -inf entries, gets the empty result, as
+ * does an invalid length or temperature.  V is at most 4,194,304
+ * (CLK_EINVAL above).  Logits must be finite or -inf (NaN entries:
+ * unspecified result, no fault).
+ *
+ * Arguments, layouts, outputs and errors are those of clk_verify_sample;
+ * the scratch must hold clk_verify_sample_exact_scratch_bytes(dtype, V, B)
+ * bytes (16-byte aligned, zeroed once before its first use, left ready for
+ * the next call; calls sharing it must not overlap on the GPU).  Every row
+ * is read once, plus one 1024-entry chunk of the drawn row. */
+CLK_API int clk_verify_sample_exact_scratch_bytes(int32_t dtype, int32_t V, int32_t B, size_t* bytes);
+CLK_API int clk_verify_sample_exact(const void* d_logits, int32_t dtype, int64_t row_stride, int64_t req_stride,
+                                    int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                    const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                    int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                                    clk_stream_t s);
+
 /* clk_verify_sample followed by clk_lookup_append of its d_out_tok /
  * d_emitted, in one launch: the sampled step of a decode loop.  Each
  * request's emitted tokens are committed to the history of d_slots[b] as

@@ -55,6 +55,8 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
                     the records' g holds the emitted tokens
     mode "sample_fused": propose_fuse_sched + verify_sample_append (the Step
                     driver's sampled step); g as for "sample"
+    mode "sample_exact": as "sample" with verify_sample_exact (the
+                    fixed-point weights)
     """
     steps = w.steps if steps is None else steps
     params = params or clk.Params.default()
@@ -70,10 +72,13 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     rec = {n: torch.zeros((steps, B), **i32) for n in ("k", "j", "L", "a", "e")}
     rec.update({n: torch.zeros((steps, B, clk.BLOCK), **i32) for n in ("c", "blk", "g")})
     scratch = clk.verify_scratch(B, device=device) if mode == "unfused" else None
-    if mode in ("sample", "sample_fused"):
+    if mode in ("sample", "sample_fused", "sample_exact"):
         if not inv_temp > 0:
             raise ValueError("mode 'sample' needs inv_temp > 0")
-        sscratch = clk.verify_sample_scratch(logits.dtype, w.V, B, device=device)
+        if mode == "sample_exact":
+            sscratch = clk.verify_sample_exact_scratch(logits.dtype, w.V, B, device=device)
+        else:
+            sscratch = clk.verify_sample_scratch(logits.dtype, w.V, B, device=device)
         uni = torch.zeros((B, clk.BLOCK, 2), dtype=torch.float32, device=device)
         temps = torch.full((B,), float(inv_temp), dtype=torch.float32, device=device)
     last_tok = torch.from_numpy(np.array([p[-1] for p in w.prompts], dtype=np.int32)).to(device)
@@ -85,7 +90,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
         elif mode == "semi":
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
             clk.fuse_sched(lk, slots, st.draft, st.k, head, st.accept, st.length, st.length, st.block)
-        elif mode in ("unfused", "sample"):
+        elif mode in ("unfused", "sample", "sample_exact"):
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
             clk.sched_step(lk, slots, st.k, st.accept, st.length, st.length)
             clk.fuse(params, last_tok, st.draft, st.k, head, st.length, st.block)
@@ -96,9 +101,10 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
             clk.verify_greedy(logits, st.block, st.length, st.argmax, st.accept, st.emitted, st.out_tok, scratch)
             clk.lookup_append(lk, slots, st.out_tok, st.emitted)
             last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
-        elif mode == "sample":
+        elif mode in ("sample", "sample_exact"):
             gen.uniforms(t, uni)
-            clk.verify_sample(logits, st.block, st.length, temps, uni, st.accept, st.emitted, st.out_tok, sscratch)
+            verify = clk.verify_sample_exact if mode == "sample_exact" else clk.verify_sample
+            verify(logits, st.block, st.length, temps, uni, st.accept, st.emitted, st.out_tok, sscratch)
             clk.lookup_append(lk, slots, st.out_tok, st.emitted)
             last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
             st.argmax.copy_(st.out_tok)  # recorded as g
