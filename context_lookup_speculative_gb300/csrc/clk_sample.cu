@@ -959,7 +959,10 @@ constexpr float kFxZMax = 4194304.0f;                // 2^22: largest |M_k * s|
 constexpr float kFxMagic = 12582912.0f;              // 1.5 * 2^23: d + magic rounds d to an integer
 constexpr int32_t kFxGuard = 12;                     // row units: 2^-12 of a unit of the row's reference
 constexpr int32_t kFxVMax = 4194304;                 // longest row (4096 chunks: T stays below 2^64)
-constexpr int kFxCtas = 4;                           // resident CTAs per SM the kernel is compiled for
+#ifndef CLK_FX_CTAS
+#define CLK_FX_CTAS 4  // resident CTAs per SM the exact sampler is compiled for
+#endif
+constexpr int kFxCtas = CLK_FX_CTAS;
 
 // The weight polynomial's coefficients, packed twice for f32x2 arithmetic.
 struct FxPoly {
