@@ -1178,6 +1178,45 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
     }
 }
 
+// Block-wide sum of v (every thread gets it); sm holds one value per warp.
+__device__ __forceinline__ unsigned long long fx_block_sum(unsigned long long v, unsigned long long* sm)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0) sm[warp] = v;
+    __syncthreads();
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int w = 0; w < kSWarpsPerCta; ++w) s += sm[w];
+    __syncthreads();
+    return s;
+}
+
+// Block-wide inclusive scan of v in thread order; total receives the sum.
+__device__ __forceinline__ unsigned long long fx_block_scan(unsigned long long v, unsigned long long* sm,
+                                                            unsigned long long& total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm[warp] = incl;
+    __syncthreads();
+    unsigned long long pre = 0ull, tot = 0ull;
+#pragma unroll
+    for (int w = 0; w < kSWarpsPerCta; ++w) {
+        if (w < warp) pre += sm[w];
+        tot += sm[w];
+    }
+    __syncthreads();
+    total = tot;
+    return pre + incl;
+}
+
 struct FxFinSmem {
     int32_t R[kBlock];             // each row's reference (largest chunk reference)
     unsigned long long T[kBlock];  // each row's total in row units
@@ -1209,6 +1248,7 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
         const int32_t r = tid >> 4, sub = tid & 15;
         int32_t Rm = kFxNoRef, bad = 0;
         if (r < L) {
+#pragma unroll 8
             for (int32_t k = sub; k < NC; k += 16) {
                 const unsigned long long q = __ldcg(rb + (int64_t)r * NC + k);
                 if (q == kFxBad) bad = 1;
@@ -1222,6 +1262,7 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
         }
         unsigned long long T = 0ull;
         if (r < L && !bad) {
+#pragma unroll 8
             for (int32_t k = sub; k < NC; k += 16) {
                 const unsigned long long q = __ldcg(rb + (int64_t)r * NC + k);
                 T += fx_rowunits(fx_sum(q), Rm - fx_ref(q));
@@ -1273,10 +1314,11 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
     __syncthreads();
     const int32_t ra = fs.a, excl = fs.excl;
     const unsigned long long* rr = rb + (int64_t)ra * NC;
-    // The chunk of the draw: the chunks' totals with the removed draft taken
-    // out of its chunk, summed once for T' and again, in order, to find the
-    // chunk whose running sum passes t = floor(k(u) T' / 2^24).
-    if (warp == 0) {
+    // The chunk of the draw, block-wide (thread j takes chunks j, j + 256,
+    // ...): the chunks' totals with the removed draft taken out of its chunk
+    // are summed for T', then scanned 256 chunks at a time to find the one
+    // whose running total passes t = floor(k(u) T' / 2^24).
+    {
         const int32_t Rr = fs.R[ra];
         const int32_t kx = excl >= 0 ? excl / kFxChunk : -1;
         const unsigned long long qx = fs.qx;
@@ -1285,39 +1327,26 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
             const unsigned long long q = __ldcg(rr + k);
             return fx_rowunits(fx_sum(q) - (k == kx ? qx : 0ull), Rr - fx_ref(q));
         };
-        unsigned long long total = 0ull;
-        for (int32_t k0 = 0; k0 < NC; k0 += 32) {
-            unsigned long long w = tk(k0 + lane);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(full, w, o);
-            total += w;
-        }
+        if (tid == 0) fs.kstar = -1;
+        unsigned long long own = 0ull;
+        for (int32_t k = tid; k < NC; k += kSThreads) own += tk(k);
+        const unsigned long long total = fx_block_sum(own, fs.wsum);
         const unsigned long long t = fx_mulshift(fx_unit(a.uniform[((int64_t)b * kBlock + ra) * 2 + 1]), total);
-        unsigned long long carry = 0ull, before = 0ull;
-        int32_t found = -1;
-        for (int32_t k0 = 0; k0 < NC && found < 0; k0 += 32) {
-            const int32_t k = k0 + lane;
+        unsigned long long carry = 0ull;
+        for (int32_t k0 = 0; k0 < NC; k0 += kSThreads) {
+            const int32_t k = k0 + tid;
             const unsigned long long w = tk(k);
-            unsigned long long incl = w;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(full, incl, o);
-                if (lane >= o) incl += y;
+            unsigned long long slab;
+            const unsigned long long incl = carry + fx_block_scan(w, fs.wsum, slab);
+            if (w > 0ull && incl - w <= t && t < incl) {  // one chunk in all: the running totals partition [0, T')
+                fs.kstar = k;
+                fs.tc = fx_chunkunits(t - (incl - w), Rr - fx_ref(__ldcg(rr + k)));
             }
-            const unsigned cross = __ballot_sync(full, k < NC && carry + incl > t);
-            if (cross) {
-                const int32_t l = __ffs(cross) - 1;
-                found = k0 + l;
-                before = carry + __shfl_sync(full, incl - w, l);
-            }
-            carry += __shfl_sync(full, incl, 31);
-        }
-        if (lane == 0) {
-            fs.kstar = found;
-            if (found >= 0) fs.tc = fx_chunkunits(t - before, Rr - fx_ref(__ldcg(rr + found)));
+            carry += slab;
+            __syncthreads();
+            if (fs.kstar >= 0) break;
         }
     }
-    __syncthreads();
     // Inside the chunk: 4 consecutive entries per thread, a block-wide
     // exclusive scan of their sums, and the thread whose run holds the target
     // walks its 4 (c skipped: weight 0).
@@ -1333,16 +1362,8 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
             q[i] = (v < V && v != excl) ? fx_q1(E::value(row[v]), s, Rk, poly) : 0u;
             own += q[i];
         }
-        unsigned long long incl = own;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(full, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) fs.wsum[warp] = incl;
-        __syncthreads();
-        unsigned long long pre = incl - own;
-        for (int w = 0; w < warp; ++w) pre += fs.wsum[w];
+        unsigned long long chunk_total;
+        const unsigned long long pre = fx_block_scan(own, fs.wsum, chunk_total) - own;
         const unsigned long long tc = fs.tc;
         if (pre <= tc && tc < pre + own) {  // one thread: the runs partition [0, chunk total)
             unsigned long long run = pre;
