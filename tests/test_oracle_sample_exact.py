@@ -236,6 +236,9 @@ def test_agrees_with_the_double_precision_sampler():
 
 
 def test_exact_loop_equals_the_sampled_loop_on_a_small_workload():
+    """The whole sampled decode loop on the fixed-point weights equals the
+    double-precision loop on a seeded workload: no decision of these runs
+    lies within the weights' rounding (about 1e-7) of its threshold."""
     import workload as wl
     w = wl.make_small("mixed", seed=76, B=6, V=2048, steps=48)
     for t in (1.0, 2.5):
