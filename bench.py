@@ -196,6 +196,7 @@ def run_ours(args, world, rank, local, dist):
         raise ValueError("--sampling needs a temperature > 0")
     temps = torch.full((B,), 1.0 / temp if temp else 1.0, dtype=torch.float32, device=device)
     uni = torch.zeros((B, 16, 2), dtype=torch.float32, device=device)
+    exact = bool(getattr(args, "exact", False)) and temp is not None  # sampling on the fixed-point weights
 
     def post(t, lg, u=None):
         """The step's verify launch: greedy, or sampled with step t's uniforms."""
@@ -205,7 +206,7 @@ def run_ours(args, world, rank, local, dist):
         if u is None:
             gen.uniforms(t, uni)
             u = uni
-        st.post_sample(lg, temps, u)
+        st.post_sample(lg, temps, u, exact=exact)
 
     def reinit():
         clk.lookup_init(lk, slots, d_ptok, d_poff)
@@ -365,8 +366,8 @@ def run_ours(args, world, rank, local, dist):
     dc = {k: c_after[k] - c_before[k] for k in ("steps", "hits", "long_steps", "drafted", "accepted", "emitted")}
     rows = params.short_len * dc["steps"] + (params.long_len - params.short_len) * dc["long_steps"]
     esz = 2 if w.dtype == wl.BF16 else 4
-    # sampled verification also re-reads one segment of each request's drawn row
-    draw_bytes = B * min(V, 16384) * esz if temp is not None else 0
+    # sampled verification also re-reads one segment (exact: one chunk) of each request's drawn row
+    draw_bytes = B * min(V, 1024 if exact else 16384) * esz if temp is not None else 0
     verify_bytes = rows * V * esz + draw_bytes * K      # logits rows read, all timed steps
     path_bytes = verify_bytes + LOOKUP_BYTES_PER_REQ * B * K
     peak, peak_kind = _peaks()
@@ -376,7 +377,7 @@ def run_ours(args, world, rank, local, dist):
     ratio = _traffic_ratio()
 
     ablation = run_lookup_ablation(lk, slots, w, device) if args.ablation else None
-    e2e = (run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp)
+    e2e = (run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp, exact)
            if (rank == 0 and not args.no_e2e) else None)
     cpu = run_cpu_baseline(args, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -407,7 +408,8 @@ def run_ours(args, world, rank, local, dist):
 
     steps_s = world * K / total_s
     out = {
-        "metric": METRIC if temp is None else METRIC + f", sampled verification at temperature {temp}",
+        "metric": METRIC if temp is None else METRIC + f", sampled verification at temperature {temp}" +
+        (" on the exact (fixed-point) weights" if exact else ""),
         "value": round(steps_s, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(total_s * 1e3 / K, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
@@ -431,7 +433,8 @@ def run_ours(args, world, rank, local, dist):
                  "overlapped_us_per_step": round(total_ms * 1e3 / K, 3),
                  "index_build_ms": round(index_build_ms, 3)},
         "roofline": {"bound": "hbm", "kernel": "k_verify_step (verify_append)" if temp is None else
-                     "k_sample_step (verify_sample_append)",
+                     ("k_sample_step_fx (verify_sample_exact_append)" if exact else
+                      "k_sample_step (verify_sample_append)"),
                      "achieved": round(verify_bytes / total_s / 1e9, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(verify_bytes / total_s / 1e9 / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
@@ -675,7 +678,7 @@ def run_ablation_sweep(args, world, rank, local):
             "data": "synthetic", "rows": rows}
 
 
-def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp=None):
+def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp=None, exact=False):
     """Same metric through the public API with host buffers.  Each step copies
     its head proposals (and, sampled at temperature `temp`, its uniforms) from
     pinned host memory, runs the two launches on the step's logits in pinned
@@ -726,7 +729,7 @@ def run_e2e(args, w, params, d_ptok, d_poff, pos_hist, device, temp=None):
         if temp is None:
             st.post(lg)
         else:
-            st.post_sample(lg, temps, uni)
+            st.post_sample(lg, temps, uni, exact=exact)
 
     def run(staged: bool):
         lk, slots = drive.make_lookup(w, params, device=device)
@@ -800,12 +803,13 @@ def run_cpu_baseline(args, w):
     threads = os.cpu_count() or 1
     temp = getattr(args, "sampling", None)
     inv_temp = 1.0 / temp if temp else 0.0
-    res = oracle.run(w, steps=steps, threads=threads, inv_temp=inv_temp)
+    exact = bool(getattr(args, "exact", False)) and temp is not None
+    res = oracle.run(w, steps=steps, threads=threads, inv_temp=inv_temp, exact=exact)
     used = min(threads, w.B)
     per_thread = res.method_s / used
     # the same steps of every (B/8)-th request on one core, scaled to the whole batch
     sub = list(range(0, w.B, max(1, w.B // 8)))
-    one = oracle.run(w, req_ids=sub, steps=steps, threads=1, inv_temp=inv_temp)
+    one = oracle.run(w, req_ids=sub, steps=steps, threads=1, inv_temp=inv_temp, exact=exact)
     return {"value": round(steps / per_thread, 3), "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"{w.B} requests x first {steps} steps of the same workload; full-scan lookup, copy, "
                       f"scheduler, fusion, argmax over every verified row, accept, append; host generation of "
@@ -883,7 +887,7 @@ def main(argv=None):
     ap.add_argument("--sample-verify", action="store_true",
                     help="time the sampling verification (point-mass drafts) on --config's shapes, one JSON line")
     ap.add_argument("--exact", action="store_true",
-                    help="with --sample-verify: time the exact sampler (fixed-point weights) instead")
+                    help="with --sample-verify or --sampling: the exact sampler (fixed-point weights) instead")
     ap.add_argument("--sweep", action="store_true",
                     help="block-size and sticky variants of the measured step on --config, one JSON line")
     ap.add_argument("--ablation-sweep", action="store_true",

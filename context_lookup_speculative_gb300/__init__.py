@@ -114,6 +114,8 @@ _SIGS = [
                                                ctypes.c_size_t, _P]),
     ("clk_verify_sample_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                                 _P, _P, _P, ctypes.c_size_t, _P]),
+    ("clk_verify_sample_exact_append", ctypes.c_int, [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P,
+                                                      _P, _P, _P, _P, ctypes.c_size_t, _P]),
     ("clk_status", ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _P]),
     ("clk_status_clear", ctypes.c_int, [_P, _P]),
     ("clk_read_counters", ctypes.c_int, [_P, _I32, _P, _P]),
@@ -409,14 +411,17 @@ def verify_sample(logits, block, length, inv_temp, uniform, accept, emitted, out
                                    scratch.numel(), _stream(stream)))
 
 
-def verify_sample_exact_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None) -> torch.Tensor:
+def verify_sample_exact_scratch(logits_dtype, V: int, B: int, device="cuda", stream=None,
+                                halves: int = 1) -> torch.Tensor:
     """A zeroed scratch buffer for verify_sample_exact with vocabulary V and
-    up to B requests."""
+    up to B requests; halves=2: two halves for the fused calls to alternate
+    (as verify_sample_scratch)."""
     dt = BF16 if logits_dtype == torch.bfloat16 else F32
     n = ctypes.c_size_t()
     _check("clk_verify_sample_exact_scratch_bytes",
            lib().clk_verify_sample_exact_scratch_bytes(dt, V, B, ctypes.byref(n)))
-    t = torch.empty(n.value, dtype=torch.uint8, device=device)
+    size = n.value if halves == 1 else 2 * ((n.value + 255) // 256 * 256)
+    t = torch.empty(size, dtype=torch.uint8, device=device)
     _check("clk_verify_scratch_init", lib().clk_verify_scratch_init(t.data_ptr(), t.numel(), _stream(stream)))
     return t
 
@@ -453,6 +458,24 @@ def verify_sample_append(h: Lookup, slots, logits, block, length, inv_temp, unif
                                           scratch.numel(), _stream(stream)))
 
 
+def verify_sample_exact_append(h: Lookup, slots, logits, block, length, inv_temp, uniform, accept, emitted, out_tok,
+                               scratch, stream=None, length_hint=None):
+    """Exact sampling verification (fixed-point weights) fused with the
+    token commit (clk_verify_sample_exact_append)."""
+    dt, rs, qs, V = _logits_args(logits)
+    B = slots.numel()
+    _check("clk_verify_sample_exact_append",
+           lib().clk_verify_sample_exact_append(h.handle, _ptr(slots), logits.data_ptr(), dt, rs, qs, V, B,
+                                                _ptr(block, shape=(B, BLOCK)), _ptr(length, shape=(B,)),
+                                                _ptr(length_hint, shape=(B,), name="length_hint"),
+                                                _ptr(inv_temp, torch.float32, (B,), "inv_temp"),
+                                                _ptr(uniform, torch.float32, (B, BLOCK, 2), "uniform"),
+                                                _ptr(accept, shape=(B,)), _ptr(emitted, shape=(B,)),
+                                                _ptr(out_tok, shape=(B, BLOCK)),
+                                                _ptr(scratch, torch.uint8, name="scratch"), scratch.numel(),
+                                                _stream(stream)))
+
+
 def verify_append(h: Lookup, slots, logits, block, length, argmax, accept, emitted, out_tok, stream=None,
                   length_hint=None):
     dt, rs, qs, V = _logits_args(logits)
@@ -474,7 +497,8 @@ class Step:
     ``pre(head)``    -> propose + scheduler + fusion: draft, k, j, length, block
     ``post(logits)`` -> verify + commit: argmax, accept, emitted, out_tok
     ``post_sample(logits, inv_temp, uniform)`` -> the same step verified by
-    sampling (point-mass drafts): accept, emitted, out_tok
+    sampling (point-mass drafts): accept, emitted, out_tok; ``exact=True``
+    samples on the fixed-point weights (clk_verify_sample_exact_append)
     The previous step's accept/length feed the scheduler.  The block lengths
     alternate between two buffers, so that ``post`` can pass the previous
     step's lengths as the verify launch's prediction while ``pre`` writes the
@@ -546,22 +570,24 @@ class Step:
                                            p["block"], self._lp[self._cur], self._lp[self._cur ^ 1], p["argmax"],
                                            p["accept"], p["emitted"], p["out_tok"], _stream(stream)))
 
-    def post_sample(self, logits, inv_temp, uniform, stream=None):
+    def post_sample(self, logits, inv_temp, uniform, stream=None, exact: bool = False):
         """Verify the block by sampling at inverse temperatures inv_temp
         (float32 [B]) with the uniforms uniform (float32 [B, 16, 2]), and
         commit the emitted tokens.  Like ``post`` it passes the previous
-        step's lengths as the prediction of the new ones."""
+        step's lengths as the prediction of the new ones.  exact=True: on the
+        fixed-point weights (clk_verify_sample_exact_append)."""
         dt, rs, qs, V = _logits_args(logits)
         if logits.shape[0] != self.B or logits.shape[1] < self._rows:
             raise ValueError(f"logits must be [{self.B}, >= {self._rows}, V]")
-        if self._sscratch is None or self._sscratch[0] != (logits.dtype, V):
-            self._sscratch = ((logits.dtype, V), verify_sample_scratch(logits.dtype, V, self.B,
-                                                                       device=self.slots.device, stream=stream,
-                                                                       halves=2))
+        key = (logits.dtype, V, bool(exact))
+        if self._sscratch is None or self._sscratch[0] != key:
+            make = verify_sample_exact_scratch if exact else verify_sample_scratch
+            self._sscratch = (key, make(logits.dtype, V, self.B, device=self.slots.device, stream=stream, halves=2))
         p = self._p
         sc = self._sscratch[1]
-        _check("clk_verify_sample_append",
-               self._lib.clk_verify_sample_append(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V,
+        name = "clk_verify_sample_exact_append" if exact else "clk_verify_sample_append"
+        _check(name,
+               getattr(self._lib, name)(self.h.handle, p["slots"], logits.data_ptr(), dt, rs, qs, V,
                                                   self.B, p["block"], self._lp[self._cur], self._lp[self._cur ^ 1],
                                                   _ptr(inv_temp, torch.float32, (self.B,), "inv_temp"),
                                                   _ptr(uniform, torch.float32, (self.B, BLOCK, 2), "uniform"),

@@ -737,189 +737,6 @@ __global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample(SampleArg
     }
 }
 
-// The sampler fused with the commit (clk_verify_sample_append), launched as
-// a programmatic dependent of the proposal launch that produces the blocks
-// and lengths.  As in the fused greedy verification, it first streams the
-// segments of every request's predicted rows, max(1 + head, hint) (the
-// short block when the hint is missing or not a valid length), while the
-// proposal launch may still run; the counts of those segments are kept and
-// decided after the wait, when the lengths are known.  Each CTA streams its
-// even share of the predicted segments, waits, and then streams its share of
-// the rows the prediction missed.  A request's total is max(predicted, L_b) rows of segments; the
-// count that reaches it finishes the request (pairs of rows past L_b are
-// never used).  A request with a valid temperature but an invalid length
-// streams its predicted rows for nothing: the count that completes it only
-// sets the counter back to zero.  The inverse temperatures are read before
-// the wait, so they must not come from the proposal launch.
-constexpr int kSMaxDefer = 32;
-constexpr int64_t kSLateBytes = 90ll << 20;  // HBM bytes streamed before the late CTAs start (tuned)
-
-// The block's next action, chosen by thread 0.
-enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
-
-struct SampleStepSmem {
-    int64_t k, kend;          // the current phase's next segment and end (flat)
-    int64_t kstop, hi1;       // where the first phase stopped; the end of this CTA's predicted share
-    int64_t c0, c1;           // the piece to stream: segments [c0, c1) of request cb,
-    int32_t cb, croff;        // rows counted from croff
-    int32_t phase, act;
-    int32_t db[kSMaxDefer];   // kept counts: request,
-    uint32_t dc[kSMaxDefer];  // and the count its addition returned
-    int32_t nd, ci;           // kept counts, and how many of them are decided
-};
-
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(SampleArgs a, LookupDev Ldev)
-{
-    // P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then Lc[B + 1]
-    // (after the wait: each request's length, read once)
-    extern __shared__ int32_t sm_p[];
-    __shared__ int32_t sm_warp[kSWarpsPerCta];
-    __shared__ FinSmem fs;
-    __shared__ SampleStepSmem ss;
-    // Let the next launch (the next proposal) be scheduled; it waits for
-    // this grid to complete before it reads anything this grid writes.  With
-    // paired scratch halves only after this launch's own wait: the next
-    // proposal may then let the next sampled verify start at once (on the
-    // other half), and by then the verify before this one has completed.
-    if (!a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int tid = threadIdx.x;
-    const int32_t B = a.B;
-    int32_t* P1 = sm_p;
-    int32_t* P2 = sm_p + (B + 1);
-    int32_t* Lc = sm_p + 2 * (B + 1);
-    const int32_t base = min(kBlock, 1 + Ldev.p.head);
-    rows_prefix(B, [&a, base](int32_t b) {
-        if (!temp_valid(a.inv_temp[b])) return 0;
-        const int32_t h = a.len_hint != nullptr ? a.len_hint[b] : 0;
-        return len_valid(h) ? max(h, base) : base;
-    }, P1, sm_warp);
-    if (tid == 0) {
-        // This CTA's share of the predicted segments.  As in the fused greedy
-        // verification, the last `late` CTAs start only when the proposal
-        // launch's CTAs leave their SMs, about kSLateBytes of HBM time in;
-        // they get f8/8 of a share, less the shorter this launch.
-        const int64_t n = (int64_t)P1[B] * a.S;
-        const int64_t G = gridDim.x;
-        const int64_t D = min((int64_t)a.late, G / 4);
-        const int64_t bytes = (int64_t)P1[B] * a.V * (int64_t)sizeof(typename SElem<DT>::T);
-        int64_t f8 = bytes > 0 ? 8 - (8 * kSLateBytes + bytes / 2) / bytes : 8;
-        f8 = f8 < 0 ? 0 : (f8 > 8 ? 8 : f8);
-        const int64_t Wtot = (G - D) * 8 + D * f8;
-        auto start = [&](int64_t c) {  // n * W(c) / Wtot without overflow
-            const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
-            return (n / Wtot) * w + (n % Wtot) * w / Wtot;
-        };
-        const int64_t lo = start(blockIdx.x), hi = start(blockIdx.x + 1);
-        ss.k = lo;
-        ss.kend = hi;
-        ss.hi1 = hi;
-        ss.phase = 0;
-        ss.nd = 0;
-        ss.ci = 0;
-    }
-    // Phase 0: this CTA's predicted segments, counts kept (stopping early if
-    // the list of kept counts is full); the wait; phase 1: its share of the
-    // missed rows; phase 2: whatever phase 0 left.  After the wait every
-    // kept count is decided: the one that equals its request's total
-    // (max(predicted, L_b) rows of segments) finishes the request, or, for
-    // an invalid length, only rewinds its counter.  The wait comes after the
-    // whole predicted share: a request completes only once all of its
-    // segments are read, so its finisher runs at the end whatever the order,
-    // and a wait in the middle would pause every CTA at about the same time.
-    for (;;) {
-        if (tid == 0) {
-            int32_t act = kActDone;
-            for (;;) {
-                if (ss.phase > 0 && ss.ci < ss.nd) {
-                    act = kActCheck;
-                    break;
-                }
-                if (ss.phase > 0) ss.ci = ss.nd = 0;
-                if (ss.k < ss.kend && !(ss.phase == 0 && ss.nd == kSMaxDefer)) {
-                    const int32_t* P = ss.phase == 1 ? P2 : P1;
-                    const int32_t b = sample_owner(P, B, ss.k / a.S);
-                    ss.cb = b;
-                    ss.c0 = ss.k;
-                    ss.c1 = min(ss.kend, (int64_t)P[b + 1] * a.S);
-                    ss.croff = ss.phase == 1 ? P1[b + 1] - P1[b] : 0;
-                    act = kActStream;
-                    break;
-                }
-                if (ss.phase == 0) {
-                    ss.kstop = ss.k;
-                    act = kActWait;
-                    break;
-                }
-                if (ss.phase == 1) {
-                    ss.phase = 2;
-                    ss.k = ss.kstop;
-                    ss.kend = ss.hi1;
-                    continue;
-                }
-                break;
-            }
-            ss.act = act;
-        }
-        __syncthreads();
-        const int32_t act = ss.act;
-        if (act == kActDone) break;
-        if (act == kActStream) {
-            const int32_t b = ss.cb;
-            const int32_t* P = ss.phase == 1 ? P2 : P1;
-            if (VEC) stream_vec<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
-            else stream_scalar<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
-            __syncthreads();  // every warp's pairs are stored
-            if (tid == 0) {
-                __threadfence();
-                const uint32_t c = (uint32_t)(ss.c1 - ss.c0);
-                ss.db[ss.nd] = b;
-                ss.dc[ss.nd] = atomicAdd(a.done + b, c) + c;
-                ss.nd += 1;
-                ss.k = ss.c1;
-            }
-        } else if (act == kActCheck) {
-            const int32_t b = ss.db[ss.ci];
-            const int32_t Lb = Lc[b];
-            const int32_t pr = P1[b + 1] - P1[b];
-            const uint32_t total = (uint32_t)((pr > 0 && len_valid(Lb)) ? max(pr, Lb) : pr) * (uint32_t)a.S;
-            if (ss.dc[ss.ci] == total) {
-                if (len_valid(Lb)) sample_finish<DT, true>(a, Ldev, b, fs);
-                else if (tid == 0) a.done[b] = 0u;
-            }
-            __syncthreads();
-            if (tid == 0) ss.ci += 1;
-        } else {  // kActWait
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            if (a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-            rows_prefix(B, [&a, P1, Lc](int32_t b) {
-                const int32_t pr = P1[b + 1] - P1[b];
-                const int32_t Lb = __ldcg(a.len + b);
-                Lc[b] = Lb;
-                return (pr > 0 && len_valid(Lb)) ? max(0, Lb - pr) : 0;
-            }, P2, sm_warp);
-            // Requests with no rows (invalid length or temperature): the
-            // empty result, nothing committed, an error.
-            if (blockIdx.x == 0) {
-                for (int32_t b = tid; b < B; b += kSThreads) {
-                    if (sample_rows(a, b) != 0) continue;
-                    for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
-                    a.accept[b] = 0;
-                    a.emitted[b] = 0;
-                    latch(Ldev.status, CLK_EINVAL, b);
-                }
-            }
-            if (tid == 0) {
-                const int64_t n = (int64_t)P2[B] * a.S;
-                ss.k = n * blockIdx.x / gridDim.x;
-                ss.kend = n * (blockIdx.x + 1) / gridDim.x;
-                ss.phase = 1;
-            }
-        }
-        __syncthreads();
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Exact sampling (clk_verify_sample_exact): the same rule on weights defined
 // as integers, so that every acceptance and every draw is an integer
@@ -1098,12 +915,13 @@ __device__ __forceinline__ unsigned long long fx_record(unsigned long long S, in
 }
 
 // Streams chunks [k0, k1) of request b (flat chunk k is chunk k % NC of the
-// request's row k / NC - P[b]): warp w takes chunks k0 + w, k0 + w + 8, ...
+// request's row roff + k / NC - P[b]): warp w takes chunks k0 + w, k0 + w + 8,
+// ...
 // Every lane holds 32 entries of its chunk (vector path: vectors lane + 32 u);
 // weights are added in 32 bits four at a time, then in 64 bits.
 template <int DT, bool VEC>
-__device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P, int32_t b, int64_t k0, int64_t k1,
-                                          const FxPoly& poly, unsigned long long* rec)
+__device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P, int32_t b, int32_t roff, int64_t k0,
+                                          int64_t k1, const FxPoly& poly, unsigned long long* rec)
 {
     using E = SElem<DT>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1114,7 +932,7 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
     for (int64_t k = k0 + warp; k < k1; k += kSWarpsPerCta) {
         const int64_t ri = k / NC;
         const int32_t ck = (int32_t)(k - ri * NC);
-        const int32_t r = (int32_t)(ri - P[b]);
+        const int32_t r = roff + (int32_t)(ri - P[b]);
         const typename E::T* row = req + (int64_t)r * a.row_stride;
         const int32_t e0 = ck * kFxChunk, n = min(kFxChunk, a.V - e0);  // entries of this chunk
         unsigned long long out;
@@ -1225,13 +1043,17 @@ struct FxFinSmem {
     unsigned long long tc;         // the draw's target inside its chunk
     unsigned long long wsum[kSWarpsPerCta];
     int32_t a, excl, kstar, tok;
+    int32_t out[kBlock];  // the emitted tokens (fused: committed)
+    int32_t flag[3];
 };
 
 // Request b is complete: decide the drafts, draw the token, write the
-// outputs, rewind the counter.  Block-wide.
-template <int DT>
-__device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long long* rec, int32_t b, FxFinSmem& fs,
-                                       const FxPoly& poly)
+// outputs, rewind the counter (fused: commit the emitted tokens; a request
+// whose rows cannot be weighed commits nothing and latches CLK_EINVAL).
+// Block-wide.
+template <int DT, bool FUSED>
+__device__ __noinline__ void fx_finish(const SampleArgs& a, const LookupDev& Ldev, const unsigned long long* rec,
+                                       int32_t b, FxFinSmem& fs, const FxPoly& poly)
 {
     using E = SElem<DT>;
     const unsigned full = 0xFFFFFFFFu;
@@ -1285,6 +1107,7 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
             a.accept[b] = 0;
             a.emitted[b] = 0;
             a.done[b] = 0u;
+            if (FUSED) latch(Ldev.status, CLK_EINVAL, b);
         }
         __syncthreads();
         return;
@@ -1380,8 +1203,9 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
     __syncthreads();
     if (tid < kBlock) {
         const int32_t r = tid;
-        a.out_tok[(int64_t)b * kBlock + r] =
-            r < ra ? a.block[(int64_t)b * kBlock + r + 1] : (r == ra ? fs.tok : CLK_SENT);
+        const int32_t out = r < ra ? a.block[(int64_t)b * kBlock + r + 1] : (r == ra ? fs.tok : CLK_SENT);
+        a.out_tok[(int64_t)b * kBlock + r] = out;
+        fs.out[r] = out;
     }
     if (tid == 0) {
         a.accept[b] = ra;
@@ -1389,6 +1213,15 @@ __device__ __noinline__ void fx_finish(const SampleArgs& a, const unsigned long 
         a.done[b] = 0u;
     }
     __syncthreads();
+    if (FUSED) {
+        const int32_t slot = a.slots[b];
+        if (slot < 0 || slot >= Ldev.max_slots) {
+            if (tid == 0) latch(Ldev.status, CLK_EINVAL, b);
+        } else {
+            block_commit_tokens(Ldev, slot, fs.out, ra + 1, fs.flag);
+        }
+        __syncthreads();
+    }
 }
 
 template <int DT, bool VEC>
@@ -1419,7 +1252,7 @@ __global__ void __launch_bounds__(kSThreads, kFxCtas) k_sample_fx(SampleArgs a, 
     while (k < hi) {
         const int32_t b = sample_owner(P, B, k / NC);
         const int64_t k1 = min(hi, (int64_t)P[b + 1] * NC);
-        fx_stream<DT, VEC>(a, P, b, k, k1, poly, rec);
+        fx_stream<DT, VEC>(a, P, b, 0, k, k1, poly, rec);
         __syncthreads();  // every warp's records are stored
         if (tid == 0) {
             __threadfence();
@@ -1428,10 +1261,228 @@ __global__ void __launch_bounds__(kSThreads, kFxCtas) k_sample_fx(SampleArgs a, 
             sm_last = atomicAdd(a.done + b, n) + n == need;
         }
         __syncthreads();
-        if (sm_last) fx_finish<DT>(a, rec, b, fs, poly);
+        if (sm_last) fx_finish<DT, false>(a, LookupDev{}, rec, b, fs, poly);
         k = k1;
     }
 }
+
+// The sampler fused with the commit (clk_verify_sample_append), launched as
+// a programmatic dependent of the proposal launch that produces the blocks
+// and lengths.  As in the fused greedy verification, it first streams the
+// segments of every request's predicted rows, max(1 + head, hint) (the
+// short block when the hint is missing or not a valid length), while the
+// proposal launch may still run; the counts of those segments are kept and
+// decided after the wait, when the lengths are known.  Each CTA streams its
+// even share of the predicted segments, waits, and then streams its share of
+// the rows the prediction missed.  A request's total is max(predicted, L_b) rows of segments; the
+// count that reaches it finishes the request (pairs of rows past L_b are
+// never used).  A request with a valid temperature but an invalid length
+// streams its predicted rows for nothing: the count that completes it only
+// sets the counter back to zero.  The inverse temperatures are read before
+// the wait, so they must not come from the proposal launch.
+constexpr int kSMaxDefer = 32;
+constexpr int64_t kSLateBytes = 90ll << 20;  // HBM bytes streamed before the late CTAs start (tuned)
+
+// The block's next action, chosen by thread 0.
+enum SampleAct : int32_t { kActStream, kActCheck, kActWait, kActDone };
+
+struct SampleStepSmem {
+    int64_t k, kend;          // the current phase's next segment and end (flat)
+    int64_t kstop, hi1;       // where the first phase stopped; the end of this CTA's predicted share
+    int64_t c0, c1;           // the piece to stream: segments [c0, c1) of request cb,
+    int32_t cb, croff;        // rows counted from croff
+    int32_t phase, act;
+    int32_t db[kSMaxDefer];   // kept counts: request,
+    uint32_t dc[kSMaxDefer];  // and the count its addition returned
+    int32_t nd, ci;           // kept counts, and how many of them are decided
+};
+
+// The fused sampler's body, on the float weights (FX = false: per-warp
+// (m, s) pairs per segment, sample_finish) or on the fixed-point ones
+// (FX = true: units are 1024-entry chunks with one record each, fx_finish).
+// Fin is the finisher's shared memory of the kind.
+template <int DT, bool VEC, bool FX, typename Fin>
+__device__ __forceinline__ void sample_step_body(const SampleArgs& a, const LookupDev& Ldev, const FxPoly& poly,
+                                                 int32_t* sm_p, int32_t* sm_warp, Fin& fs, SampleStepSmem& ss)
+{
+    // sm_p: P1[B + 1] (predicted rows), P2[B + 1] (missed rows), then
+    // Lc[B + 1] (after the wait: each request's length, read once)
+    // Let the next launch (the next proposal) be scheduled; it waits for
+    // this grid to complete before it reads anything this grid writes.  With
+    // paired scratch halves only after this launch's own wait: the next
+    // proposal may then let the next sampled verify start at once (on the
+    // other half), and by then the verify before this one has completed.
+    if (!a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    const int32_t B = a.B;
+    int32_t* P1 = sm_p;
+    int32_t* P2 = sm_p + (B + 1);
+    int32_t* Lc = sm_p + 2 * (B + 1);
+    const int32_t base = min(kBlock, 1 + Ldev.p.head);
+    rows_prefix(B, [&a, base](int32_t b) {
+        if (!temp_valid(a.inv_temp[b])) return 0;
+        const int32_t h = a.len_hint != nullptr ? a.len_hint[b] : 0;
+        return len_valid(h) ? max(h, base) : base;
+    }, P1, sm_warp);
+    if (tid == 0) {
+        // This CTA's share of the predicted segments.  As in the fused greedy
+        // verification, the last `late` CTAs start only when the proposal
+        // launch's CTAs leave their SMs, about kSLateBytes of HBM time in;
+        // they get f8/8 of a share, less the shorter this launch.
+        const int64_t n = (int64_t)P1[B] * a.S;
+        const int64_t G = gridDim.x;
+        const int64_t D = min((int64_t)a.late, G / 4);
+        const int64_t bytes = (int64_t)P1[B] * a.V * (int64_t)sizeof(typename SElem<DT>::T);
+        int64_t f8 = bytes > 0 ? 8 - (8 * kSLateBytes + bytes / 2) / bytes : 8;
+        f8 = f8 < 0 ? 0 : (f8 > 8 ? 8 : f8);
+        const int64_t Wtot = (G - D) * 8 + D * f8;
+        auto start = [&](int64_t c) {  // n * W(c) / Wtot without overflow
+            const int64_t w = c <= G - D ? c * 8 : (G - D) * 8 + (c - (G - D)) * f8;
+            return (n / Wtot) * w + (n % Wtot) * w / Wtot;
+        };
+        const int64_t lo = start(blockIdx.x), hi = start(blockIdx.x + 1);
+        ss.k = lo;
+        ss.kend = hi;
+        ss.hi1 = hi;
+        ss.phase = 0;
+        ss.nd = 0;
+        ss.ci = 0;
+    }
+    // Phase 0: this CTA's predicted segments, counts kept (stopping early if
+    // the list of kept counts is full); the wait; phase 1: its share of the
+    // missed rows; phase 2: whatever phase 0 left.  After the wait every
+    // kept count is decided: the one that equals its request's total
+    // (max(predicted, L_b) rows of segments) finishes the request, or, for
+    // an invalid length, only rewinds its counter.  The wait comes after the
+    // whole predicted share: a request completes only once all of its
+    // segments are read, so its finisher runs at the end whatever the order,
+    // and a wait in the middle would pause every CTA at about the same time.
+    for (;;) {
+        if (tid == 0) {
+            int32_t act = kActDone;
+            for (;;) {
+                if (ss.phase > 0 && ss.ci < ss.nd) {
+                    act = kActCheck;
+                    break;
+                }
+                if (ss.phase > 0) ss.ci = ss.nd = 0;
+                if (ss.k < ss.kend && !(ss.phase == 0 && ss.nd == kSMaxDefer)) {
+                    const int32_t* P = ss.phase == 1 ? P2 : P1;
+                    const int32_t b = sample_owner(P, B, ss.k / a.S);
+                    ss.cb = b;
+                    ss.c0 = ss.k;
+                    ss.c1 = min(ss.kend, (int64_t)P[b + 1] * a.S);
+                    ss.croff = ss.phase == 1 ? P1[b + 1] - P1[b] : 0;
+                    act = kActStream;
+                    break;
+                }
+                if (ss.phase == 0) {
+                    ss.kstop = ss.k;
+                    act = kActWait;
+                    break;
+                }
+                if (ss.phase == 1) {
+                    ss.phase = 2;
+                    ss.k = ss.kstop;
+                    ss.kend = ss.hi1;
+                    continue;
+                }
+                break;
+            }
+            ss.act = act;
+        }
+        __syncthreads();
+        const int32_t act = ss.act;
+        if (act == kActDone) break;
+        if (act == kActStream) {
+            const int32_t b = ss.cb;
+            const int32_t* P = ss.phase == 1 ? P2 : P1;
+            if constexpr (FX) {
+                fx_stream<DT, VEC>(a, P, b, ss.croff, ss.c0, ss.c1, poly, reinterpret_cast<unsigned long long*>(a.part));
+            } else {
+                if (VEC) stream_vec<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
+                else stream_scalar<DT>(a, P, b, ss.croff, ss.c0, ss.c1);
+            }
+            __syncthreads();  // every warp's pairs (or chunk records) are stored
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t c = (uint32_t)(ss.c1 - ss.c0);
+                ss.db[ss.nd] = b;
+                ss.dc[ss.nd] = atomicAdd(a.done + b, c) + c;
+                ss.nd += 1;
+                ss.k = ss.c1;
+            }
+        } else if (act == kActCheck) {
+            const int32_t b = ss.db[ss.ci];
+            const int32_t Lb = Lc[b];
+            const int32_t pr = P1[b + 1] - P1[b];
+            const uint32_t total = (uint32_t)((pr > 0 && len_valid(Lb)) ? max(pr, Lb) : pr) * (uint32_t)a.S;
+            if (ss.dc[ss.ci] == total) {
+                if (len_valid(Lb)) {
+                    if constexpr (FX) {
+                        fx_finish<DT, true>(a, Ldev, reinterpret_cast<const unsigned long long*>(a.part), b, fs, poly);
+                    } else {
+                        sample_finish<DT, true>(a, Ldev, b, fs);
+                    }
+                } else if (tid == 0) {
+                    a.done[b] = 0u;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) ss.ci += 1;
+        } else {  // kActWait
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (a.paired) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            rows_prefix(B, [&a, P1, Lc](int32_t b) {
+                const int32_t pr = P1[b + 1] - P1[b];
+                const int32_t Lb = __ldcg(a.len + b);
+                Lc[b] = Lb;
+                return (pr > 0 && len_valid(Lb)) ? max(0, Lb - pr) : 0;
+            }, P2, sm_warp);
+            // Requests with no rows (invalid length or temperature): the
+            // empty result, nothing committed, an error.
+            if (blockIdx.x == 0) {
+                for (int32_t b = tid; b < B; b += kSThreads) {
+                    if (sample_rows(a, b) != 0) continue;
+                    for (int r = 0; r < kBlock; ++r) a.out_tok[(int64_t)b * kBlock + r] = CLK_SENT;
+                    a.accept[b] = 0;
+                    a.emitted[b] = 0;
+                    latch(Ldev.status, CLK_EINVAL, b);
+                }
+            }
+            if (tid == 0) {
+                const int64_t n = (int64_t)P2[B] * a.S;
+                ss.k = n * blockIdx.x / gridDim.x;
+                ss.kend = n * (blockIdx.x + 1) / gridDim.x;
+                ss.phase = 1;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSThreads, CLK_SAMPLE_CTAS) k_sample_step(SampleArgs a, LookupDev Ldev)
+{
+    extern __shared__ int32_t sm_p[];
+    __shared__ int32_t sm_warp[kSWarpsPerCta];
+    __shared__ FinSmem fs;
+    __shared__ SampleStepSmem ss;
+    sample_step_body<DT, VEC, false>(a, Ldev, FxPoly{}, sm_p, sm_warp, fs, ss);
+}
+
+// The exact sampler fused with the commit (clk_verify_sample_exact_append):
+// the fused schedule above on 1024-entry chunks.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSThreads, kFxCtas) k_sample_step_fx(SampleArgs a, LookupDev Ldev, FxPoly poly)
+{
+    extern __shared__ int32_t sm_p[];
+    __shared__ int32_t sm_warp[kSWarpsPerCta];
+    __shared__ FxFinSmem fs;
+    __shared__ SampleStepSmem ss;
+    sample_step_body<DT, VEC, true>(a, Ldev, poly, sm_p, sm_warp, fs, ss);
+}
+
 
 int fx_sizes(int32_t dtype, int32_t V, int32_t B, int32_t* NC, size_t* bytes)
 {
@@ -1548,6 +1599,52 @@ int launch_sample(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, Ldev));
 }
 
+// The exact sampler fused with the commit: launched as launch_sample's fused
+// path launches the float one (programmatic dependent of the proposal launch,
+// the CTAs dispatched behind it given a smaller share).
+template <int DT, bool VEC>
+int launch_sample_fx_fused(const SampleArgs& a, const LookupDev& Ldev, cudaStream_t s)
+{
+    static std::atomic<int> cache[64];  // resident CTAs per SM, per device (calls from any host thread)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CLK_ECUDA;
+    const size_t smem = (size_t)3 * (a.B + 1) * sizeof(int32_t);
+    auto kern = k_sample_step_fx<DT, VEC>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CLK_ECUDA;
+    int occ = (dev >= 0 && dev < 64 && smem <= 4096) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (occ <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSThreads, smem <= 4096 ? 4096 : smem) !=
+                cudaSuccess ||
+            occ < 1)
+            return CLK_ECUDA;
+        if (dev >= 0 && dev < 64 && smem <= 4096) cache[dev].store(occ, std::memory_order_relaxed);
+    }
+    const int sms = num_sms();
+    if (sms <= 0) return CLK_ECUDA;
+    const int64_t chunks = (int64_t)a.B * kBlock * a.S;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((int64_t)occ * sms, chunks));
+    SampleArgs args = a;
+    if (a.late > 0) {
+        const int64_t taken = (int64_t)displaced_by_proposal<k_sample_step_fx<DT, VEC>>(kSThreads, Ldev.nlev, occ) *
+                              (a.B < sms ? a.B : sms);
+        const int64_t late = grid - ((int64_t)occ * sms - taken);
+        args.late = late > 0 ? (int32_t)late : 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args, Ldev, fx_poly()));
+}
+
 }  // namespace
 }  // namespace clk
 
@@ -1619,7 +1716,14 @@ int sample_entry(clk_lookup* h, const int32_t* d_slots, const void* d_logits, in
     const int64_t W = 16 / (int64_t)esz;
     const bool vec = aligned(d_logits, 16) && V % W == 0 && row_stride % W == 0 && req_stride % W == 0;
     const bool bf = dtype == CLK_DTYPE_BF16;
-    if (exact) {  // stateless only
+    if (exact && h != nullptr) {
+        const LookupDev& L = h->dev;
+        if (bf) return vec ? launch_sample_fx_fused<CLK_DTYPE_BF16, true>(a, L, cs)
+                           : launch_sample_fx_fused<CLK_DTYPE_BF16, false>(a, L, cs);
+        return vec ? launch_sample_fx_fused<CLK_DTYPE_F32, true>(a, L, cs)
+                   : launch_sample_fx_fused<CLK_DTYPE_F32, false>(a, L, cs);
+    }
+    if (exact) {
         if (bf) return vec ? launch_fx<CLK_DTYPE_BF16, true>(a, cs) : launch_fx<CLK_DTYPE_BF16, false>(a, cs);
         return vec ? launch_fx<CLK_DTYPE_F32, true>(a, cs) : launch_fx<CLK_DTYPE_F32, false>(a, cs);
     }
@@ -1661,27 +1765,30 @@ extern "C" int clk_verify_sample_exact(const void* d_logits, int32_t dtype, int6
                         (cudaStream_t)s, false, true);
 }
 
-extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
-                                        int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
-                                        const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
-                                        const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
-                                        int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch,
-                                        size_t scratch_bytes, clk_stream_t s)
+namespace {
+
+// The fused sampled verification, float (exact = false) or fixed-point
+// weights.  A scratch of two halves (each half of the buffer, rounded down to
+// 256 bytes, whatever the batch, and each at least what this batch needs):
+// consecutive calls alternate them, and the next proposal may let the next
+// call start streaming before its own wait.  One buffer: the next proposal
+// must not let the next verify start before this one completes.
+int sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype, int64_t row_stride,
+                  int64_t req_stride, int32_t V, int32_t B, const int32_t* d_block, const int32_t* d_len,
+                  const int32_t* d_len_hint, const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                  int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes, clk_stream_t s,
+                  bool exact)
 {
     if (h == nullptr) return CLK_EINVAL;
-    // A scratch of two halves (each half of the buffer, rounded down to 256
-    // bytes, whatever the batch, and each at least what this batch needs):
-    // consecutive calls alternate them, and the next proposal may let the
-    // next call start streaming before its own wait.  One buffer: the next
-    // proposal must not let the next verify start before this one completes.
     int32_t S = 0;
     size_t need = 0;
     const size_t half_bytes = (scratch_bytes / 2) & ~(size_t)255;
-    const bool paired = sample_sizes(dtype, V, B, &S, &need) == CLK_OK && d_scratch != nullptr && half_bytes >= need;
+    const int sz = exact ? fx_sizes(dtype, V, B, &S, &need) : sample_sizes(dtype, V, B, &S, &need);
+    const bool paired = sz == CLK_OK && d_scratch != nullptr && half_bytes >= need;
     void* half = paired ? static_cast<char*>(d_scratch) + (size_t)h->sparity * half_bytes : d_scratch;
     const int rc = sample_entry(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len,
                                 d_len_hint, d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, half,
-                                paired ? half_bytes : scratch_bytes, (cudaStream_t)s, paired);
+                                paired ? half_bytes : scratch_bytes, (cudaStream_t)s, paired, exact);
     if (rc == CLK_OK && paired) {
         h->sparity ^= 1;
         h->last_fused = kFusedSampledPaired;
@@ -1690,4 +1797,29 @@ extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, c
         h->last_fused = rc == CLK_OK ? kFusedSampled : kFusedNone;
     }
     return rc;
+}
+
+}  // namespace
+
+extern "C" int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
+                                        int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                                        const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
+                                        const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                        int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch,
+                                        size_t scratch_bytes, clk_stream_t s)
+{
+    return sample_append(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_len_hint,
+                         d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, s, false);
+}
+
+extern "C" int clk_verify_sample_exact_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits,
+                                              int32_t dtype, int64_t row_stride, int64_t req_stride, int32_t V,
+                                              int32_t B, const int32_t* d_block, const int32_t* d_len,
+                                              const int32_t* d_len_hint, const float* d_inv_temp,
+                                              const float* d_uniform, int32_t* d_accept, int32_t* d_emitted,
+                                              int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
+                                              clk_stream_t s)
+{
+    return sample_append(h, d_slots, d_logits, dtype, row_stride, req_stride, V, B, d_block, d_len, d_len_hint,
+                         d_inv_temp, d_uniform, d_accept, d_emitted, d_out_tok, d_scratch, scratch_bytes, s, true);
 }

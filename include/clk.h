@@ -467,6 +467,25 @@ CLK_API int clk_verify_sample_append(clk_lookup* h, const int32_t* d_slots, cons
                                      int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch, size_t scratch_bytes,
                                      clk_stream_t s);
 
+/* clk_verify_sample_exact followed by clk_lookup_append of its d_out_tok /
+ * d_emitted, in one launch: the sampled step of a decode loop on the exact
+ * (fixed-point) weights.  Everything else is as for
+ * clk_verify_sample_append: a programmatic dependent of the preceding launch,
+ * the rows of a predicted length read before the wait (d_len_hint only a
+ * prediction), the empty result, no commit and CLK_EINVAL latched for an
+ * invalid length, temperature, slot or token, and the two scratch halves;
+ * the scratch holds clk_verify_sample_exact_scratch_bytes(dtype, V, B) (or
+ * twice that, rounded up to 256 bytes, for the halves).  A request with a row
+ * that cannot be weighed (clk_verify_sample_exact) also gets the empty
+ * result, commits nothing and latches CLK_EINVAL.  The results equal those
+ * of clk_verify_sample_exact and clk_lookup_append. */
+CLK_API int clk_verify_sample_exact_append(clk_lookup* h, const int32_t* d_slots, const void* d_logits, int32_t dtype,
+                                           int64_t row_stride, int64_t req_stride, int32_t V, int32_t B,
+                                           const int32_t* d_block, const int32_t* d_len, const int32_t* d_len_hint,
+                                           const float* d_inv_temp, const float* d_uniform, int32_t* d_accept,
+                                           int32_t* d_emitted, int32_t* d_out_tok, void* d_scratch,
+                                           size_t scratch_bytes, clk_stream_t s);
+
 /* ---------------------------------------------------------------------- */
 /* Status, counters, inspection (these synchronise the stream)             */
 /* ---------------------------------------------------------------------- */

@@ -196,14 +196,67 @@ def test_exact_sampled_loop_matches_the_oracle(inv_temp):
     assert not msgs, "\n".join(msgs[:8])
 
 
-@pytest.mark.parametrize("inv_temp", [4.0, float(np.float32(1 / 0.7))])
-def test_exact_sampled_loop_full_size_mixed_batch_64_steps(inv_temp):
-    """The mixed serving batch (B = 64, V = 248,320, bf16) for 64 steps of
-    the exact sampled loop, at temperatures 0.25 and 0.7: every record,
-    history and counter equal to the oracle's."""
-    w = wl.make("2").with_steps(64)
-    dev = drive.run_device(w, mode="sample_exact", inv_temp=inv_temp)
+@pytest.mark.parametrize("inv_temp", [1.0, 2.5])
+def test_exact_fused_sampled_loop_matches_the_oracle(inv_temp):
+    """The decode loop as the Step driver runs it with the exact sampler
+    fused with the commit (clk_verify_sample_exact_append): every record,
+    history and counter equal to the oracle's loop on the same weights."""
+    w = wl.make_small("mixed", seed=76, B=6, V=2048, steps=48)
+    dev = drive.run_device(w, mode="sample_exact_fused", inv_temp=inv_temp)
     ref = oracle.run(w, threads=THREADS, inv_temp=inv_temp, exact=True)
     msgs = drive.compare(dev, ref)
     assert not msgs, "\n".join(msgs[:8])
+
+
+@pytest.mark.parametrize("inv_temp", [4.0, float(np.float32(1 / 0.7))])
+def test_exact_sampled_loop_full_size_mixed_batch_64_steps(inv_temp):
+    """The mixed serving batch (B = 64, V = 248,320, bf16) for 64 steps of
+    the exact sampled loop at temperatures 0.25 and 0.7, both as the Step
+    driver runs it (the sampler fused with the commit, two launches a step)
+    and unfused: every record, history and counter equal to the oracle's."""
+    w = wl.make("2").with_steps(64)
+    ref = oracle.run(w, threads=THREADS, inv_temp=inv_temp, exact=True)
     assert (ref.a > 0).any()
+    for mode in ("sample_exact_fused", "sample_exact"):
+        dev = drive.run_device(w, mode=mode, inv_temp=inv_temp)
+        msgs = drive.compare(dev, ref)
+        assert not msgs, mode + ": " + "\n".join(msgs[:8])
+
+
+@pytest.mark.parametrize("hint", ["none", "short", "long", "exact", "garbage"])
+def test_exact_fused_results_do_not_depend_on_the_length_hint(hint):
+    """clk_verify_sample_exact_append reads the rows of a predicted length
+    before the preceding launch has finished; every chunk's record is the same
+    whichever CTA reads it, so the outputs equal the stateless exact sampler's
+    bit for bit for any hint, and each valid request commits exactly its
+    emitted tokens; invalid requests and a row that cannot be weighed commit
+    nothing and latch CLK_EINVAL."""
+    B, V = 40, 4096
+    x, blk, L, t, u = _case(B, V, torch.bfloat16, seed=90)
+    L[::7] = 0
+    t[3] = 0.0
+    x[5, 2, 17] = 5.0e6  # request 5: a row whose chunk maximum is past 2^22
+    L[5] = 16
+    want_acc, want_out = _check(x, blk, L, t, u)
+    assert want_acc[5] == 0 and (want_out[5] == SENT).all()
+    rng = np.random.default_rng(90)
+    hints = {"none": None, "short": np.full(B, 8), "long": np.full(B, 16), "exact": L.cpu().numpy(),
+             "garbage": rng.integers(-5, 40, size=B)}
+    h = hints[hint]
+    s = torch.arange(B, dtype=torch.int32, device="cuda")
+    hint_t = None if h is None else torch.from_numpy(np.asarray(h, np.int32)).cuda()
+    for halves in (1, 2):
+        lk = clk.Lookup(max_slots=B, max_hist=64, vocab=V)
+        clk.lookup_init(lk, s, torch.ones(B, dtype=torch.int32, device="cuda"),
+                        torch.arange(B + 1, dtype=torch.int64, device="cuda"))
+        acc = torch.full((B,), 77, dtype=torch.int32, device="cuda")
+        em, out = torch.full_like(acc, 77), torch.full((B, 16), 77, dtype=torch.int32, device="cuda")
+        scratch = clk.verify_sample_exact_scratch(x.dtype, V, B, halves=halves)
+        clk.verify_sample_exact_append(lk, s, x, blk, L, t, u, acc, em, out, scratch, length_hint=hint_t)
+        torch.cuda.synchronize()
+        assert np.array_equal(acc.cpu().numpy(), want_acc)
+        assert np.array_equal(out.cpu().numpy(), want_out)
+        emn, outn = em.cpu().numpy(), out.cpu().numpy()
+        for b in range(B):
+            assert lk.history(b).tolist() == [1] + outn[b][:emn[b]].tolist(), b
+        assert lk.status()[0] == clk.EINVAL

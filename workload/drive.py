@@ -57,6 +57,8 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
                     driver's sampled step); g as for "sample"
     mode "sample_exact": as "sample" with verify_sample_exact (the
                     fixed-point weights)
+    mode "sample_exact_fused": as "sample_fused" on the fixed-point weights
+                    (verify_sample_exact_append)
     """
     steps = w.steps if steps is None else steps
     params = params or clk.Params.default()
@@ -72,7 +74,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     rec = {n: torch.zeros((steps, B), **i32) for n in ("k", "j", "L", "a", "e")}
     rec.update({n: torch.zeros((steps, B, clk.BLOCK), **i32) for n in ("c", "blk", "g")})
     scratch = clk.verify_scratch(B, device=device) if mode == "unfused" else None
-    if mode in ("sample", "sample_fused", "sample_exact"):
+    if mode in ("sample", "sample_fused", "sample_exact", "sample_exact_fused"):
         if not inv_temp > 0:
             raise ValueError("mode 'sample' needs inv_temp > 0")
         if mode == "sample_exact":
@@ -85,7 +87,7 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
     for t in range(steps):
         gen.head(t, head7)
         head = head7[:, :params.head].contiguous()
-        if mode in ("fused", "sample_fused"):
+        if mode in ("fused", "sample_fused", "sample_exact_fused"):
             st.pre(head)
         elif mode == "semi":
             clk.lookup_propose(lk, slots, st.draft, st.k, st.j)
@@ -108,9 +110,9 @@ def run_device(w: wl.Workload, steps: Optional[int] = None, params=None, mode: s
             clk.lookup_append(lk, slots, st.out_tok, st.emitted)
             last_tok = st.out_tok.gather(1, st.accept.long().unsqueeze(1)).squeeze(1).contiguous()
             st.argmax.copy_(st.out_tok)  # recorded as g
-        elif mode == "sample_fused":
+        elif mode in ("sample_fused", "sample_exact_fused"):
             gen.uniforms(t, uni)
-            st.post_sample(logits, temps, uni)
+            st.post_sample(logits, temps, uni, exact=mode == "sample_exact_fused")
             st.argmax.copy_(st.out_tok)  # recorded as g
         else:
             st.post(logits)
