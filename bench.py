@@ -55,6 +55,31 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# The exact sampler is bound by arithmetic, not HBM.  Its algorithmic work per
+# entry, in thread instructions: the scaled difference d (one fused
+# multiply-add), the rounding split (three adds) and six Horner steps, all
+# packed two entries to an instruction (5 per entry), plus six integer
+# operations (the mantissa scaled, the shift amount, the funnel shift, the
+# two of the rounding and the sum).  Peak: one warp instruction per scheduler
+# per clock, four schedulers per SM.
+FX_INSTR_PER_ENTRY = 11
+
+
+def _alu_roofline(kernel: str, entries: float, seconds: float, clocks: dict, hbm: dict) -> dict:
+    import torch
+
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = float(clocks.get("sm_max_mhz") or 2070.0)
+    peak = 4 * 32 * sms * mhz * 1e6 / 1e12  # thread instructions, T/s
+    achieved = entries * FX_INSTR_PER_ENTRY / seconds / 1e12
+    return {"bound": "alu", "kernel": kernel, "achieved": round(achieved, 3), "peak": round(peak, 3),
+            "unit": "T thread-instructions/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"4 schedulers x 32 lanes x {sms} SMs x {mhz:.0f} MHz (one instruction per scheduler "
+                           f"per clock)",
+            "algorithmic_instructions_per_entry": FX_INSTR_PER_ENTRY, "entries_per_launch": int(entries),
+            "hbm": hbm}
+
+
 def _verify_sources_hash() -> str:
     h = hashlib.sha256()
     for f in ("clk_verify.cu", "clk_device.cuh"):
@@ -461,6 +486,9 @@ def run_ours(args, world, rank, local, dist):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if exact:  # the exact sampler is bound by arithmetic: its roofline in instructions, HBM beside it
+        out["roofline"] = _alu_roofline(out["roofline"]["kernel"], verify_bytes / esz / K, total_s / K,
+                                        out["clocks"], out["roofline"])
     return out
 
 
@@ -585,17 +613,20 @@ def run_sample_verify(args, world, rank, local, dist):
     name = "exact sampled verify launches/s (fixed-point weights)" if exact else \
         "sampled verify launches/s (point-mass drafts)"
     kern = "k_sample_fx (verify_sample_exact)" if exact else "k_sample (verify_sample)"
+    hbm_roof = {"bound": "hbm", "kernel": kern, "achieved": round(alg / mean_us / 1e3, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(alg / mean_us / 1e3 / peak, 4),
+                "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg}
+    csum = clocks.summary()
     return {"metric": name, "value": round(1e6 / mean_us, 2),
             "unit": "launches/s", "n_gpus": world, "steps": K, "warmup": W, "us_per_launch": round(mean_us, 3),
             "higher_is_better": True, "dtype": "bf16" if w.dtype == wl.BF16 else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name}: {CONFIG_NAMES[args.config]}", "batch": B, "vocab": V,
                        "temperature": 0.3, "block": "16 for copy-heavy requests, 8 for chat-like",
                        "l2": "every launch reads its own pre-generated logits (larger than L2)"},
-            "roofline": {"bound": "hbm", "kernel": kern, "achieved": round(alg / mean_us / 1e3, 1),
-                         "peak": peak, "unit": "GB/s", "frac": round(alg / mean_us / 1e3 / peak, 4),
-                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
+            "roofline": hbm_roof if not exact else
+            _alu_roofline(kern, rows * V + B * min(V, 1024), mean_us * 1e-6, csum, hbm_roof),
             "exp_per_launch": rows * V, "tokens_per_request_launch": round(emitted.sum().item() / (B * K), 4),
-            "clocks": clocks.summary(), "gpu_launches": K}
+            "clocks": csum, "gpu_launches": K}
 
 
 def _kind_metrics(after, before, kinds, head):
