@@ -886,6 +886,16 @@ struct FxVec;
 template <>
 struct FxVec<CLK_DTYPE_BF16> {
     __device__ static uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+    // the largest of a lane's 4 vectors: packed bf16 maxima over all 16 words, then the two halves
+    __device__ static float vmax(const uint4 (&X)[4])
+    {
+        using E = SElem<CLK_DTYPE_BF16>;
+        __nv_bfloat162 m = __hmax2(__hmax2(E::as2(X[0].x), E::as2(X[0].y)), __hmax2(E::as2(X[0].z), E::as2(X[0].w)));
+#pragma unroll
+        for (int u = 1; u < 4; ++u)
+            m = __hmax2(m, __hmax2(__hmax2(E::as2(X[u].x), E::as2(X[u].y)), __hmax2(E::as2(X[u].z), E::as2(X[u].w))));
+        return fmaxf(__low2float(m), __high2float(m));
+    }
     // the 8 weights of one vector, in pairs, then two sums of four
     __device__ static unsigned long long weights(const uint4& v, unsigned long long s2, unsigned long long nR2,
                                                  const FxPoly& P)
@@ -900,6 +910,14 @@ struct FxVec<CLK_DTYPE_BF16> {
 template <>
 struct FxVec<CLK_DTYPE_F32> {
     __device__ static uint4 neg_inf() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+    __device__ static float vmax(const uint4 (&X)[8])
+    {
+        using E = SElem<CLK_DTYPE_F32>;
+        float m = E::vmax(X[0]);
+#pragma unroll
+        for (int u = 1; u < 8; ++u) m = fmaxf(m, E::vmax(X[u]));
+        return m;
+    }
     __device__ static unsigned long long weights(const uint4& v, unsigned long long s2, unsigned long long nR2,
                                                  const FxPoly& P)
     {
@@ -929,10 +947,13 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
     const float s = a.inv_temp[b] * kLog2e;
     const unsigned long long s2 = pk(s, s);
     const typename E::T* req = static_cast<const typename E::T*>(a.logits) + (int64_t)b * a.req_stride;
-    for (int64_t k = k0 + warp; k < k1; k += kSWarpsPerCta) {
-        const int64_t ri = k / NC;
-        const int32_t ck = (int32_t)(k - ri * NC);
-        const int32_t r = roff + (int32_t)(ri - P[b]);
+    unsigned long long* recb = rec + (int64_t)b * kBlock * NC;
+    // this warp's first chunk (one division per call), then 8 chunks on per step
+    const int64_t kw = k0 + warp;
+    const int64_t ri0 = kw / NC;
+    int32_t ck = (int32_t)(kw - ri0 * NC);
+    int32_t r = roff + (int32_t)(ri0 - P[b]);
+    for (int64_t k = kw; k < k1; k += kSWarpsPerCta) {
         const typename E::T* row = req + (int64_t)r * a.row_stride;
         const int32_t e0 = ck * kFxChunk, n = min(kFxChunk, a.V - e0);  // entries of this chunk
         unsigned long long out;
@@ -946,10 +967,7 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
                 const int32_t vi = lane + 32 * u;
                 X[u] = vi < nvec ? __ldcs(rv + vi) : FxVec<DT>::neg_inf();
             }
-            float mx = E::vmax(X[0]);
-#pragma unroll
-            for (int u = 1; u < NV; ++u) mx = fmaxf(mx, E::vmax(X[u]));
-            mx = fx_warp_max(mx);
+            float mx = fx_warp_max(FxVec<DT>::vmax(X));
             if (mx == -INFINITY) {
                 out = fx_record(0ull, kFxNoRef);
             } else {
@@ -992,7 +1010,12 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
                 }
             }
         }
-        if (lane == 0) rec[((int64_t)b * kBlock + r) * NC + ck] = out;
+        if (lane == 0) recb[r * NC + ck] = out;
+        ck += kSWarpsPerCta;
+        while (ck >= NC) {  // warp-uniform; once at most unless a row has fewer than 8 chunks
+            ck -= NC;
+            ++r;
+        }
     }
 }
 
