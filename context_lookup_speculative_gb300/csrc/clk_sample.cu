@@ -962,10 +962,15 @@ __device__ __forceinline__ void fx_stream(const SampleArgs& a, const int32_t* P,
             const uint4* rv = reinterpret_cast<const uint4*>(row + e0);
             const int32_t nvec = n / E::W;
             uint4 X[NV];
+            if (nvec == NV * 32) {  // a whole chunk (all but a row's last): no bounds to test
 #pragma unroll
-            for (int u = 0; u < NV; ++u) {
-                const int32_t vi = lane + 32 * u;
-                X[u] = vi < nvec ? __ldcs(rv + vi) : FxVec<DT>::neg_inf();
+                for (int u = 0; u < NV; ++u) X[u] = __ldcs(rv + lane + 32 * u);
+            } else {
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    const int32_t vi = lane + 32 * u;
+                    X[u] = vi < nvec ? __ldcs(rv + vi) : FxVec<DT>::neg_inf();
+                }
             }
             float mx = fx_warp_max(FxVec<DT>::vmax(X));
             if (mx == -INFINITY) {
