@@ -287,6 +287,7 @@ MUTANTS = {
         "const uint64_t w = or_fx_rowunits(qc, Rr - Rrow[kc]);",
         "const uint64_t w = or_fx_q(or_row_value(row, dtype, cd), s, (float)Rr, c);"),
     "chunk reference from the first entry": ("if (x > M) M = x;", "if (v == v0) M = x;"),
+    "weights rounded down": ("    return (((m << 7) >> sh) + 1) >> 1;", "    return (m << 6) >> sh;"),
 }
 
 
@@ -357,3 +358,39 @@ def test_unmutated_source_passes(tmp_path):
 def test_planted_mistake_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     assert not _pins_pass(_build_mutant(tmp_path, name, old, new)), name
+
+
+def test_implied_distribution_is_close_to_the_softmax():
+    """The exact sampler's distribution (each entry's weight in row units
+    over the row's total) is within 1e-6 in total variation of the softmax
+    computed in double, at several temperatures, including rows whose chunk
+    maxima are far apart (a spike in one chunk)."""
+    rng = np.random.default_rng(12)
+    L2E = np.float32(1.4426950408889634)
+    for t in (0.25, 1.0, 1.4285714, 4.0):
+        for spike in (0.0, 8.0):
+            V = 3000
+            row = (rng.standard_normal(V) * 1.5).astype(np.float32)
+            row[int(rng.integers(0, V))] += np.float32(spike)
+            S, R = oracle.fx_chunks(row, t)
+            s = np.float32(np.float32(t) * L2E)
+            Rr = int(R.max())
+            w = np.array([oracle.fx_weight(row[i], s, int(R[i // oracle.FX_CHUNK])) *
+                          2.0 ** (int(R[i // oracle.FX_CHUNK]) - Rr) for i in range(V)])
+            z = row.astype(np.float64) * float(s)
+            p = 2.0 ** (z - z.max())
+            tv = 0.5 * np.abs(w / w.sum() - p / p.sum()).sum()
+            assert tv < 1e-6, (t, spike, tv)
+
+
+def test_weight_rounding_is_unbiased():
+    """Entries far below their chunk's reference have small integer weights;
+    rounding them to the nearest integer (not down) leaves no systematic
+    bias: over many such entries the mean error against 2^(d + 29.5) is a
+    small fraction of a unit."""
+    rng = np.random.default_rng(13)
+    d = rng.uniform(-24.0, -14.0, 20000).astype(np.float32)
+    ideal = 2.0 ** (d.astype(np.float64) + 29.5)
+    err = np.array([oracle.fx_weight(x, 1.0, 0) for x in d]) - ideal
+    assert abs(err.mean()) < 0.02, err.mean()
+    assert (np.abs(err) <= 0.5 + ideal * 2.0 ** -21).all()
