@@ -29,6 +29,10 @@
 // results do not depend on the grid or on timing.  k_sample serves the
 // stateless entry point; k_sample_step, fused with the token commit, starts
 // streaming predicted rows before the proposal launch it depends on ends.
+// k_sample_fx and k_sample_step_fx are the same two on weights defined as
+// integers (clk_verify_sample_exact*, the section "Exact sampling" below),
+// whose decisions another implementation of the definition reproduces bit
+// for bit.
 #include <algorithm>
 #include <atomic>
 
